@@ -1,0 +1,164 @@
+"""Seeded synthetic inputs for the five workloads, on the CPU.
+
+This module only draws random numbers and encodes them into the library's input formats.  It
+holds none of the product's arithmetic (no decode, no product, no accumulation); the tests, the
+benchmark and the smoke check feed the same bytes to both the CUDA path and the CPU oracle.
+
+Workloads (all operands row-major, K contiguous, one UE8M0 scale per 32 elements along K):
+
+* ``mxfp8_small``   -- MXFP8 M=128 N=256 K=128, source values N(0,1).
+* ``f16_4096``      -- fp16 GEMM M=N=K=4096, A [M,K] and B [K,N] drawn N(0,1)/sqrt(K).
+* ``mxfp8_8192``    -- MXFP8 M=N=K=8192; each row of A and of B gets variance 10^U(-2,2).
+* ``w4a16_prefill`` -- fp16 A [4096,4096] N(0,1); int4 W [14336,4096] from N(0, 0.02^2).
+* ``w8_decode``     -- fp16 X [M,8192] N(0,1), M in {1,8,16}; int8 W [28672,8192] from N(0, 0.02^2).
+
+Encoding recipes (the pages only say "power-of-two block scales, 32 elements per block"; the
+per-format details below are the workload definitions):
+
+* MXFP8: per block X = floor(log2(amax)) - 8 (clamped to [-127, 127]), scale byte X + 127,
+  element = E4M3(round-to-nearest-even(v / 2^X)) with saturation to +-448.  An all-zero block
+  gets scale byte 127 and zero data.
+* intN (N = 4 or 8, qmax = 7 or 127): scale s = 2^ceil(log2(amax / qmax)), byte log2(s) + 127,
+  q = round-half-even(w / s) clamped to [-qmax-1, qmax].  int4 is packed two per byte, the even
+  k in the low nibble ("TensorOps: quantized matmul ...", section "VALIDATED ON M4 MAX", fact 5).
+
+The E4M3 rounding is done by PyTorch's float8_e4m3fn cast (round-to-nearest-even) after the
+saturating clamp; exponents come from ``torch.frexp`` so no ``log2`` rounding is involved.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+BLOCK = 32
+E4M3_MAX = 448.0
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal(shape, g: torch.Generator, std: float = 1.0) -> torch.Tensor:
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x
+
+
+def _block_amax(x: torch.Tensor) -> torch.Tensor:
+    rows, k = x.shape
+    if k % BLOCK:
+        raise ValueError("K must be a multiple of 32")
+    return x.abs().reshape(rows, k // BLOCK, BLOCK).amax(dim=2)
+
+
+def quantize_mxfp8(x: torch.Tensor):
+    """fp32 [rows, K] -> (E4M3 bytes uint8 [rows, K], UE8M0 bytes uint8 [rows, K/32])."""
+    x = x.to(torch.float32)
+    rows, k = x.shape
+    amax = _block_amax(x)
+    _, e = torch.frexp(amax)                       # amax = f * 2^e, f in [0.5, 1)
+    X = (e - 1 - 8).to(torch.int32)                # floor(log2(amax)) - 8
+    X = torch.where(amax > 0, X, torch.zeros_like(X)).clamp(-127, 127)
+    scale_bytes = (X + 127).to(torch.uint8)
+    xs = x.reshape(rows, k // BLOCK, BLOCK)
+    scaled = torch.ldexp(xs.to(torch.float64), (-X).to(torch.float64).unsqueeze(2))
+    scaled = scaled.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float32)
+    q = scaled.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, k)
+    return q.contiguous(), scale_bytes.contiguous()
+
+
+def quantize_int_blocks(w: torch.Tensor, qmax: int):
+    """fp32 [rows, K] -> (int8 values [rows, K] in [-qmax-1, qmax], UE8M0 bytes [rows, K/32])."""
+    w = w.to(torch.float64)
+    rows, k = w.shape
+    amax = _block_amax(w)
+    y = amax / qmax
+    f, e = torch.frexp(y)                          # y = f * 2^e
+    c = torch.where(f == 0.5, e - 1, e)            # ceil(log2(y)); exact powers of two stay
+    c = torch.where(amax > 0, c, torch.zeros_like(c)).clamp(-127, 127)
+    scale_bytes = (c + 127).to(torch.uint8)
+    ws = w.reshape(rows, k // BLOCK, BLOCK)
+    q = torch.round(torch.ldexp(ws, (-c).to(torch.float64).unsqueeze(2)))  # half to even
+    q = q.clamp(-qmax - 1, qmax).to(torch.int8).reshape(rows, k)
+    return q.contiguous(), scale_bytes.contiguous()
+
+
+def pack_int4(q: torch.Tensor) -> torch.Tensor:
+    """int8 values in [-8, 7], [rows, K] -> packed uint8 [rows, K/2], even k in the low nibble."""
+    rows, k = q.shape
+    if k % 2:
+        raise ValueError("K must be even for int4")
+    u = (q.to(torch.int16) & 0xF).to(torch.uint8).reshape(rows, k // 2, 2)
+    return (u[:, :, 0] | (u[:, :, 1] << 4)).contiguous()
+
+
+def log_uniform_row_std(rows: int, g: torch.Generator, lo_exp=-2.0, hi_exp=2.0) -> torch.Tensor:
+    """Per-row standard deviation sqrt(10^U(lo, hi))."""
+    u = torch.rand(rows, generator=g, dtype=torch.float64) * (hi_exp - lo_exp) + lo_exp
+    return torch.sqrt(torch.pow(10.0, u)).to(torch.float32)
+
+
+# ------------------------------------------------------------------------------ workloads
+WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode")
+
+
+def mxfp8_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
+    """MXFP8 operands: A [M,K], B [N,K] (E4M3 bytes) with UE8M0 scales [rows, K/32]."""
+    g = generator(seed)
+    if row_variance:
+        sa = log_uniform_row_std(M, g)
+        sb = log_uniform_row_std(N, g)
+        a = normal((M, K), g) * sa[:, None]
+        b = normal((N, K), g) * sb[:, None]
+    else:
+        a = normal((M, K), g)
+        b = normal((N, K), g)
+    qa, sa_b = quantize_mxfp8(a)
+    qb, sb_b = quantize_mxfp8(b)
+    return {"a": qa, "sa": sa_b, "b": qb, "sb": sb_b, "M": M, "N": N, "K": K}
+
+
+def f16_inputs(M: int, N: int, K: int, seed: int):
+    g = generator(seed)
+    s = 1.0 / math.sqrt(K)
+    a = (normal((M, K), g) * s).to(torch.float16)
+    b = (normal((K, N), g) * s).to(torch.float16)
+    return {"a": a.contiguous(), "b": b.contiguous(), "M": M, "N": N, "K": K}
+
+
+def w4a16_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
+    g = generator(seed)
+    a = normal((M, K), g).to(torch.float16)
+    w = normal((N, K), g, std=w_std)
+    q, s = quantize_int_blocks(w, 7)
+    return {"a": a.contiguous(), "w": pack_int4(q), "w_values": q, "sw": s,
+            "M": M, "N": N, "K": K}
+
+
+def w8_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
+    g = generator(seed)
+    x = normal((M, K), g).to(torch.float16)
+    w = normal((N, K), g, std=w_std)
+    q, s = quantize_int_blocks(w, 127)
+    return {"x": x.contiguous(), "w": q.view(torch.uint8).contiguous(), "sw": s,
+            "M": M, "N": N, "K": K}
+
+
+def workload(name: str, M: int | None = None):
+    """Full-size inputs of a named workload (seed = its position in ``WORKLOADS``)."""
+    seed = WORKLOADS.index(name)
+    if name == "mxfp8_small":
+        return mxfp8_inputs(128, 256, 128, seed)
+    if name == "f16_4096":
+        return f16_inputs(4096, 4096, 4096, seed)
+    if name == "mxfp8_8192":
+        return mxfp8_inputs(8192, 8192, 8192, seed, row_variance=True)
+    if name == "w4a16_prefill":
+        return w4a16_inputs(4096, 14336, 4096, seed)
+    if name == "w8_decode":
+        return w8_inputs(16 if M is None else M, 28672, 8192, seed)
+    raise KeyError(name)

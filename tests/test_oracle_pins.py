@@ -1,0 +1,240 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test ties one oracle function to a library routine, a closed form, an invariant or an exact
+rational brute force, so that a dropped term, a wrong sign, a swapped index or a transposed
+operand in the oracle fails at least one of them.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_quantized_tcgen05_gb300 import synth
+
+
+# ------------------------------------------------------------------------ decode tables
+def test_e4m3_table_matches_torch_float8(orc):
+    """All 256 E4M3 codes equal PyTorch's float8_e4m3fn -> fp64 conversion (OCP E4M3)."""
+    t = orc.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(t, ref, equal_nan=True)
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.isnan(t).sum() == 2          # one NaN pattern per sign, no infinity
+
+
+def test_e4m3_closed_form_points(orc):
+    """Largest finite 448 = 1.75 * 2^8, smallest subnormal 2^-9, smallest normal 2^-6, 1.0."""
+    t = orc.e4m3_table()
+    assert t[0x7E] == 448.0 and t[0xFE] == -448.0
+    assert t[0x01] == 2.0 ** -9 and t[0x08] == 2.0 ** -6 and t[0x38] == 1.0
+    assert t[0x00] == 0.0 and np.signbit(t[0x80])
+    finite = t[np.isfinite(t)]
+    pos = np.sort(finite[finite > 0])
+    assert pos.size == 126 and np.all(np.diff(pos) > 0)     # strictly monotone codes 1..126
+    assert np.array_equal(t[1:127], pos)
+
+
+def test_ue8m0_table_matches_torch_e8m0(orc):
+    """All 256 UE8M0 codes equal PyTorch's float8_e8m0fnu conversion: 2^(e-127), 0xFF NaN."""
+    u = orc.ue8m0_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.array_equal(u, ref, equal_nan=True)
+    assert u[127] == 1.0 and u[128] == 2.0 and u[0] == 2.0 ** -127 and np.isnan(u[255])
+    assert np.all(u[1:255] == 2.0 * u[0:254])
+
+
+# ----------------------------------------------------------------------- fp16 rounding
+def test_f16_rn_matches_numpy(orc):
+    """fp64 -> binary16 round-to-nearest-even agrees with numpy's float16 cast, including
+    exact ties, the subnormal range and the overflow threshold."""
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000),
+        (np.arange(-3000, 3000) + 0.5) * 2.0 ** -24,           # subnormal ties
+        (1024 + np.arange(0, 2048) + 0.5) * 2.0 ** -10,        # ties in [1, 3)
+        np.array([65504.0, 65519.999, 65520.0, 65536.0, -65520.0, 1e9, 0.0, -0.0,
+                  2.0 ** -25, 2.0 ** -25 * 1.0000001, 2.0 ** -14 - 2.0 ** -30]),
+    ])
+    got = orc.f16_rn(x)
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_f16_decode_all_codes(orc):
+    codes = np.arange(65536, dtype=np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    got = np.array([orc.f16_value(int(c)) for c in codes[::7]])
+    assert np.array_equal(got, ref[::7], equal_nan=True)
+
+
+# ----------------------------------------------------------------------- integer planes
+def test_int4_nibble_order_follows_page_rule(orc):
+    """Packing per the page's rule byte = (v[2i] & 0xF) | ((v[2i+1] & 0xF) << 4) decodes back to
+    the two's-complement values, even index from the low nibble."""
+    vals = list(range(-8, 8)) + [7, -8, 0, 1, -1, 3]
+    packed = np.array([(vals[2 * i] & 0xF) | ((vals[2 * i + 1] & 0xF) << 4)
+                       for i in range(len(vals) // 2)], np.uint8)
+    got = [orc.int4_get(packed, k) for k in range(len(vals))]
+    assert got == vals
+    q = torch.tensor([vals], dtype=torch.int8)
+    assert np.array_equal(synth.pack_int4(q).numpy()[0], packed)
+
+
+def test_int8_dequant_is_twos_complement(orc):
+    data = np.arange(256, dtype=np.uint8).reshape(8, 32)
+    sc = np.full((8, 1), 127, np.uint8)
+    got = orc.dequant(orc.INT8, data, sc)
+    assert np.array_equal(got.ravel(), data.view(np.int8).astype(np.float64).ravel())
+
+
+def test_scale_maps_to_block_of_32_along_k(orc):
+    """Element (r, k) takes scale S[r, k // 32]: a distinct scale per (row, block) shows it."""
+    rows, K = 3, 128
+    data = np.full((rows, K), 0x38, np.uint8)               # E4M3 1.0 everywhere
+    sc = (np.arange(rows * (K // 32), dtype=np.uint8).reshape(rows, K // 32) + 120)
+    got = orc.dequant(orc.E4M3, data, sc)
+    want = np.repeat(2.0 ** (sc.astype(np.float64) - 127), 32, axis=1)
+    assert np.array_equal(got, want)
+
+
+# -------------------------------------------------------------------------- products
+def _rand_e4m3(rng, shape):
+    b = rng.integers(0, 256, shape, dtype=np.uint8)
+    b[(b & 0x7F) == 0x7F] = 0x3C                          # no NaN codes
+    return b
+
+
+def _torch_dequant_e4m3(b, s):
+    v = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    sc = torch.from_numpy(s).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    return v * np.repeat(sc, 32, axis=1)
+
+
+def test_mxfp8_brute_force_exact_rationals(orc):
+    """Tiny shapes: the oracle equals sum of exact rational products within fp64 rounding."""
+    rng = np.random.default_rng(1)
+    for (M, N, K) in [(1, 1, 32), (3, 2, 64), (4, 4, 64), (2, 3, 32)]:
+        a = _rand_e4m3(rng, (M, K))
+        b = _rand_e4m3(rng, (N, K))
+        sa = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+        sb = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+        res = orc.mxfp8(a, sa, b, sb)
+        A = _torch_dequant_e4m3(a, sa)
+        B = _torch_dequant_e4m3(b, sb)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(Fraction(A[m, k]) * Fraction(B[n, k]) for k in range(K))
+                mag = sum(abs(Fraction(A[m, k]) * Fraction(B[n, k])) for k in range(K))
+                assert abs(Fraction(res.C[m, n]) - exact) <= Fraction(2.0 ** -50) * mag
+                assert Fraction(res.D[m, n]) == pytest.approx(float(mag), rel=1e-14)
+                f16 = np.float16(float(exact)).view(np.uint16)
+                assert res.f16_bits[m, n] == f16 or abs(float(exact)) < 2.0 ** -20
+
+
+def test_mxfp8_matches_library_matmul(orc):
+    """Library special case: fp64 matmul of torch-decoded operands, non-square, 1e-12 of D."""
+    rng = np.random.default_rng(2)
+    M, N, K = 48, 80, 256
+    a = _rand_e4m3(rng, (M, K))
+    b = _rand_e4m3(rng, (N, K))
+    sa = rng.integers(100, 150, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(100, 150, (N, K // 32), dtype=np.uint8)
+    res = orc.mxfp8(a, sa, b, sb)
+    A = _torch_dequant_e4m3(a, sa)
+    B = _torch_dequant_e4m3(b, sb)
+    C = A @ B.T
+    D = np.abs(A) @ np.abs(B).T
+    assert np.all(np.abs(res.C - C) <= 1e-12 * D)
+    assert np.allclose(res.D, D, rtol=1e-12)
+    rows = np.array([5, 0, 47, 13])
+    sub = orc.mxfp8(a, sa, b, sb, rows=rows)
+    assert np.array_equal(sub.C, res.C[rows])
+
+
+def test_mxfp8_invariants(orc):
+    """Doubling every A scale doubles C exactly; identity and one-hot-K give closed forms."""
+    rng = np.random.default_rng(3)
+    M, N, K = 32, 40, 128
+    a = _rand_e4m3(rng, (M, K))
+    b = _rand_e4m3(rng, (N, K))
+    sa = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+    base = orc.mxfp8(a, sa, b, sb)
+    dbl = orc.mxfp8(a, sa + 1, b, sb)
+    assert np.array_equal(dbl.C, 2.0 * base.C)
+    # identity: A = I (E4M3 1.0 on the diagonal, scale 2^0), K = N
+    Kq = N = 64
+    b2 = _rand_e4m3(rng, (N, Kq))
+    sb2 = rng.integers(120, 135, (N, Kq // 32), dtype=np.uint8)
+    eye = np.zeros((Kq, Kq), np.uint8)
+    eye[np.arange(Kq), np.arange(Kq)] = 0x38
+    res = orc.mxfp8(eye, np.full((Kq, Kq // 32), 127, np.uint8), b2, sb2)
+    assert np.array_equal(res.C, _torch_dequant_e4m3(b2, sb2).T)
+    # one-hot K: only k = 37 is non-zero in A, so C[m, n] = a[m,37] * b[n,37]
+    a3 = np.zeros((M, K), np.uint8)
+    a3[:, 37] = _rand_e4m3(rng, (M,))
+    res3 = orc.mxfp8(a3, sa, b, sb)
+    A3 = _torch_dequant_e4m3(a3, sa)
+    B = _torch_dequant_e4m3(b, sb)
+    assert np.array_equal(res3.C, np.outer(A3[:, 37], B[:, 37]))
+
+
+def test_gemm_f16_matches_library_and_orientation(orc):
+    """fp16 A [M,K] @ B [K,N]: equals numpy fp64 matmul; a transposed B would fail."""
+    rng = np.random.default_rng(4)
+    M, N, K = 24, 40, 72
+    a = (rng.standard_normal((M, K))).astype(np.float16)
+    b = (rng.standard_normal((K, N))).astype(np.float16)
+    res = orc.gemm_f16(a, b)
+    C = a.astype(np.float64) @ b.astype(np.float64)
+    D = np.abs(a.astype(np.float64)) @ np.abs(b.astype(np.float64))
+    assert res.C.shape == (M, N)
+    assert np.all(np.abs(res.C - C) <= 1e-13 * D)
+    assert np.array_equal(res.f16_bits, C.astype(np.float16).view(np.uint16)) or \
+        np.mean(res.f16_bits == C.astype(np.float16).view(np.uint16)) > 0.99
+
+
+def test_w4a16_matches_unpacked_values(orc):
+    """Oracle on packed int4 equals fp64 matmul over the unpacked ints times 2^(s-127)."""
+    M, N, K = 16, 48, 128
+    d = synth.w4a16_inputs(M, N, K, seed=11)
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    q = d["w_values"].numpy().astype(np.float64)
+    s = 2.0 ** (d["sw"].numpy().astype(np.float64) - 127)
+    W = q * np.repeat(s, 32, axis=1)
+    A = d["a"].numpy().astype(np.float64)
+    C = A @ W.T
+    D = np.abs(A) @ np.abs(W).T
+    assert np.all(np.abs(res.C - C) <= 1e-13 * D)
+
+
+def test_w8_gemv_matches_library(orc):
+    M, N, K = 5, 96, 256
+    d = synth.w8_inputs(M, N, K, seed=12)
+    res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    q = d["w"].numpy().view(np.int8).astype(np.float64)
+    s = 2.0 ** (d["sw"].numpy().astype(np.float64) - 127)
+    W = q * np.repeat(s, 32, axis=1)
+    X = d["x"].numpy().astype(np.float64)
+    C = X @ W.T
+    D = np.abs(X) @ np.abs(W).T
+    assert np.all(np.abs(res.C - C) <= 1e-13 * D)
+    assert np.allclose(res.D, D, rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------- tolerance
+def test_tolerance_check_catches_planted_error(orc):
+    """The element-wise check rejects a single wrong element and accepts fp16 rounding."""
+    rng = np.random.default_rng(5)
+    a = _rand_e4m3(rng, (16, 64))
+    b = _rand_e4m3(rng, (32, 64))
+    sa = np.full((16, 2), 124, np.uint8)
+    sb = np.full((32, 2), 124, np.uint8)
+    res = orc.mxfp8(a, sa, b, sb)
+    ok, _, _ = orc.within_tolerance(res.f16.astype(np.float32), res)
+    assert ok
+    bad = res.f16.astype(np.float32).copy()
+    bad[3, 7] += 0.01 * res.D[3, 7] + 1e-3
+    ok, _, info = orc.within_tolerance(bad, res)
+    assert not ok and info["n_bad"] == 1
