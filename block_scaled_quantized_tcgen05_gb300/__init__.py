@@ -1,0 +1,222 @@
+"""Python binding of the block-scaled quantized GEMM library (``libqgemm.so``, C ABI).
+
+Argument marshalling only: every function here passes torch tensors' device pointers, strides
+and the current CUDA stream to the C entry point of the same name and raises ``QGemmError`` on a
+non-OK status.  All arithmetic runs in the library's CUDA kernels; there is no CPU fallback, and
+loading fails loudly when the library has not been built (``python -m
+block_scaled_quantized_tcgen05_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "load_library", "library_path",
+    "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
+    "qgemm_mxfp8", "gemm_f16", "qgemm_w4a16", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
+    "qgemm_selftest_wait_timeout",
+]
+
+F16, E4M3, INT8, INT4 = 0, 1, 2, 3
+OK = 0
+STATUS_NAMES = {0: "QGEMM_OK", 1: "QGEMM_ERR_INVALID_ARG", 2: "QGEMM_ERR_UNSUPPORTED_SHAPE",
+                3: "QGEMM_ERR_MISALIGNED", 4: "QGEMM_ERR_UNSUPPORTED_DTYPE", 5: "QGEMM_ERR_CUDA",
+                6: "QGEMM_ERR_TIMEOUT"}
+
+_lib = None
+
+
+class QGemmError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{where}: {self.name}: {message}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libqgemm.so (built in-tree).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"libqgemm.so not built at {path}; run "
+                          "`python -m block_scaled_quantized_tcgen05_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I64, I32, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
+    S = ctypes.c_int
+    sig = {
+        "qgemm_version": (I32, []),
+        "qgemm_create_tensor": (S, [ctypes.POINTER(P), S, I64, I64, P, I64, P, I64, I32]),
+        "qgemm_tensor_slice": (S, [P, I64, I64, I64, I64, ctypes.POINTER(P)]),
+        "qgemm_destroy_tensor": (None, [P]),
+        "qgemm_tensor_info": (S, [P, ctypes.POINTER(I32), ctypes.POINTER(I64),
+                                  ctypes.POINTER(I64), ctypes.POINTER(P), ctypes.POINTER(I64),
+                                  ctypes.POINTER(P), ctypes.POINTER(I64)]),
+        "qgemm_mxfp8": (S, [P, P, P, I64, P]),
+        "gemm_f16": (S, [P, I64, P, I64, P, I64, I64, I64, I64, P]),
+        "qgemm_w4a16": (S, [P, I64, I64, P, P, I64, P]),
+        "qgemm_w8_gemv": (S, [P, I64, I64, P, P, I64, P]),
+        "qgemm_dequant_debug": (S, [P, P, P]),
+        "qgemm_status_string": (ctypes.c_char_p, [S]),
+        "qgemm_last_error_message": (ctypes.c_char_p, []),
+        "qgemm_poll_device_error": (S, [P, ctypes.POINTER(ctypes.c_uint32)]),
+        "qgemm_set_wait_timeout_ns": (None, [U64]),
+        "qgemm_selftest_wait_timeout": (S, [U64, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        msg = load_library().qgemm_last_error_message().decode(errors="replace")
+        raise QGemmError(status, where, msg)
+
+
+def _stream(stream):
+    """cudaStream_t of a torch.cuda.Stream (default: torch's current stream)."""
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _row_stride_bytes(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.stride(1) != 1:
+        raise ValueError("inner dimension must be contiguous")
+    return t.stride(0) * t.element_size()
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major tensor with a contiguous inner dimension")
+    return t.stride(0)
+
+
+class QTensor:
+    """Owning Python handle of a qgemm_tensor view; keeps the borrowed torch tensors alive."""
+
+    def __init__(self, handle: int, dtype: int, rows: int, k: int, refs):
+        self.handle = ctypes.c_void_p(handle)
+        self.dtype, self.rows, self.k = dtype, rows, k
+        self._refs = refs
+
+    def close(self):
+        if self.handle and self.handle.value:
+            load_library().qgemm_destroy_tensor(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def qgemm_version() -> int:
+    return load_library().qgemm_version()
+
+
+def qgemm_status_string(status: int) -> str:
+    return load_library().qgemm_status_string(status).decode()
+
+
+def qgemm_create_tensor(dtype: int, data, scales=None, rows: int | None = None,
+                        k: int | None = None, block_k: int = 32) -> QTensor:
+    """View of a [rows, k] quantized matrix.  ``data`` is a 2-D device tensor holding the data
+    plane row-major (uint8 for E4M3 / INT8 / packed INT4, fp16 for F16); ``scales`` is the
+    [rows, k/32] uint8 UE8M0 plane (None for F16)."""
+    lib = load_library()
+    rows = data.shape[0] if rows is None else rows
+    if k is None:
+        k = {F16: data.shape[1], E4M3: data.shape[1], INT8: data.shape[1],
+             INT4: 2 * data.shape[1]}[dtype]
+    out = ctypes.c_void_p()
+    st = lib.qgemm_create_tensor(ctypes.byref(out), dtype, rows, k, _ptr(data),
+                                 _row_stride_bytes(data), _ptr(scales),
+                                 _row_stride_bytes(scales) if scales is not None else 0, block_k)
+    _check(st, "qgemm_create_tensor")
+    return QTensor(out.value, dtype, rows, k, (data, scales))
+
+
+def qgemm_tensor_slice(t: QTensor, row0: int, nrows: int, k0: int, nk: int) -> QTensor:
+    lib = load_library()
+    out = ctypes.c_void_p()
+    _check(lib.qgemm_tensor_slice(t.handle, row0, nrows, k0, nk, ctypes.byref(out)),
+           "qgemm_tensor_slice")
+    return QTensor(out.value, t.dtype, nrows, nk, t._refs)
+
+
+def qgemm_destroy_tensor(t: QTensor):
+    t.close()
+
+
+def qgemm_mxfp8(A: QTensor, B: QTensor, C, stream=None):
+    _check(load_library().qgemm_mxfp8(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
+           "qgemm_mxfp8")
+    return C
+
+
+def gemm_f16(A, B, C, stream=None):
+    M, K = A.shape
+    N = B.shape[1]
+    _check(load_library().gemm_f16(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), M, N, K,
+                                   _stream(stream)), "gemm_f16")
+    return C
+
+
+def qgemm_w4a16(A, W: QTensor, C, stream=None):
+    _check(load_library().qgemm_w4a16(_ptr(A), _ld(A), A.shape[0], W.handle, _ptr(C), _ld(C),
+                                      _stream(stream)), "qgemm_w4a16")
+    return C
+
+
+def qgemm_w8_gemv(X, W: QTensor, Y, stream=None):
+    _check(load_library().qgemm_w8_gemv(_ptr(X), _ld(X), X.shape[0], W.handle, _ptr(Y), _ld(Y),
+                                        _stream(stream)), "qgemm_w8_gemv")
+    return Y
+
+
+def qgemm_dequant_debug(t: QTensor, out, stream=None):
+    _check(load_library().qgemm_dequant_debug(t.handle, _ptr(out), _stream(stream)),
+           "qgemm_dequant_debug")
+    return out
+
+
+def qgemm_poll_device_error(stream=None) -> int:
+    """Synchronise and return (and clear) the device error word; 0 when no wait gave up."""
+    code = ctypes.c_uint32(0)
+    st = load_library().qgemm_poll_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (OK, 6):
+        _check(st, "qgemm_poll_device_error")
+    return code.value
+
+
+def qgemm_set_wait_timeout_ns(ns: int):
+    load_library().qgemm_set_wait_timeout_ns(int(ns))
+
+
+def qgemm_selftest_wait_timeout(timeout_ns: int, stream=None):
+    _check(load_library().qgemm_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
+           "qgemm_selftest_wait_timeout")

@@ -1,0 +1,238 @@
+// f16_gemm.cu -- fp16 GEMM on tcgen05 (kind::f16, fp32 accumulation in TMEM, fp16 output).
+//
+// C[M, N] = fp16_rn(A[M, K] @ B[K, N]); A row-major (K-major operand), B row-major [K, N]
+// (N contiguous: an MN-major operand).  The unquantized half x half -> half matmul of
+// "TensorOps: quantized matmul ..." (kernel M0 of "VALIDATED ON M4 MAX") and of the TileLang
+// page's fast path (fp16 in, fp32 accumulate, cast to fp16 on store), on GB300's pipeline:
+//   warp 0     producer: per 64-wide k-tile one TMA box of A (128 rows x 128 B) and BN/64
+//              boxes of B (64 k-rows x 64 n = 128 B), all with the 128-byte swizzle.
+//   warp 1     TMEM owner + MMA issuer: four 128 x BN x 16 MMAs per k-tile; B is described
+//              as MN-major (64-element swizzle atoms BN/64 apart, 8-row k groups 1 KB apart).
+//   warps 2-5  epilogue: TMEM -> fp16 -> global, masked at the M / N edges.
+#include "qgemm_common.cuh"
+#include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
+
+namespace {
+
+using namespace qg;
+
+constexpr int BM = 128;
+constexpr int BK = 64;         // fp16 elements of K per k-tile (one 128-byte swizzle row)
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;      // 16 KB
+    static constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2; // 64 k-rows x 64 n = 8 KB
+    static constexpr uint32_t B_BYTES = (BN / 64) * B_ATOM_BYTES;
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+};
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (format 0),
+// A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t f16_idesc(int n) {
+    return (1u << 4) | (1u << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                __half *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned *err,
+                uint64_t timeout_ns) {
+    using G = Cfg<BN>;
+    constexpr int S = G::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sb + G::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + G::OFF_BAR + 8u * (S + s); };
+    const uint32_t tmem_full = sb + G::OFF_BAR + 8u * (2 * S);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_SLOT);
+
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        uint32_t stage = 0, phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t sA = sb + G::OFF_A + stage * G::A_BYTES;
+                    const uint32_t sB = sb + G::OFF_B + stage * G::B_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), G::A_BYTES + G::B_BYTES);
+                    tma_load_2d(sA, &tmA, full_bar(stage), kt * BK, mb * BM);
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_2d(sB + c * G::B_ATOM_BYTES, &tmB, full_bar(stage),
+                                    nb * BN + 64 * c, kt * BK);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+        for (int i = max(0, issued - S); i < issued; ++i) {
+            if (!mbar_wait(full_bar(i % S), (i / S) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1) {
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        const uint32_t idesc = f16_idesc(BN);
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t adesc =
+                        smem_desc(sb + G::OFF_A + stage * G::A_BYTES, 16, 1024, SWZ_128B);
+                    // MN-major B: LBO = stride between 64-wide N atoms, SBO = 8 k-rows.
+                    const uint64_t bdesc = smem_desc(sb + G::OFF_B + stage * G::B_BYTES,
+                                                     G::B_ATOM_BYTES, 1024, SWZ_128B);
+#pragma unroll
+                    for (uint32_t j = 0; j < BK / 16; ++j) {
+                        // A: 16 halves = 32 bytes along the swizzle row; B: 16 k-rows = 2 KB
+                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 128 * j, idesc,
+                                (kt > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(tmem_full);
+            __syncwarp();
+            acc_phase ^= 1;
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
+        if (lane == 0) tc_commit(drain_bar);
+        __syncwarp();
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else {
+        const uint32_t q = warp & 3;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int row = mb * BM + static_cast<int>(q * 32 + lane);
+            __half *crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+                tmem_wait_ld();
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int BN>
+cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb, __half *C,
+                      int64_t ldc, int M, int N, int K, const qgi::LaunchCtx &ctx,
+                      bool *encode_ok) {
+    using G = Cfg<BN>;
+    CUtensorMap tmA, tmB;
+    *encode_ok = qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
+                                    BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, ldb * 2, 64,
+                                    BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    auto kern = gemm_f16_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, M, N, K, ctx.err,
+                                                        ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace qgi {
+
+cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64_t ldb,
+                            __half *C, int64_t ldc, int M, int N, int K, const LaunchCtx &ctx,
+                            bool *encode_ok) {
+    if (N > 128) return launch_bn<256>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
+    return launch_bn<128>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
+}
+
+}  // namespace qgi

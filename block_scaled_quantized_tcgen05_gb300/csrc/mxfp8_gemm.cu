@@ -1,0 +1,291 @@
+// mxfp8_gemm.cu -- block-scaled FP8 (E4M3 data, UE8M0 scale per 32 along K) GEMM on tcgen05.
+//
+// C[M, N] = fp16_rn( sum_k e4m3(A[m,k]) 2^(SA[m,k/32]-127) * e4m3(B[n,k]) 2^(SB[n,k/32]-127) )
+//
+// The quantized matmul2d of "Optimize custom machine learning operations with Metal tensors"
+// (sections "Shader MXFP8 tensor types", "Slicing and quantized matmul") re-designed for
+// sm_103a: the tensor core consumes the E4M3 planes and the UE8M0 planes directly
+// (tcgen05.mma kind::mxf8f6f4 with block_scale), so no dequantised copy ever exists.
+//
+// One persistent CTA per SM walks output tiles of 128 x BN.  Warp roles:
+//   warp 0     producer: TMA loads of the A / B k-tiles (128 B of K per row, 128-byte swizzle)
+//              and cp.async loads of their scale bytes, rearranged on the fly into the
+//              32-row x 16-byte layout that tcgen05.cp.32x128b.warpx4 expects.
+//   warp 1     TMEM owner and MMA issuer: per k-tile it copies the scale bytes into TMEM,
+//              then issues four 128 x BN x 32 block-scaled MMAs (scale-factor id = K step).
+//   warps 2-5  epilogue: TMEM -> registers -> fp16 (round to nearest even) -> global.
+// Stages are handed over with mbarriers (full: TMA bytes + 32 cp.async arrivals; empty:
+// tcgen05.commit).  Every wait is bounded by the caller's timeout.
+#include "qgemm_common.cuh"
+#include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
+
+namespace {
+
+using namespace qg;
+
+constexpr int BM = 128;
+constexpr int BK = 128;                     // E4M3 elements (= bytes) per k-tile
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_COL0 = 256;           // TMEM column of the first scale-factor slot
+constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA: 4 columns, SFB: 4 per 128 rows of B
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK;
+    static constexpr uint32_t B_BYTES = BN * BK;
+    static constexpr uint32_t SFA_BYTES = BM * 4;
+    static constexpr uint32_t SFB_BYTES = BN * 4;
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    // full[S], empty[S], tmem_full, tmem_empty, drain, then the TMEM address slot
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+    static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(BN <= 256 && BN % 128 == 0, "BN");
+};
+
+// Instruction descriptor, kind::mxf8f6f4: A, B E4M3 (format 0), K-major, D fp32 (implicit),
+// N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 7 at bit 27.  The K-step selects which
+// byte of each 32-bit TMEM scale word is used: A's id at bits 29-30, B's at bits 4-5.
+__host__ __device__ constexpr uint32_t mx_idesc(int n) {
+    return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(BM >> 7) << 27);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const uint8_t *__restrict__ sfa, int64_t lds_a, const uint8_t *__restrict__ sfb,
+                  int64_t lds_b, __half *__restrict__ C, int64_t ldc, int M, int N, int K,
+                  unsigned *err, uint64_t timeout_ns) {
+    using G = Cfg<BN>;
+    constexpr int S = G::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sb + G::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + G::OFF_BAR + 8u * (S + s); };
+    const uint32_t tmem_full = sb + G::OFF_BAR + 8u * (2 * S);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_SLOT);
+
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = (K + BK - 1) / BK;
+    const int nkb = K / 32;  // scale blocks per row
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1 + 32);  // producer's expect_tx arrival + 32 cp.async arrivals
+            mbar_init(empty_bar(s), 1);      // tcgen05.commit
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);          // every epilogue thread
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        uint32_t stage = 0, phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            const int m0 = mb * BM, n0 = nb * BN;
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sA = sb + G::OFF_A + stage * G::A_BYTES;
+                const uint32_t sB = sb + G::OFF_B + stage * G::B_BYTES;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(stage), G::A_BYTES + G::B_BYTES);
+                    tma_load_2d(sA, &tmA, full_bar(stage), kt * BK, m0);
+                    tma_load_2d(sB, &tmB, full_bar(stage), kt * BK, n0);
+                }
+                // Scale bytes: row r's 4 bytes for this k-tile go to word (r / 32) of 16-byte
+                // line (r % 32) of its 128-row group.
+                const int kb0 = kt * 4;
+                const uint32_t nbytes = static_cast<uint32_t>(min(4, nkb - kb0));
+                const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
+                const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int r = m0 + 32 * c + static_cast<int>(lane);
+                    const bool v = r < M;
+                    const uint8_t *src = v ? sfa + static_cast<int64_t>(r) * lds_a + kb0 : sfa;
+                    cp_async_4(sSFA + lane * 16 + c * 4, src, v ? nbytes : 0u);
+                }
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
+                        const bool v = r < N;
+                        const uint8_t *src = v ? sfb + static_cast<int64_t>(r) * lds_b + kb0 : sfb;
+                        cp_async_4(sSFB + h * 512 + lane * 16 + c * 4, src, v ? nbytes : 0u);
+                    }
+                }
+                cp_async_arrive_noinc(full_bar(stage));
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+        // Drain: every load this warp issued has landed before the CTA may exit.
+        for (int i = max(0, issued - S); i < issued; ++i) {
+            if (!mbar_wait(full_bar(i % S), (i / S) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        const uint32_t idesc = mx_idesc(BN);
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.cp reads
+                    const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
+                    const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
+                    const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
+                    tc_cp_32x128b_warpx4(sf_col, smem_desc(sSFA, 0, 128, SWZ_NONE));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        tc_cp_32x128b_warpx4(sf_col + 4 + 4 * h,
+                                             smem_desc(sSFB + h * 512, 0, 128, SWZ_NONE));
+                    const uint64_t adesc =
+                        smem_desc(sb + G::OFF_A + stage * G::A_BYTES, 16, 1024, SWZ_128B);
+                    const uint64_t bdesc =
+                        smem_desc(sb + G::OFF_B + stage * G::B_BYTES, 16, 1024, SWZ_128B);
+#pragma unroll
+                    for (uint32_t j = 0; j < BK / 32; ++j) {
+                        // advance 32 bytes of K inside the 128-byte swizzle row
+                        mma_mxf8(tmem_base, adesc + 2 * j, bdesc + 2 * j,
+                                 idesc | (j << 4) | (j << 29), sf_col, sf_col + 4,
+                                 (kt > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(tmem_full);
+            __syncwarp();
+            acc_phase ^= 1;
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
+        // Drain: all MMAs and TMEM copies of this CTA have completed before TMEM is freed.
+        if (lane == 0) tc_commit(drain_bar);
+        __syncwarp();
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const uint32_t q = warp & 3;  // TMEM lane quarter this warp may read
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int row = mb * BM + static_cast<int>(q * 32 + lane);
+            __half *crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+                tmem_wait_ld();
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int BN>
+cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                      const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    using G = Cfg<BN>;
+    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
+              K = static_cast<int>(A->k);
+    CUtensorMap tmA, tmB;
+    *encode_ok = qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, K, M, A->ld, BK,
+                                    BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, K, N, B->ld, BK,
+                                    BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    auto kern = mxfp8_gemm_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, A->scales, A->lds, B->scales,
+                                                        B->lds, C, ldc, M, N, K, ctx.err,
+                                                        ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace qgi {
+
+cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                         const LaunchCtx &ctx, bool *encode_ok) {
+    if (B->rows > 128) return launch_bn<256>(A, B, C, ldc, ctx, encode_ok);
+    return launch_bn<128>(A, B, C, ldc, ctx, encode_ok);
+}
+
+}  // namespace qgi

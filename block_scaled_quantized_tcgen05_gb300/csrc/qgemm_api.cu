@@ -1,0 +1,407 @@
+// qgemm_api.cu -- the C ABI: argument validation, tensor views, TMA descriptor encoding, the
+// device error word and status strings.  Kernels live in the other translation units.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <new>
+
+#include "qgemm.h"
+#include "qgemm_internal.h"
+
+namespace {
+
+// Device error word: a kernel whose bounded wait ran out sets a bit here.  Host code reaches it
+// only through the address returned by cudaGetSymbolAddress on the current device.
+__device__ unsigned int g_device_error_word;
+
+thread_local char g_last_msg[512] = "";
+
+uint64_t g_timeout_ns = 4000000000ull;
+
+constexpr int MAX_DEVICES = 64;
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned *err = nullptr;
+};
+DeviceInfo g_dev[MAX_DEVICES];
+std::mutex g_dev_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+qgemm_status cuda_fail(cudaError_t e, const char *what) {
+    return qgi::fail(QGEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+                     cudaGetErrorString(e));
+}
+
+// Per-device set-up on the current device: SM count and the address of the error word.
+qgemm_status get_ctx(void *stream, qgi::LaunchCtx *ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES) return qgi::fail(QGEMM_ERR_CUDA, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        d.err = static_cast<unsigned *>(p);
+        d.ready = true;
+    }
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    ctx->err = d.err;
+    ctx->timeout_ns = g_timeout_ns;
+    ctx->num_sms = d.num_sms;
+    ctx->device = dev;
+    return QGEMM_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t elem_bits(int32_t dt) {
+    switch (dt) {
+    case QGEMM_F16: return 16;
+    case QGEMM_E4M3:
+    case QGEMM_INT8: return 8;
+    case QGEMM_INT4: return 4;
+    default: return 0;
+    }
+}
+
+constexpr int64_t MAX_DIM = (int64_t(1) << 31) - 1;
+
+}  // namespace
+
+namespace qgi {
+
+qgemm_status fail(qgemm_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_msg, sizeof(g_last_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                   uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                   uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) {
+        fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu stride %llu",
+             static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
+             (unsigned long long)row_stride_bytes);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace qgi
+
+using qgi::fail;
+
+extern "C" {
+
+int32_t qgemm_version(void) { return (1 << 16) | 0; }
+
+const char *qgemm_status_string(qgemm_status s) {
+    switch (s) {
+    case QGEMM_OK: return "QGEMM_OK";
+    case QGEMM_ERR_INVALID_ARG: return "QGEMM_ERR_INVALID_ARG";
+    case QGEMM_ERR_UNSUPPORTED_SHAPE: return "QGEMM_ERR_UNSUPPORTED_SHAPE";
+    case QGEMM_ERR_MISALIGNED: return "QGEMM_ERR_MISALIGNED";
+    case QGEMM_ERR_UNSUPPORTED_DTYPE: return "QGEMM_ERR_UNSUPPORTED_DTYPE";
+    case QGEMM_ERR_CUDA: return "QGEMM_ERR_CUDA";
+    case QGEMM_ERR_TIMEOUT: return "QGEMM_ERR_TIMEOUT";
+    }
+    return "QGEMM_ERR_UNKNOWN";
+}
+
+const char *qgemm_last_error_message(void) { return g_last_msg; }
+
+void qgemm_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns < 1000000ull ? 1000000ull : ns; }
+
+qgemm_status qgemm_create_tensor(qgemm_tensor **out, qgemm_dtype dt, int64_t rows, int64_t k,
+                                 const void *data, int64_t data_row_stride_bytes,
+                                 const uint8_t *scales_ue8m0, int64_t scale_row_stride_bytes,
+                                 int32_t block_k) {
+    if (!out) return fail(QGEMM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    const int64_t bits = elem_bits(dt);
+    if (bits == 0) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "unknown dtype %d", (int)dt);
+    if (rows < 0 || k < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative shape");
+    if (rows > MAX_DIM || k > MAX_DIM) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    if (!data && rows * k > 0) return fail(QGEMM_ERR_INVALID_ARG, "data is NULL");
+    const int64_t row_bytes = (k * bits + 7) / 8;
+    if (rows > 1 && data_row_stride_bytes < row_bytes)
+        return fail(QGEMM_ERR_INVALID_ARG, "data row stride %lld < row size %lld",
+                    (long long)data_row_stride_bytes, (long long)row_bytes);
+    if (data_row_stride_bytes < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative data stride");
+    if (dt == QGEMM_F16) {
+        if (scales_ue8m0) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "F16 takes no scale plane");
+    } else {
+        if (block_k != 32)
+            return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "block_k must be 32 (got %d)", block_k);
+        if (k % 32) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "k %% 32 != 0 (k = %lld)", (long long)k);
+        if (!scales_ue8m0 && rows * k > 0) return fail(QGEMM_ERR_INVALID_ARG, "scales is NULL");
+        if (scale_row_stride_bytes < 0 || (rows > 1 && scale_row_stride_bytes < k / 32))
+            return fail(QGEMM_ERR_INVALID_ARG, "scale row stride %lld < k/32",
+                        (long long)scale_row_stride_bytes);
+    }
+    qgemm_tensor *t = new (std::nothrow) qgemm_tensor;
+    if (!t) return fail(QGEMM_ERR_INVALID_ARG, "out of host memory");
+    t->dtype = dt;
+    t->rows = rows;
+    t->k = k;
+    t->data = static_cast<const uint8_t *>(data);
+    t->ld = data_row_stride_bytes;
+    t->scales = scales_ue8m0;
+    t->lds = scale_row_stride_bytes;
+    *out = t;
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_tensor_slice(const qgemm_tensor *t, int64_t row0, int64_t nrows, int64_t k0,
+                                int64_t nk, qgemm_tensor **out) {
+    if (!out) return fail(QGEMM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!t) return fail(QGEMM_ERR_INVALID_ARG, "tensor is NULL");
+    if (row0 < 0 || nrows < 0 || k0 < 0 || nk < 0 || row0 + nrows > t->rows || k0 + nk > t->k)
+        return fail(QGEMM_ERR_INVALID_ARG, "slice out of range");
+    if (t->dtype != QGEMM_F16 && (k0 % 32 || nk % 32))
+        return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "k0 and nk must be multiples of 32");
+    qgemm_tensor *s = new (std::nothrow) qgemm_tensor(*t);
+    if (!s) return fail(QGEMM_ERR_INVALID_ARG, "out of host memory");
+    const int64_t bits = elem_bits(t->dtype);
+    s->rows = nrows;
+    s->k = nk;
+    s->data = t->data + row0 * t->ld + (k0 * bits) / 8;
+    if (t->scales) s->scales = t->scales + row0 * t->lds + k0 / 32;
+    *out = s;
+    return QGEMM_OK;
+}
+
+void qgemm_destroy_tensor(qgemm_tensor *t) { delete t; }
+
+qgemm_status qgemm_tensor_info(const qgemm_tensor *t, int32_t *dtype, int64_t *rows, int64_t *k,
+                               const void **data, int64_t *data_row_stride_bytes,
+                               const uint8_t **scales, int64_t *scale_row_stride_bytes) {
+    if (!t) return fail(QGEMM_ERR_INVALID_ARG, "tensor is NULL");
+    if (dtype) *dtype = t->dtype;
+    if (rows) *rows = t->rows;
+    if (k) *k = t->k;
+    if (data) *data = t->data;
+    if (data_row_stride_bytes) *data_row_stride_bytes = t->ld;
+    if (scales) *scales = t->scales;
+    if (scale_row_stride_bytes) *scale_row_stride_bytes = t->lds;
+    return QGEMM_OK;
+}
+
+static qgemm_status check_out_f16(const void *C, int64_t ldc, int64_t M, int64_t N) {
+    if (M * N == 0) return QGEMM_OK;
+    if (!C) return fail(QGEMM_ERR_INVALID_ARG, "output is NULL");
+    if (ldc < N) return fail(QGEMM_ERR_INVALID_ARG, "ldc %lld < N %lld", (long long)ldc, (long long)N);
+    if (!aligned(C, 16) || ldc % 8)
+        return fail(QGEMM_ERR_MISALIGNED, "output must be 16-byte aligned with ldc %% 8 == 0");
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                         void *stream) {
+    if (!A || !B) return fail(QGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if (A->dtype != QGEMM_E4M3 || B->dtype != QGEMM_E4M3)
+        return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "qgemm_mxfp8 takes E4M3 views");
+    if (A->k != B->k) return fail(QGEMM_ERR_INVALID_ARG, "K mismatch (%lld vs %lld)",
+                                  (long long)A->k, (long long)B->k);
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    qgemm_status st = check_out_f16(C, ldc, M, N);
+    if (st != QGEMM_OK) return st;
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (K % 32) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "K %% 32 != 0");
+    for (const qgemm_tensor *t : {A, B}) {
+        if (K > 0 && (!aligned(t->data, 16) || t->ld % 16))
+            return fail(QGEMM_ERR_MISALIGNED, "E4M3 data must be 16-byte aligned, row stride %% 16 == 0");
+        if (K > 0 && (!aligned(t->scales, 4) || t->lds % 4))
+            return fail(QGEMM_ERR_MISALIGNED, "scale plane must be 4-byte aligned, stride %% 4 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+    }
+    bool enc = true;
+    e = qgi::launch_mxfp8(A, B, static_cast<__half *>(C), ldc, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_mxfp8 launch");
+}
+
+qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                      int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative shape");
+    if (M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    qgemm_status st = check_out_f16(C, ldc, M, N);
+    if (st != QGEMM_OK) return st;
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (K > 0) {
+        if (!A || !B) return fail(QGEMM_ERR_INVALID_ARG, "A or B is NULL");
+        if (lda < K || ldb < N) return fail(QGEMM_ERR_INVALID_ARG, "lda < K or ldb < N");
+        if (!aligned(A, 16) || !aligned(B, 16) || lda % 8 || ldb % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "A, B must be 16-byte aligned, lda/ldb %% 8 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+    }
+    bool enc = true;
+    e = qgi::launch_gemm_f16(static_cast<const __half *>(A), lda, static_cast<const __half *>(B),
+                             ldb, static_cast<__half *>(C), ldc, (int)M, (int)N, (int)K, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "gemm_f16 launch");
+}
+
+qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                         void *C_f16, int64_t ldc, void *stream) {
+    if (!W) return fail(QGEMM_ERR_INVALID_ARG, "W is NULL");
+    if (W->dtype != QGEMM_INT4) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "W must be an INT4 view");
+    if (M < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative M");
+    if (M > MAX_DIM) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "M >= 2^31");
+    const int64_t N = W->rows, K = W->k;
+    qgemm_status st = check_out_f16(C_f16, ldc, M, N);
+    if (st != QGEMM_OK) return st;
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (K % 64) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "K %% 64 != 0 (K = %lld)", (long long)K);
+    if (K > 0) {
+        if (!A_f16) return fail(QGEMM_ERR_INVALID_ARG, "A is NULL");
+        if (lda < K) return fail(QGEMM_ERR_INVALID_ARG, "lda < K");
+        if (!aligned(A_f16, 16) || lda % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "A must be 16-byte aligned, lda %% 8 == 0");
+        if (!aligned(W->data, 16) || W->ld % 16)
+            return fail(QGEMM_ERR_MISALIGNED, "int4 data must be 16-byte aligned, stride %% 16 == 0");
+        if (!aligned(W->scales, 4) || W->lds % 4)
+            return fail(QGEMM_ERR_MISALIGNED, "scale plane must be 4-byte aligned, stride %% 4 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C_f16), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+    }
+    bool enc = true;
+    e = qgi::launch_w4a16(static_cast<const __half *>(A_f16), lda, (int)M, W,
+                          static_cast<__half *>(C_f16), ldc, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16 launch");
+}
+
+qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                           void *Y_f16, int64_t ldy, void *stream) {
+    if (!W) return fail(QGEMM_ERR_INVALID_ARG, "W is NULL");
+    if (W->dtype != QGEMM_INT8) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "W must be an INT8 view");
+    if (M < 1 || M > 16) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "M must be in 1..16 (got %lld)",
+                                     (long long)M);
+    const int64_t N = W->rows, K = W->k;
+    if (N == 0) return QGEMM_OK;
+    if (!Y_f16) return fail(QGEMM_ERR_INVALID_ARG, "Y is NULL");
+    if (ldy < N) return fail(QGEMM_ERR_INVALID_ARG, "ldy < N");
+    if (!aligned(Y_f16, 2)) return fail(QGEMM_ERR_MISALIGNED, "Y must be 2-byte aligned");
+    if (K % 32) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "K %% 32 != 0");
+    if (K > 0) {
+        if (!X_f16) return fail(QGEMM_ERR_INVALID_ARG, "X is NULL");
+        if (ldx < K) return fail(QGEMM_ERR_INVALID_ARG, "ldx < K");
+        if (!aligned(X_f16, 16) || ldx % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "X must be 16-byte aligned, ldx %% 8 == 0");
+        if (!aligned(W->data, 8) || W->ld % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "int8 data must be 8-byte aligned, stride %% 8 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_fill_zero_f16(static_cast<__half *>(Y_f16), ldy, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+    }
+    e = qgi::launch_w8_gemv(static_cast<const __half *>(X_f16), ldx, (int)M, W,
+                            static_cast<__half *>(Y_f16), ldy, ctx);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w8_gemv launch");
+}
+
+qgemm_status qgemm_dequant_debug(const qgemm_tensor *t, float *out, void *stream) {
+    if (!t) return fail(QGEMM_ERR_INVALID_ARG, "tensor is NULL");
+    if (t->rows * t->k == 0) return QGEMM_OK;
+    if (!out) return fail(QGEMM_ERR_INVALID_ARG, "out is NULL");
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e = qgi::launch_dequant(t, out, ctx);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_dequant_debug launch");
+}
+
+qgemm_status qgemm_poll_device_error(void *stream, uint32_t *code_out) {
+    if (code_out) *code_out = 0;
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ctx.err, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (word) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(ctx.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    }
+    if (code_out) *code_out = word;
+    if (word) return fail(QGEMM_ERR_TIMEOUT, "device error word 0x%x", word);
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e = qgi::launch_selftest_wait(timeout_ns, ctx);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "self-test launch");
+}
+
+}  // extern "C"

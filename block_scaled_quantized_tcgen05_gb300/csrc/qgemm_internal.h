@@ -1,0 +1,56 @@
+// qgemm_internal.h -- host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qgemm.h"
+
+// The view behind the opaque handle: borrowed device pointers plus shape.
+struct qgemm_tensor {
+    int32_t dtype;
+    int64_t rows;
+    int64_t k;
+    const uint8_t *data;
+    int64_t ld;          // bytes between rows of the data plane
+    const uint8_t *scales;
+    int64_t lds;         // bytes between rows of the scale plane
+};
+
+namespace qgi {
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    unsigned *err;        // device error word
+    uint64_t timeout_ns;  // bound on every device-side wait
+    int num_sms;
+    int device;
+};
+
+// Records a formatted message for qgemm_last_error_message() and returns `s`.
+qgemm_status fail(qgemm_status s, const char *fmt, ...);
+
+// Encode a 2-D tiled TMA descriptor (inner dimension first).  Returns false on failure.
+bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                   uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                   uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// Kernel launchers (one per translation unit).  Arguments are already validated.
+cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                         const LaunchCtx &ctx, bool *encode_ok);
+cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64_t ldb,
+                            __half *C, int64_t ldc, int M, int N, int K, const LaunchCtx &ctx,
+                            bool *encode_ok);
+cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
+                         int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
+cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
+                           __half *Y, int64_t ldy, const LaunchCtx &ctx);
+cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);
+cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
+                                 const LaunchCtx &ctx);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, const LaunchCtx &ctx);
+
+}  // namespace qgi

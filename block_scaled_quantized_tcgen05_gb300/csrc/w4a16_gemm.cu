@@ -1,0 +1,363 @@
+// w4a16_gemm.cu -- weight-only int4 GEMM for prefill shapes on tcgen05.
+//
+// C[M, N] = fp16_rn( sum_k A[m, k] * q(W[n, k]) * 2^(SW[n, k/32] - 127) ),  fp32 accumulation.
+//
+// "TensorOps: quantized matmul ..." (sections "Revised kernel strategy" and "M2 = block-32 fp16
+// scaling") dequantises each 32-block of int4 weights with its scale into on-chip memory and
+// then runs the half x half matmul; the same page's escape-hatch note recommends dequantising
+// straight into the operand the matrix unit reads.  On GB300 the operand the tensor core reads
+// is shared memory in the 128-byte-swizzled K-major layout, so converter warps write the
+// dequantised fp16 weight tile directly in that layout:
+//   warp 0     TMA producer for the activation tile A (128 rows x 64 k, 128-byte swizzle).
+//   warp 1     TMEM owner + MMA issuer (kind::f16, both operands K-major).
+//   warps 2-5  epilogue (TMEM -> fp16 -> global).
+//   warps 6-9  converters: cp.async the packed int4 bytes and scale words of future k-tiles into
+//              a private ring (each thread consumes only what it copied), then per 32-block
+//              turn 32 nibbles into fp16 (q + 8 placed in the mantissa of 1024, minus 1032; the
+//              high nibble as 1024 + 16 (q + 8), times 1/16, minus 72), multiply by the fp16
+//              power of two 2^(e-127) and store 16-byte chunks at their swizzled position.
+// The fp16 weight q * 2^(e-127) is exact for 103 <= e <= 139.
+#include "qgemm_common.cuh"
+#include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
+
+namespace {
+
+using namespace qg;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int RAW = 3;            // k-tiles of int4 prefetched ahead by each converter thread
+constexpr int CONV_THREADS = 128;
+constexpr int THREADS = 192 + CONV_THREADS;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr int UNITS = 4;          // (row, 32-block) units per converter thread per k-tile
+
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t RAW_DATA_BYTES = UNITS * CONV_THREADS * 16;  // [unit][thread] 16 B
+constexpr uint32_t RAW_SCALE_BYTES = UNITS * CONV_THREADS * 4;  // [unit][thread] 4 B
+constexpr uint32_t RAW_SLOT_BYTES = RAW_DATA_BYTES + RAW_SCALE_BYTES;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr uint32_t OFF_RAW = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t OFF_BAR = OFF_RAW + RAW * RAW_SLOT_BYTES;
+constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// kind::f16, D fp32, A and B fp16, both K-major, N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                           (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4_full(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// fp16 bits of 2^(e-127) for e in [103, 142] (subnormals below 2^-14); outside that range the
+// nearest representable behaviour: 0 below, +inf above.
+__device__ __forceinline__ uint32_t ue8m0_to_f16x2(uint32_t e) {
+    const int x = static_cast<int>(e) - 127;
+    uint32_t h;
+    if (x > 15) h = 0x7C00u;
+    else if (x >= -14) h = static_cast<uint32_t>(x + 15) << 10;
+    else if (x >= -24) h = 1u << (x + 24);
+    else h = 0u;
+    return h | (h << 16);
+}
+
+// 8 int4 (one 32-bit word, k = 8w .. 8w+7, even k in low nibbles) times the fp16x2 scale ->
+// four fp16x2 words in k order.
+__device__ __forceinline__ void i4x8_to_f16(uint32_t v, uint32_t s2, uint32_t (&o)[4]) {
+    const uint32_t u = v ^ 0x88888888u;  // q + 8 in every nibble
+    const uint32_t MAGIC = 0x64006400u;   // fp16 1024.0 in both halves
+    const uint32_t t0 = (u & 0x000F000Fu) | MAGIC;         // 1024 + u(k0), 1024 + u(k4)
+    const uint32_t t1 = (u & 0x00F000F0u) | MAGIC;         // 1024 + 16 u(k1), ... (k5)
+    const uint32_t t2 = ((u >> 8) & 0x000F000Fu) | MAGIC;  // k2, k6
+    const uint32_t t3 = ((u >> 8) & 0x00F000F0u) | MAGIC;  // k3, k7
+    const uint32_t B1032 = 0x64086408u;   // 1032.0
+    const uint32_t R16 = 0x2C002C00u;     // 1/16
+    const uint32_t N72 = 0xD480D480u;     // -72.0
+    const uint32_t h0 = h2_mul(h2_sub(t0, B1032), s2);         // (q0, q4) * s
+    const uint32_t h1 = h2_mul(h2_fma(t1, R16, N72), s2);      // (q1, q5) * s
+    const uint32_t h2 = h2_mul(h2_sub(t2, B1032), s2);         // (q2, q6) * s
+    const uint32_t h3 = h2_mul(h2_fma(t3, R16, N72), s2);      // (q3, q7) * s
+    o[0] = __byte_perm(h0, h1, 0x5410);  // (q0, q1)
+    o[1] = __byte_perm(h2, h3, 0x5410);  // (q2, q3)
+    o[2] = __byte_perm(h0, h1, 0x7632);  // (q4, q5)
+    o[3] = __byte_perm(h2, h3, 0x7632);  // (q6, q7)
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__restrict__ W,
+                  int64_t ldw, const uint8_t *__restrict__ SW, int64_t ldsw,
+                  __half *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned *err,
+                  uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
+
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1 + CONV_THREADS);  // TMA arrival + every converter thread
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        // -------------------------------------------------------- activation producer
+        uint32_t stage = 0, phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(stage), A_BYTES);
+                    tma_load_2d(sb + OFF_A + stage * A_BYTES, &tmA, full_bar(stage), kt * BK,
+                                mb * BM);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+        for (int i = max(0, issued - STAGES); i < issued; ++i) {
+            if (!mbar_wait(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t adesc = smem_desc(sb + OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
+                    const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
+#pragma unroll
+                    for (uint32_t j = 0; j < BK / 16; ++j)
+                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 2 * j, IDESC,
+                                (kt > 0 || j > 0) ? 1u : 0u);
+                    tc_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(tmem_full);
+            __syncwarp();
+            acc_phase ^= 1;
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
+        if (lane == 0) tc_commit(drain_bar);
+        __syncwarp();
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------- epilogue
+        const uint32_t q = warp & 3;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int row = mb * BM + static_cast<int>(q * 32 + lane);
+            __half *crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+                tmem_wait_ld();
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+            acc_phase ^= 1;
+        }
+    } else {
+        // ----------------------------------------------------------------- converters
+        const int ct = static_cast<int>(threadIdx.x) - 192;   // 0..127
+        const int h = ct & 1;                                   // which 32-block of the k-tile
+        const int rsub = ct >> 1;                               // row within each 64-row group
+        const int my_tiles = (num_tiles > static_cast<int>(blockIdx.x))
+                                 ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                                 : 0;
+        const int total = my_tiles * KT;
+        // Issue the copies of iteration `it` (tile index, k-tile) into raw slot it % RAW.
+        auto issue = [&](int it) {
+            if (it < total) {
+                const int tile = blockIdx.x + (it / KT) * gridDim.x;
+                const int kt = it % KT;
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, mb, nb);
+                const uint32_t rs = sb + OFF_RAW + (it % RAW) * RAW_SLOT_BYTES;
+                const int blk = kt * 2 + h;                     // scale block index along K
+#pragma unroll
+                for (int i = 0; i < UNITS; ++i) {
+                    int n = nb * BN + 64 * i + rsub;
+                    n = n < N ? n : N - 1;                      // rows past N are never stored
+                    const uint8_t *src = W + static_cast<int64_t>(n) * ldw + kt * (BK / 2) + 16 * h;
+                    cp_async_16(rs + (i * CONV_THREADS + ct) * 16, src);
+                    const uint8_t *ssrc = SW + static_cast<int64_t>(n) * ldsw + (blk & ~3);
+                    cp_async_4_full(rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4, ssrc);
+                }
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int p = 0; p < RAW; ++p) issue(p);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int it = 0; it < total; ++it) {
+            const int kt = it % KT;
+            cp_async_wait<RAW - 1>();
+            if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *rs = smem + OFF_RAW + (it % RAW) * RAW_SLOT_BYTES;
+            const uint32_t sB = sb + OFF_B + stage * B_BYTES;
+            const int blk = kt * 2 + h;
+#pragma unroll
+            for (int i = 0; i < UNITS; ++i) {
+                const uint4 d = *reinterpret_cast<const uint4 *>(rs + (i * CONV_THREADS + ct) * 16);
+                const uint32_t sw = *reinterpret_cast<const uint32_t *>(
+                    rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4);
+                const uint32_t e = (sw >> (8 * (blk & 3))) & 0xFF;
+                const uint32_t s2 = ue8m0_to_f16x2(e);
+                const int r = 64 * i + rsub;                     // row inside the 256-row tile
+                const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t o[4];
+                    i4x8_to_f16(words[w], s2, o);
+                    const int c = 4 * h + w;                     // 16-byte chunk (8 k) in the row
+                    const uint32_t dst = sB + r * 128 + ((c ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]),
+                                 "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(full_bar(stage));
+            issue(it + RAW);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        cp_async_wait<0>();
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace
+
+namespace qgi {
+
+cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
+                         int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
+    const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
+    CUtensorMap tmA;
+    *encode_ok = encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    w4a16_gemm_kernel<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(
+        tmA, W->data, W->ld, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace qgi

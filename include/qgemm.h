@@ -1,0 +1,190 @@
+/*
+ * qgemm.h -- C ABI of the block-scaled quantized GEMM library for GB300 (sm_103a).
+ *
+ * The operation is the quantized matmul2d of "TensorOps: quantized matmul, cooperative tensors,
+ * and the neural accelerator" (section "Quantized matmul2d -- and the custom-format escape
+ * hatch"): the quantized product uses the same call shape as the fp16 one, the operands carry a
+ * data plane plus a scale plane, and the library dequantises on the fly.  Every product below is
+ *
+ *     C[m, n] = fp16_rn( sum_k deq(A)[m, k] * deq(B)[n, k] )       (fp32 accumulation)
+ *
+ * with deq(X)[r, k] = decode(X.data[r, k]) * 2^(X.scales[r, k / 32] - 127).  The output is always
+ * overwritten ("mode multiply", same page, section "The real matmul2d API").
+ *
+ * Conventions that hold for every call:
+ *   - All data, scale and output pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or retains device memory; a qgemm_tensor only borrows pointers.
+ *   - Matrices are row-major with the reduction dimension K contiguous ("K-major"), except the
+ *     right operand of gemm_f16, which is B[K, N] row-major (N contiguous).
+ *   - Row strides are given in BYTES for qgemm_tensor planes and in ELEMENTS for plain fp16
+ *     matrices (lda, ldb, ldc, ldx, ldy).
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = legacy default stream).  Compute
+ *     calls only validate and enqueue; they return before the GPU finishes.  Errors found on the
+ *     host are returned before anything is enqueued (nothing is written).  A failed launch
+ *     returns QGEMM_ERR_CUDA.
+ *   - Every device-side wait is bounded.  A kernel that gives up records a code in a device
+ *     error word that qgemm_poll_device_error() reads; its outputs are then unspecified.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QGEMM_OK = 0,
+    QGEMM_ERR_INVALID_ARG = 1,       /* null pointer, negative size, inconsistent shapes       */
+    QGEMM_ERR_UNSUPPORTED_SHAPE = 2, /* a size the kernels do not take (e.g. K % 32 != 0)      */
+    QGEMM_ERR_MISALIGNED = 3,        /* pointer or stride alignment below what the kernel needs */
+    QGEMM_ERR_UNSUPPORTED_DTYPE = 4, /* wrong data type for the call, or block size != 32     */
+    QGEMM_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed (see last message)   */
+    QGEMM_ERR_TIMEOUT = 6            /* a kernel's bounded wait ran out (device error word)    */
+} qgemm_status;
+
+typedef enum {
+    QGEMM_F16 = 0,   /* IEEE binary16, no scale plane                                        */
+    QGEMM_E4M3 = 1,  /* FP8 E4M3 (OCP, no infinity), one byte per element                    */
+    QGEMM_INT8 = 2,  /* two's complement int8, one byte per element                          */
+    QGEMM_INT4 = 3   /* two's complement int4, two per byte, even k in the low nibble        */
+} qgemm_dtype;
+
+/* Opaque, host-side, NON-owning view of one quantized matrix [rows, k]. */
+typedef struct qgemm_tensor qgemm_tensor;
+
+/* Library version, (major << 16) | minor. */
+int32_t qgemm_version(void);
+
+/* Create a view of a quantized matrix: data plane plus UE8M0 scale plane.
+ * Passage: "TensorOps: quantized matmul ...", section "Scale planes: one MTLTensor = data +
+ * scales" (one object carries the data plane and an auxiliary plane of block scales; the block
+ * factors give how many data elements share one scale) and "Optimize custom machine learning
+ * operations with Metal tensors", section "Creating quantized tensors with scale factors" (a
+ * failed creation reports an error and yields no tensor).  The scale type must be UE8M0 and the
+ * block 32 along K by 1 along rows (same first page, "Kernel-phase findings", fact 2).
+ *   out            receives the new view; set to NULL on any error.
+ *   dt             element type of the data plane.
+ *   rows, k        logical shape [rows, k]; k is the contiguous (reduction) dimension.
+ *   data           device pointer to element (0, 0); row r starts at data + r * data_row_stride_bytes.
+ *                  int4: element (r, k) is nibble (k & 1) of byte k / 2 of row r.
+ *   scales_ue8m0   device pointer to the [rows, ceil(k / 32)] UE8M0 scale plane; scale (r, b) at
+ *                  scales_ue8m0 + r * scale_row_stride_bytes + b.  Must be NULL for QGEMM_F16 and
+ *                  non-NULL for the other types.
+ *   block_k        must be 32 (QGEMM_ERR_UNSUPPORTED_DTYPE otherwise; ignored for QGEMM_F16).
+ * Errors: QGEMM_ERR_INVALID_ARG (null out/data, negative sizes, strides shorter than a row),
+ *         QGEMM_ERR_UNSUPPORTED_SHAPE (k % 32 != 0 for a scaled type; odd k for int4),
+ *         QGEMM_ERR_UNSUPPORTED_DTYPE (unknown dtype, block_k != 32, scales present for F16). */
+qgemm_status qgemm_create_tensor(qgemm_tensor **out, qgemm_dtype dt, int64_t rows, int64_t k,
+                                 const void *data, int64_t data_row_stride_bytes,
+                                 const uint8_t *scales_ue8m0, int64_t scale_row_stride_bytes,
+                                 int32_t block_k);
+
+/* View of rows [row0, row0 + nrows) and columns [k0, k0 + nk) of t; data and scale planes are
+ * sliced together so the sub-view's block grid stays aligned ("TensorOps: quantized matmul ...",
+ * section "Scale planes ...": slicing a quantized tensor slices both planes, respecting the block
+ * size).  k0 must be a multiple of 32 for scaled types (and even for int4); the slice must lie
+ * inside t.  The new view borrows the same memory and is independent of t's lifetime.
+ * Errors: QGEMM_ERR_INVALID_ARG (null, out of range), QGEMM_ERR_UNSUPPORTED_SHAPE (k0 or nk not
+ * block-aligned). */
+qgemm_status qgemm_tensor_slice(const qgemm_tensor *t, int64_t row0, int64_t nrows, int64_t k0,
+                                int64_t nk, qgemm_tensor **out);
+
+/* Free the view (host memory only; never touches device memory).  NULL is a no-op. */
+void qgemm_destroy_tensor(qgemm_tensor *t);
+
+/* Read back a view's fields (any out-pointer may be NULL). */
+qgemm_status qgemm_tensor_info(const qgemm_tensor *t, int32_t *dtype, int64_t *rows, int64_t *k,
+                               const void **data, int64_t *data_row_stride_bytes,
+                               const uint8_t **scales, int64_t *scale_row_stride_bytes);
+
+/* MXFP8 GEMM: C[M, N] = fp16_rn(sum_k deq(A)[m, k] * deq(B)[n, k]), fp32 accumulation.
+ * Passage: "Optimize custom machine learning operations with Metal tensors", sections "Shader
+ * MXFP8 tensor types" and "Slicing and quantized matmul" (E4M3 data with a UE8M0 block-32 scale
+ * plane fed straight into matmul2d), with the right operand stored transposed, i.e. [N, K]
+ * ("TensorOps: quantized matmul ...", "Kernel-phase findings", fact 2).
+ *   A   QGEMM_E4M3 view [M, K];  B   QGEMM_E4M3 view [N, K] (same K).
+ *   C   device fp16 [M, N] with row stride ldc elements (ldc >= N).
+ * Requirements: K % 32 == 0; data pointers and byte strides 16-byte aligned; scale pointers and
+ * scale strides 4-byte aligned; C and ldc * 2 16-byte aligned.  Any M, N >= 0 (ragged tiles are
+ * masked); M or N == 0 writes nothing; K == 0 writes zeros.
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                         void *stream);
+
+/* fp16 GEMM: C[M, N] = fp16_rn(A[M, K] @ B[K, N]), fp32 accumulation, all row-major fp16.
+ * Passage: "TensorOps: quantized matmul ...", "VALIDATED ON M4 MAX" (kernel M0, half x half ->
+ * half) and "TileLang Metal Backend Internals", section 1 (fp16 input, fp32 accumulation, fp16
+ * output cast on store).
+ * Requirements: A, B, C 16-byte aligned; lda, ldb, ldc multiples of 8 elements; lda >= K,
+ * ldb >= N, ldc >= N.  Any M, N, K >= 0 (ragged tiles masked; K == 0 writes zeros).
+ * Errors: INVALID_ARG, MISALIGNED (nothing enqueued); CUDA. */
+qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                      int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Weight-only int4 GEMM (prefill): C[M, N] = fp16_rn(sum_k A[m, k] * deq(W)[n, k]).
+ * Passage: "TensorOps: quantized matmul ...", "Revised kernel strategy" and "M2 = block-32 fp16
+ * scaling" (dequantise each 32-block of the int4 weight with its scale, then feed the half x half
+ * matmul, accumulating across blocks), with the int4 packing of "VALIDATED ON M4 MAX", fact 5.
+ *   A   device fp16 [M, K], row stride lda elements.
+ *   W   QGEMM_INT4 view [N, K] with UE8M0 scales [N, K / 32].
+ *   C   device fp16 [M, N], row stride ldc.
+ * Numerics: each weight is dequantised to fp16 exactly as q * 2^(e - 127), which is exact for
+ * scale bytes 103 <= e <= 139 (|w| between 2^-24 and 2^15); outside that range the dequantised
+ * fp16 weight is rounded (or overflows to inf for e >= 141 and q = -8).
+ * Requirements: K % 64 == 0; A, C 16-byte aligned; lda, ldc multiples of 8; W data 16-byte
+ * aligned with a 16-byte multiple row stride; any M, N.
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA. */
+qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                         void *C_f16, int64_t ldc, void *stream);
+
+/* Decode GEMV with int8 weights: Y[m, n] = fp16_rn(sum_k X[m, k] * deq(W)[n, k]), 1 <= M <= 16.
+ * Passage: "TensorOps: quantized matmul ...", section "Why this matters here" (decode is bound
+ * by memory bandwidth; int8 weights are read at int8 cost) and "VALIDATED ON M4 MAX" (kernel
+ * M1a, half x int8 -> half).  Each 32-block partial sum is scaled by its power of two in fp32,
+ * so every scale byte 0..254 is handled exactly.
+ *   X   device fp16 [M, K], row stride ldx elements.
+ *   W   QGEMM_INT8 view [N, K] with UE8M0 scales [N, K / 32].
+ *   Y   device fp16 [M, N], row stride ldy elements.
+ * Requirements: 1 <= M <= 16; K % 32 == 0; X 16-byte aligned, ldx multiple of 8; W data and row
+ * stride 8-byte aligned; Y 2-byte aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA. */
+qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                           void *Y_f16, int64_t ldy, void *stream);
+
+/* Dequantise-only debug kernel: out[r, k] = decode(t.data[r, k]) * 2^(t.scales[r, k/32] - 127)
+ * as fp32 (fp16 views: the value itself), written densely as [rows, k] row-major.  Exists so
+ * that the decoded operand values can be compared bit for bit with the CPU reference, as the
+ * "Running inline ML operations in a shader with Metal 4" sample checks its GPU result against a
+ * CPU implementation.  E4M3 NaN codes and scale byte 255 give NaN.
+ * Errors: INVALID_ARG (null t or out); CUDA. */
+qgemm_status qgemm_dequant_debug(const qgemm_tensor *t, float *out, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qgemm_status_string(qgemm_status s);
+
+/* Detail of the last error returned on the calling thread (static per-thread buffer). */
+const char *qgemm_last_error_message(void);
+
+/* Synchronise `stream`, then read and clear the device error word of the current device.
+ * *code_out (may be NULL) receives the raw word: 0 = no kernel gave up; otherwise bits name the
+ * wait that ran out (1 producer, 2 MMA issuer, 4 epilogue, 8 drain, 16 test wait).
+ * Returns QGEMM_ERR_TIMEOUT if the word was non-zero, QGEMM_ERR_CUDA if synchronisation failed. */
+qgemm_status qgemm_poll_device_error(void *stream, uint32_t *code_out);
+
+/* Upper bound, in nanoseconds, on every device-side wait of kernels launched after this call
+ * (default 4e9).  Values below 1e6 are raised to 1e6. */
+void qgemm_set_wait_timeout_ns(uint64_t ns);
+
+/* Failure-detection self test: launches one kernel that waits on a barrier nothing ever
+ * completes, with the wait limit `timeout_ns`; the wait gives up, records bit 16 in the device
+ * error word and the kernel returns normally.  No output; use qgemm_poll_device_error().
+ * Errors: CUDA. */
+qgemm_status qgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

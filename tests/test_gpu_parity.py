@@ -1,0 +1,285 @@
+"""GPU parity: every kernel of the library against the CPU oracle, through the C ABI.
+
+Tolerance (element-wise): |C_gpu - C| <= 2e-3 * sum_k |a_mk b_nk| + 2^-24, with C the fp64
+product of the decoded operands; non-finite values must match.  Decoded operands must match bit
+for bit (dequantise-only debug kernel).
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_quantized_tcgen05_gb300 as q
+from block_scaled_quantized_tcgen05_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+REL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from block_scaled_quantized_tcgen05_gb300 import build
+    build.build()
+    q.load_library()
+    q.qgemm_set_wait_timeout_ns(2_000_000_000)
+    return torch.device("cuda:0")
+
+
+def _check(got: torch.Tensor, res, orc, rows=None, what=""):
+    ok, worst, info = orc.within_tolerance(got.float().cpu().numpy(), res, REL, rows)
+    assert ok, f"{what}: {info}"
+    assert q.qgemm_poll_device_error() == 0, f"{what}: device wait timed out"
+    return worst
+
+
+def _mx_views(d, dev):
+    a, sa, b, sb = (d[k].to(dev) for k in ("a", "sa", "b", "sb"))
+    return q.qgemm_create_tensor(q.E4M3, a, sa), q.qgemm_create_tensor(q.E4M3, b, sb), (a, sa, b, sb)
+
+
+# ----------------------------------------------------------------------- dequant debug
+def test_dequant_debug_bit_exact_all_codes(dev, orc):
+    rows, K = 256, 256
+    data = torch.arange(rows * K, dtype=torch.int64).remainder(256).to(torch.uint8).reshape(rows, K)
+    data = data[torch.randperm(rows, generator=synth.generator(1))].contiguous()
+    sc = torch.randint(0, 247, (rows, K // 32), generator=synth.generator(2), dtype=torch.uint8)
+    sc[0, 0] = 255                                               # NaN scale
+    for dt in (q.E4M3, q.INT8):
+        t = q.qgemm_create_tensor(dt, data.to(dev), sc.to(dev))
+        out = torch.empty(rows, K, dtype=torch.float32, device=dev)
+        q.qgemm_dequant_debug(t, out)
+        ref = orc.dequant(orc.E4M3 if dt == q.E4M3 else orc.INT8, data.numpy(), sc.numpy())
+        got = out.cpu().numpy().astype(np.float64)
+        assert np.array_equal(np.isnan(got), np.isnan(ref))
+        fin = ~np.isnan(ref)
+        assert np.array_equal(got[fin], ref[fin].astype(np.float32).astype(np.float64))
+    # int4: every nibble value in both positions
+    sc4 = torch.randint(100, 150, (rows, 2 * K // 32), generator=synth.generator(3),
+                        dtype=torch.uint8)
+    t4 = q.qgemm_create_tensor(q.INT4, data.to(dev), sc4.to(dev))
+    out4 = torch.empty(rows, 2 * K, dtype=torch.float32, device=dev)
+    q.qgemm_dequant_debug(t4, out4)
+    ref4 = orc.dequant(orc.INT4, data.numpy(), sc4.numpy())
+    assert np.array_equal(out4.cpu().numpy().astype(np.float64), ref4)
+    # fp16 view: the values themselves
+    h = torch.randn(64, 96, generator=synth.generator(4)).half()
+    th = q.qgemm_create_tensor(q.F16, h.to(dev), None)
+    outh = torch.empty(64, 96, dtype=torch.float32, device=dev)
+    q.qgemm_dequant_debug(th, outh)
+    assert torch.equal(outh.cpu(), h.float())
+
+
+# ------------------------------------------------------------------------------ MXFP8
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 520, 416), (128, 96, 64),
+                                   (1, 1, 32), (257, 384, 1024), (640, 768, 256)])
+def test_mxfp8_matches_oracle(dev, orc, M, N, K):
+    d = synth.mxfp8_inputs(M, N, K, seed=M + N + K, row_variance=True)
+    A, B, _ = _mx_views(d, dev)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, C)
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    _check(C, res, orc, what=f"mxfp8 {M}x{N}x{K}")
+    assert orc.cosine(C.float().cpu().numpy(), res.C) > 0.99999
+
+
+def test_mxfp8_padded_strides_and_output(dev, orc):
+    M, N, K = 200, 264, 256
+    d = synth.mxfp8_inputs(M, N, K, seed=5)
+    a = torch.zeros(M, K + 64, dtype=torch.uint8)
+    a[:, :K] = d["a"]
+    sa = torch.full((M, 16), 127, dtype=torch.uint8)
+    sa[:, :K // 32] = d["sa"]
+    A = q.qgemm_create_tensor(q.E4M3, a.to(dev)[:, :K], sa.to(dev)[:, :K // 32])
+    B = q.qgemm_create_tensor(q.E4M3, d["b"].to(dev), d["sb"].to(dev))
+    Cbig = torch.full((M, N + 40), 7.0, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, Cbig[:, :N])
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    _check(Cbig[:, :N], res, orc, what="mxfp8 strided")
+    assert torch.all(Cbig[:, N:] == 7.0)                        # nothing written past N
+
+
+def test_mxfp8_invariants(dev, orc):
+    M, N, K = 256, 512, 512
+    d = synth.mxfp8_inputs(M, N, K, seed=21)
+    A, B, (a, sa, b, sb) = _mx_views(d, dev)
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, C)
+    # doubling every A scale doubles C exactly (away from the fp16 subnormal range)
+    A2 = q.qgemm_create_tensor(q.E4M3, a, sa + 1)
+    C2 = torch.empty_like(C)
+    q.qgemm_mxfp8(A2, B, C2)
+    big = C.abs() >= 2.0 ** -13
+    assert torch.equal(C2[big], 2 * C[big])
+    # identity A (E4M3 1.0, scale 2^0), K = N: C = fp16(deq(B)^T)
+    Ki = 256
+    bi = d["b"][:, :Ki].contiguous()
+    sbi = d["sb"][:, :Ki // 32].contiguous()
+    eye = torch.zeros(Ki, Ki, dtype=torch.uint8)
+    eye[torch.arange(Ki), torch.arange(Ki)] = 0x38
+    Ai = q.qgemm_create_tensor(q.E4M3, eye.to(dev), torch.full((Ki, Ki // 32), 127, dtype=torch.uint8, device=dev))
+    Bi = q.qgemm_create_tensor(q.E4M3, bi.to(dev), sbi.to(dev))
+    Ci = torch.empty(Ki, N, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(Ai, Bi, Ci)
+    want = orc.f16_rn(orc.dequant(orc.E4M3, bi.numpy(), sbi.numpy()).T.copy())
+    assert np.array_equal(Ci.cpu().numpy().view(np.uint16), want)
+    # one-hot K: C = fp16(a[:, 37] * b[:, 37])
+    a1 = torch.zeros_like(d["a"])
+    a1[:, 37] = d["a"][:, 37]
+    A1 = q.qgemm_create_tensor(q.E4M3, a1.to(dev), sa)
+    C1 = torch.empty_like(C)
+    q.qgemm_mxfp8(A1, B, C1)
+    res1 = orc.mxfp8(a1.numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    assert np.array_equal(C1.cpu().numpy().view(np.uint16), res1.f16_bits)
+    # slicing rows of A and B (data and scales together) gives exactly the matching block of C
+    As = q.qgemm_tensor_slice(A, 64, 100, 0, K)
+    Bs = q.qgemm_tensor_slice(B, 128, 200, 0, K)
+    Cs = torch.empty(100, 200, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(As, Bs, Cs)
+    assert torch.equal(Cs, C[64:164, 128:328])
+    # slicing K into halves: C ~ C_lo + C_hi
+    Alo, Ahi = q.qgemm_tensor_slice(A, 0, M, 0, K // 2), q.qgemm_tensor_slice(A, 0, M, K // 2, K // 2)
+    Blo, Bhi = q.qgemm_tensor_slice(B, 0, N, 0, K // 2), q.qgemm_tensor_slice(B, 0, N, K // 2, K // 2)
+    Clo, Chi = torch.empty_like(C), torch.empty_like(C)
+    q.qgemm_mxfp8(Alo, Blo, Clo)
+    q.qgemm_mxfp8(Ahi, Bhi, Chi)
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    ok, _, info = orc.within_tolerance((Clo.float() + Chi.float()).cpu().numpy(), res, 2 * REL)
+    assert ok, info
+
+
+def test_mxfp8_edge_cases(dev, orc):
+    d = synth.mxfp8_inputs(64, 128, 64, seed=9)
+    A, B, _ = _mx_views(d, dev)
+    # K = 0: the empty sum is zero
+    A0 = q.qgemm_create_tensor(q.E4M3, torch.zeros(64, 16, dtype=torch.uint8, device=dev),
+                               torch.zeros(64, 4, dtype=torch.uint8, device=dev), k=0)
+    B0 = q.qgemm_create_tensor(q.E4M3, torch.zeros(128, 16, dtype=torch.uint8, device=dev),
+                               torch.zeros(128, 4, dtype=torch.uint8, device=dev), k=0)
+    C = torch.full((64, 128), 3.0, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A0, B0, C)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+    # M = 0: nothing happens
+    Ae = q.qgemm_tensor_slice(A, 0, 0, 0, 64)
+    q.qgemm_mxfp8(Ae, B, C[:0])
+    # NaN propagation: an E4M3 NaN code or a 0xFF scale poisons its row
+    a = d["a"].clone()
+    sa = d["sa"].clone()
+    a[3, 5] = 0x7F
+    sa[7, 1] = 255
+    An = q.qgemm_create_tensor(q.E4M3, a.to(dev), sa.to(dev))
+    Cn = torch.empty(64, 128, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(An, B, Cn)
+    Cn = Cn.cpu()
+    assert torch.isnan(Cn[3]).all() and torch.isnan(Cn[7]).all()
+    assert not torch.isnan(Cn[[0, 1, 2, 4, 5, 6]]).any()
+    # wrong argument: error status, no launch
+    with pytest.raises(q.QGemmError) as ei:
+        q.qgemm_mxfp8(A, q.qgemm_tensor_slice(B, 0, 128, 0, 32), C)
+    assert ei.value.name == "QGEMM_ERR_INVALID_ARG"
+
+
+def test_mxfp8_full_size_sampled(dev, orc):
+    """8192^3 with per-row variance 10^U(-2,2): full GPU product, oracle on sampled rows."""
+    d = synth.workload("mxfp8_8192")
+    A, B, _ = _mx_views(d, dev)
+    C = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, C)
+    rows = np.sort(np.random.default_rng(0).choice(8192, 48, replace=False))
+    rows = np.concatenate([[0, 127, 128, 8191], rows])
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy(), rows=rows)
+    got = C[torch.from_numpy(rows).to(dev)]
+    _check(got, res, orc, what="mxfp8 8192^3 sampled")
+
+
+# ------------------------------------------------------------------------------- fp16
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 328, 200), (96, 64, 512),
+                                   (384, 512, 1024)])
+def test_gemm_f16_matches_oracle(dev, orc, M, N, K):
+    d = synth.f16_inputs(M, N, K, seed=M * 7 + N)
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.gemm_f16(d["a"].to(dev), d["b"].to(dev), C)
+    res = orc.gemm_f16(d["a"].numpy(), d["b"].numpy())
+    _check(C, res, orc, what=f"f16 {M}x{N}x{K}")
+
+
+def test_gemm_f16_full_size_sampled(dev, orc):
+    d = synth.workload("f16_4096")
+    C = torch.empty(4096, 4096, dtype=torch.float16, device=dev)
+    q.gemm_f16(d["a"].to(dev), d["b"].to(dev), C)
+    rows = np.concatenate([[0, 4095], np.sort(np.random.default_rng(1).choice(4096, 30, replace=False))])
+    res = orc.gemm_f16(d["a"].numpy(), d["b"].numpy(), rows=rows)
+    _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="f16 4096^3 sampled")
+
+
+# ------------------------------------------------------------------------------ W4A16
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 256), (256, 640, 1024)])
+def test_w4a16_matches_oracle(dev, orc, M, N, K):
+    d = synth.w4a16_inputs(M, N, K, seed=M + 3 * N)
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(d["a"].to(dev), W, C)
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    _check(C, res, orc, what=f"w4a16 {M}x{N}x{K}")
+
+
+def test_w4a16_full_size_sampled(dev, orc):
+    d = synth.workload("w4a16_prefill")
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
+    C = torch.empty(4096, 14336, dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(d["a"].to(dev), W, C)
+    rows = np.concatenate([[0, 4095], np.sort(np.random.default_rng(2).choice(4096, 14, replace=False))])
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy(), rows=rows)
+    _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="w4a16 sampled")
+
+
+# ------------------------------------------------------------------------------- GEMV
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_w8_gemv_matches_oracle(dev, orc, M):
+    N, K = 1000, 1056
+    d = synth.w8_inputs(M, N, K, seed=M)
+    W = q.qgemm_create_tensor(q.INT8, d["w"].to(dev), d["sw"].to(dev))
+    Y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_w8_gemv(d["x"].to(dev), W, Y)
+    res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    _check(Y, res, orc, what=f"w8 gemv M={M}")
+
+
+def test_w8_gemv_extreme_scales(dev, orc):
+    """Per-block fp32 scaling handles every scale byte exactly (no fp16 folding)."""
+    M, N, K = 4, 64, 256
+    d = synth.w8_inputs(M, N, K, seed=99)
+    sw = torch.randint(60, 200, d["sw"].shape, generator=synth.generator(5), dtype=torch.uint8)
+    W = q.qgemm_create_tensor(q.INT8, d["w"].to(dev), sw.to(dev))
+    Y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_w8_gemv(d["x"].to(dev), W, Y)
+    res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy(), sw.numpy())
+    _check(Y, res, orc, what="w8 gemv extreme scales")
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_w8_gemv_full_size_sampled(dev, orc, M):
+    d = synth.workload("w8_decode", M=M)
+    W = q.qgemm_create_tensor(q.INT8, d["w"].to(dev), d["sw"].to(dev))
+    Y = torch.empty(M, 28672, dtype=torch.float16, device=dev)
+    q.qgemm_w8_gemv(d["x"].to(dev), W, Y)
+    cols = np.concatenate([[0, 28671], np.sort(np.random.default_rng(M).choice(28672, 2046, replace=False))])
+    res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy()[cols], d["sw"].numpy()[cols])
+    _check(Y[:, torch.from_numpy(cols).to(dev)], res, orc, what=f"w8 gemv 28672x8192 M={M}")
+
+
+# -------------------------------------------------------------------- failure detection
+def test_bounded_wait_gives_up_and_context_survives(dev, orc):
+    q.qgemm_poll_device_error()
+    q.qgemm_selftest_wait_timeout(2_000_000)            # 2 ms on a barrier nothing completes
+    code = q.qgemm_poll_device_error()
+    assert code & 16
+    assert q.qgemm_poll_device_error() == 0             # cleared
+    d = synth.mxfp8_inputs(128, 256, 128, seed=0)
+    A, B, _ = _mx_views(d, dev)
+    C = torch.empty(128, 256, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, C)
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    _check(C, res, orc, what="after self-test")
