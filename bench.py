@@ -1,0 +1,401 @@
+"""Benchmark of the block-scaled quantized GEMM hot path on GB300.
+
+One step = one pass of every row of the hot path over its workload, inputs resident in HBM:
+  1. MXFP8 GEMM        M = N = K = 8192   (E4M3 + UE8M0 per 32 along K, per-row variance)
+  2. fp16 GEMM         M = N = K = 4096
+  3. W4A16 GEMM        M = 4096, N = 14336, K = 4096 (int4 weights, UE8M0 per 32)
+  4. W8 decode GEMV    M = 1, 8, 16; N = 28672, K = 8192 (weights rotate over two copies)
+Each kernel is timed with CUDA events on the stream it is launched on.  The headline ``value``
+is the MXFP8 8192^3 GEMM in TFLOP/s; the GEMV in GB/s and the other rows are reported beside it.
+
+``--impl reference`` times the CPU oracle (test infrastructure, plain fp64 C) on a bounded sample
+of the same workload instead.  Under torchrun (N > 1) every rank runs the whole step on its own
+GPU (independent problems, no collective: weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+SPEC_FP8_TFLOPS = 4500.0
+SPEC_F16_TFLOPS = 2250.0
+SPEC_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "MXFP8 GEMM TFLOP/s at 8192^3 (% of GB300 FP8 peak); W8 GEMV GB/s (% of HBM)"
+WORKLOAD = "mxfp8_8192 + f16_4096 + w4a16_prefill + w8_decode(M=1,8,16)"
+
+
+def _peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import block_scaled_quantized_tcgen05_gb300 as q
+    from block_scaled_quantized_tcgen05_gb300 import synth
+
+    q.build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ------------------------------------------------------------- inputs (resident in HBM)
+    only = args.only
+    want = (lambda k: only is None or only == k)
+    mx = None
+    if want("mxfp8"):
+        mx = synth.workload("mxfp8_8192")
+        a, sa, b, sb = (mx[k].to(dev) for k in ("a", "sa", "b", "sb"))
+        A8 = q.qgemm_create_tensor(q.E4M3, a, sa)
+        B8 = q.qgemm_create_tensor(q.E4M3, b, sb)
+        C8 = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
+    if want("f16"):
+        f = synth.workload("f16_4096")
+        fa, fb = f["a"].to(dev), f["b"].to(dev)
+        fc = torch.empty(4096, 4096, dtype=torch.float16, device=dev)
+        del f
+    if want("w4a16"):
+        w4 = synth.workload("w4a16_prefill")
+        w4a = w4["a"].to(dev)
+        W4 = q.qgemm_create_tensor(q.INT4, w4["w"].to(dev), w4["sw"].to(dev))
+        w4c = torch.empty(4096, 14336, dtype=torch.float16, device=dev)
+        del w4
+    if want("gemv"):
+        gv = synth.workload("w8_decode", M=16)
+        W8s = []
+        for copy in range(2):        # two weight copies (484 MB): no GEMV reads L2-resident weights
+            w8 = gv["w"].to(dev) if copy == 0 else gv["w"].to(dev).clone()
+            s8 = gv["sw"].to(dev) if copy == 0 else gv["sw"].to(dev).clone()
+            W8s.append(q.qgemm_create_tensor(q.INT8, w8, s8))
+        X16 = gv["x"].to(dev)
+        Ys = {m: torch.empty(m, 28672, dtype=torch.float16, device=dev) for m in (1, 8, 16)}
+        del gv
+
+    all_kernels = ["mxfp8", "f16", "w4a16", "gemv_m1", "gemv_m8", "gemv_m16"]
+    kernels = [k for k in all_kernels if want(k.split("_")[0])]
+    stream = torch.cuda.current_stream()
+
+    def launch(k, i):
+        if k == "mxfp8":
+            q.qgemm_mxfp8(A8, B8, C8)
+        elif k == "f16":
+            q.gemm_f16(fa, fb, fc)
+        elif k == "w4a16":
+            q.qgemm_w4a16(w4a, W4, w4c)
+        else:
+            m = int(k[6:])
+            q.qgemm_w8_gemv(X16[:m], W8s[(i + m) % 2], Ys[m])
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for j, k in enumerate(kernels):
+            launch(k, i)
+            if ev is not None:
+                ev[j + 1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if q.qgemm_poll_device_error() != 0:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)]
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus if rank == 0 else None)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if rank == 0 else None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if q.qgemm_poll_device_error() != 0:
+        raise RuntimeError("a kernel wait timed out during the timed region")
+
+    total_ms = t0.elapsed_time(t1)
+    per = {k: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+           for j, k in enumerate(kernels)}
+    mean = {k: sum(v) / len(v) for k, v in per.items()}
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms] + [mean[k] for k in kernels], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+        mean = {k: float(t[1 + j]) for j, k in enumerate(kernels)}
+
+    # ----------------------------------------------------------- e2e through host buffers
+    e2e = None
+    if rank == 0 and mx is not None and not args.no_e2e:
+        e2e = e2e_mxfp8(q, torch, dev, a, sa, b, sb, reps=max(3, min(10, args.steps)))
+
+    # ---------------------------------------------------------- derived numbers
+    flops = {"mxfp8": 2.0 * 8192 ** 3, "f16": 2.0 * 4096 ** 3, "w4a16": 2.0 * 4096 * 14336 * 4096}
+    gemv_bytes = {m: 28672 * 8192 + 28672 * 256 + m * 8192 * 2 + m * 28672 * 2 for m in (1, 8, 16)}
+    peaks, peak_kind = _peaks()
+    fp8_peak_sust = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    secondary = {}
+    for k in kernels:
+        if k in ("f16", "w4a16"):
+            tf = flops[k] / (mean[k] * 1e-3) / 1e12
+            secondary[k] = {"us": round(mean[k] * 1e3, 2), "tflops": round(tf, 1),
+                            "frac_of_f16_spec_2250": round(tf / SPEC_F16_TFLOPS, 4),
+                            "frac_of_measured_bf16_sustained": round(
+                                tf / peaks.get("bf16_tflops_sustained", 1700.0), 4)}
+        elif k.startswith("gemv"):
+            m = int(k[6:])
+            gbs = gemv_bytes[m] / (mean[k] * 1e-3) / 1e9
+            secondary[k] = {"us": round(mean[k] * 1e3, 2), "gbs": round(gbs, 1),
+                            "frac_of_measured_hbm": round(gbs / hbm, 4),
+                            "frac_of_spec_hbm_8000": round(gbs / SPEC_HBM_GBS, 4)}
+    mx_tflops = None
+    if "mxfp8" in mean:
+        mx_tflops = flops["mxfp8"] / (mean["mxfp8"] * 1e-3) / 1e12
+        secondary["mxfp8"] = {"us": round(mean["mxfp8"] * 1e3, 2), "tflops": round(mx_tflops, 1),
+                              "frac_of_fp8_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4)}
+    value = ws * mx_tflops if mx_tflops is not None else None
+    launches = len(kernels) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 2) if value is not None else None,
+        "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+ue8m0",
+        "data": "synthetic (seeded, shapes and distributions of the workloads)",
+        "config": {"workload": WORKLOAD if only is None else only,
+                   "headline": "mxfp8_8192 M=N=K=8192",
+                   "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2: each kernel's inputs are evicted by the rest of "
+                         "the step (>129 MB between reuses); GEMV weights rotate over 2 copies"},
+        "roofline": None if mx_tflops is None else {
+            "kernel": "mxfp8_gemm_kernel<256>", "bound": "tensor",
+            "achieved": round(mx_tflops, 1), "peak": round(fp8_peak_sust, 1),
+            "unit": "TFLOP/s", "frac": round(mx_tflops / fp8_peak_sust, 4),
+            "peak_source": f"{peak_kind} bf16 sustained x 2 (nominal fp8/bf16 ratio)",
+            "frac_of_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4),
+            "traffic": None},
+        "kernels": secondary,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and mx is not None and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows, mx)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def e2e_mxfp8(q, torch, dev, a, sa, b, sb, reps):
+    """The same metric through the public C-ABI call with pinned host buffers: every rep copies
+    A, B and their scales host->device, runs the GEMM and copies C back."""
+    ha, hsa, hb, hsb = (t.cpu().pin_memory() for t in (a, sa, b, sb))
+    hc = torch.empty(8192, 8192, dtype=torch.float16).pin_memory()
+    da, dsa, db, dsb = (torch.empty_like(t, device=dev) for t in (ha, hsa, hb, hsb))
+    dc = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
+    A = q.qgemm_create_tensor(q.E4M3, da, dsa)
+    B = q.qgemm_create_tensor(q.E4M3, db, dsb)
+    stream = torch.cuda.current_stream()
+
+    def once():
+        for d, h in ((da, ha), (dsa, hsa), (db, hb), (dsb, hsb)):
+            d.copy_(h, non_blocking=True)
+        q.qgemm_mxfp8(A, B, dc)
+        hc.copy_(dc, non_blocking=True)
+
+    once()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    bi = sum(t.numel() * t.element_size() for t in (ha, hsa, hb, hsb))
+    bo = hc.numel() * hc.element_size()
+    return {"value": round(2.0 * 8192 ** 3 / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_call": round(ms, 3)}
+
+
+# --------------------------------------------------------------------- CPU oracle timing
+def cpu_baseline(rows: int, d):
+    """The oracle (plain fp64 C, OpenMP over all host cores) on a sample of the MXFP8 8192^3
+    workload: `rows` output rows x all 8192 columns, decode of A rows and all of B included."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    a, sa, b, sb = (d[k].numpy() for k in ("a", "sa", "b", "sb"))
+    sel = np.arange(rows)
+    t = time.perf_counter()
+    oracle.mxfp8(a, sa, b, sb, rows=sel)
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * 8192 * 8192
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    omp = os.environ.get("OMP_NUM_THREADS")
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": int(omp) if omp else cores, "kind": "oracle",
+            "sample": f"MXFP8 8192^3: {rows} rows x 8192 cols x K=8192 (fp64 decode + dot), "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the CPU oracle as it stands, each step a bounded sample of the workload."""
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from block_scaled_quantized_tcgen05_gb300 import synth
+    oracle.build()
+    d = synth.workload("mxfp8_8192")
+    a, sa, b, sb = (d[k].numpy() for k in ("a", "sa", "b", "sb"))
+    rows = args.ref_rows
+    for i in range(args.warmup):
+        oracle.mxfp8(a, sa, b, sb, rows=np.arange(i % 8, i % 8 + 1))
+    t = time.perf_counter()
+    for i in range(args.steps):
+        sel = (np.arange(rows) + i * rows) % 8192
+        oracle.mxfp8(a, sa, b, sb, rows=sel)
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * 8192 * 8192 * args.steps
+    value = flops / dt / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, shapes and distributions of the workloads)",
+        "config": {"workload": "mxfp8_8192 M=N=K=8192 (oracle on a row sample per step)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{rows} output rows x 8192 cols x K=8192 per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default=None, choices=["mxfp8", "f16", "w4a16", "gemv"],
+                    help="run one row of the hot path only (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_ours(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

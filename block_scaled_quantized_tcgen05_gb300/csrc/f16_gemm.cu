@@ -45,7 +45,7 @@ __host__ __device__ constexpr uint32_t f16_idesc(int n) {
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                __half *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned *err,
+                __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, unsigned *err,
                 uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
@@ -188,7 +188,7 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
                 tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
             }
             tc_fence_before();
             mbar_arrive(tmem_empty);
@@ -219,7 +219,8 @@ cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb
     if (e != cudaSuccess) return e;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, M, N, K, ctx.err,
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, c_vec, M, N, K, ctx.err,
                                                         ctx.timeout_ns);
     return cudaGetLastError();
 }

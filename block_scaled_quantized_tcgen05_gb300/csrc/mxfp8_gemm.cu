@@ -57,11 +57,24 @@ __host__ __device__ constexpr uint32_t mx_idesc(int n) {
     return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(BM >> 7) << 27);
 }
 
-template <int BN>
+// Up to 4 consecutive scale bytes (little-endian in one word), zero beyond `n`.
+__device__ __forceinline__ uint32_t load_scale_word(const uint8_t *p, uint32_t n) {
+    uint32_t w = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i)
+        if (i < n) w |= static_cast<uint32_t>(__ldg(p + i)) << (8 * i);
+    return w;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+template <int BN, bool SF_VEC>
 __global__ void __launch_bounds__(THREADS, 1)
 mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const uint8_t *__restrict__ sfa, int64_t lds_a, const uint8_t *__restrict__ sfb,
-                  int64_t lds_b, __half *__restrict__ C, int64_t ldc, int M, int N, int K,
+                  int64_t lds_b, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
                   unsigned *err, uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
@@ -132,24 +145,47 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t nbytes = static_cast<uint32_t>(min(4, nkb - kb0));
                 const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
                 const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int r = m0 + 32 * c + static_cast<int>(lane);
-                    const bool v = r < M;
-                    const uint8_t *src = v ? sfa + static_cast<int64_t>(r) * lds_a + kb0 : sfa;
-                    cp_async_4(sSFA + lane * 16 + c * 4, src, v ? nbytes : 0u);
-                }
-#pragma unroll
-                for (int h = 0; h < BN / 128; ++h) {
+                if constexpr (SF_VEC) {
+                    // 4-byte aligned scale rows: asynchronous copies, arrival when they land
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
-                        const bool v = r < N;
-                        const uint8_t *src = v ? sfb + static_cast<int64_t>(r) * lds_b + kb0 : sfb;
-                        cp_async_4(sSFB + h * 512 + lane * 16 + c * 4, src, v ? nbytes : 0u);
+                        const int r = m0 + 32 * c + static_cast<int>(lane);
+                        const bool v = r < M;
+                        const uint8_t *src = v ? sfa + static_cast<int64_t>(r) * lds_a + kb0 : sfa;
+                        cp_async_4(sSFA + lane * 16 + c * 4, src, v ? nbytes : 0u);
                     }
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
+                            const bool v = r < N;
+                            const uint8_t *src =
+                                v ? sfb + static_cast<int64_t>(r) * lds_b + kb0 : sfb;
+                            cp_async_4(sSFB + h * 512 + lane * 16 + c * 4, src, v ? nbytes : 0u);
+                        }
+                    }
+                    cp_async_arrive_noinc(full_bar(stage));
+                } else {
+                    // any scale stride: byte loads, then a proxy fence before the arrival
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int r = m0 + 32 * c + static_cast<int>(lane);
+                        const uint32_t w = r < M ? load_scale_word(sfa + static_cast<int64_t>(r) * lds_a + kb0, nbytes) : 0u;
+                        st_shared_u32(sSFA + lane * 16 + c * 4, w);
+                    }
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
+                            const uint32_t w = r < N ? load_scale_word(sfb + static_cast<int64_t>(r) * lds_b + kb0, nbytes) : 0u;
+                            st_shared_u32(sSFB + h * 512 + lane * 16 + c * 4, w);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(full_bar(stage));
                 }
-                cp_async_arrive_noinc(full_bar(stage));
                 ++issued;
                 if (++stage == S) {
                     stage = 0;
@@ -240,7 +276,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
                 tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
             }
             tc_fence_before();
             mbar_arrive(tmem_empty);
@@ -254,7 +290,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int BN>
+template <int BN, bool SF_VEC>
 cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                       const qgi::LaunchCtx &ctx, bool *encode_ok) {
     using G = Cfg<BN>;
@@ -266,14 +302,15 @@ cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, i
                  qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, K, N, B->ld, BK,
                                     BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
-    auto kern = mxfp8_gemm_kernel<BN>;
+    auto kern = mxfp8_gemm_kernel<BN, SF_VEC>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, A->scales, A->lds, B->scales,
-                                                        B->lds, C, ldc, M, N, K, ctx.err,
+                                                        B->lds, C, ldc, c_vec, M, N, K, ctx.err,
                                                         ctx.timeout_ns);
     return cudaGetLastError();
 }
@@ -284,8 +321,15 @@ namespace qgi {
 
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                          const LaunchCtx &ctx, bool *encode_ok) {
-    if (B->rows > 128) return launch_bn<256>(A, B, C, ldc, ctx, encode_ok);
-    return launch_bn<128>(A, B, C, ldc, ctx, encode_ok);
+    auto al4 = [](const qgemm_tensor *t) {
+        return reinterpret_cast<uintptr_t>(t->scales) % 4 == 0 && t->lds % 4 == 0;
+    };
+    const bool vec = al4(A) && al4(B);
+    if (B->rows > 128)
+        return vec ? launch_bn<256, true>(A, B, C, ldc, ctx, encode_ok)
+                   : launch_bn<256, false>(A, B, C, ldc, ctx, encode_ok);
+    return vec ? launch_bn<128, true>(A, B, C, ldc, ctx, encode_ok)
+               : launch_bn<128, false>(A, B, C, ldc, ctx, encode_ok);
 }
 
 }  // namespace qgi

@@ -31,14 +31,15 @@ __device__ __forceinline__ uint8_t *align_1024(uint8_t *p) {
 }
 
 // Write 32 consecutive fp32 accumulators of one output row as fp16 to crow[col0 .. col0 + 31],
-// masking columns >= N.  crow is 16-byte aligned whenever col0 is a multiple of 8.
-__device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
+// masking columns >= N.  `vec` says crow + col0 is 16-byte aligned (C 16-byte aligned and its
+// row stride a multiple of 8 elements); otherwise 2-byte stores are used.
+__device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N, bool vec,
                                                   const uint32_t (&v)[32]) {
     uint32_t p[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) p[i] = pack_f16x2(__uint_as_float(v[2 * i]),
                                                    __uint_as_float(v[2 * i + 1]));
-    if (col0 + 32 <= N) {
+    if (vec && col0 + 32 <= N) {
         uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2],

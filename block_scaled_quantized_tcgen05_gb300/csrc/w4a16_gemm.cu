@@ -116,10 +116,11 @@ __device__ __forceinline__ void i4x8_to_f16(uint32_t v, uint32_t s2, uint32_t (&
     o[3] = __byte_perm(h2, h3, 0x7632);  // (q6, q7)
 }
 
+template <bool SF_VEC>
 __global__ void __launch_bounds__(THREADS, 1)
 w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__restrict__ W,
                   int64_t ldw, const uint8_t *__restrict__ SW, int64_t ldsw,
-                  __half *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned *err,
+                  __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, unsigned *err,
                   uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
@@ -251,7 +252,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
                 tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, v);
+                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
             }
             tc_fence_before();
             mbar_arrive(tmem_empty);
@@ -281,8 +282,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                     n = n < N ? n : N - 1;                      // rows past N are never stored
                     const uint8_t *src = W + static_cast<int64_t>(n) * ldw + kt * (BK / 2) + 16 * h;
                     cp_async_16(rs + (i * CONV_THREADS + ct) * 16, src);
-                    const uint8_t *ssrc = SW + static_cast<int64_t>(n) * ldsw + (blk & ~3);
-                    cp_async_4_full(rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4, ssrc);
+                    if constexpr (SF_VEC) {
+                        // the aligned scale word holding this block's byte
+                        const uint8_t *ssrc = SW + static_cast<int64_t>(n) * ldsw + (blk & ~3);
+                        cp_async_4_full(rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4, ssrc);
+                    }
                 }
             }
             cp_async_commit();
@@ -301,12 +305,24 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             const uint8_t *rs = smem + OFF_RAW + (it % RAW) * RAW_SLOT_BYTES;
             const uint32_t sB = sb + OFF_B + stage * B_BYTES;
             const int blk = kt * 2 + h;
+            int nb_cur = 0;
+            if constexpr (!SF_VEC) {
+                int mb_cur;
+                tile_coords(blockIdx.x + (it / KT) * gridDim.x, tiles_m, tiles_n, mb_cur, nb_cur);
+            }
 #pragma unroll
             for (int i = 0; i < UNITS; ++i) {
                 const uint4 d = *reinterpret_cast<const uint4 *>(rs + (i * CONV_THREADS + ct) * 16);
-                const uint32_t sw = *reinterpret_cast<const uint32_t *>(
-                    rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4);
-                const uint32_t e = (sw >> (8 * (blk & 3))) & 0xFF;
+                uint32_t e;
+                if constexpr (SF_VEC) {
+                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(
+                        rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4);
+                    e = (sw >> (8 * (blk & 3))) & 0xFF;
+                } else {
+                    int n = nb_cur * BN + 64 * i + rsub;
+                    n = n < N ? n : N - 1;
+                    e = __ldg(SW + static_cast<int64_t>(n) * ldsw + blk);
+                }
                 const uint32_t s2 = ue8m0_to_f16x2(e);
                 const int r = 64 * i + rsub;                     // row inside the 256-row tile
                 const uint32_t words[4] = {d.x, d.y, d.z, d.w};
@@ -350,13 +366,16 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
     *encode_ok = encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const bool sf_vec = reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0;
+    auto kern = sf_vec ? w4a16_gemm_kernel<true> : w4a16_gemm_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-    w4a16_gemm_kernel<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmA, W->data, W->ld, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    kern<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(tmA, W->data, W->ld, W->scales, W->lds, C,
+                                                    ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -104,7 +104,7 @@ def test_compute_calls_reject_before_launch(lib):
     assert lib.qgemm_mxfp8(a, b2, C, 256, None) == 1            # K mismatch
     assert lib.qgemm_mxfp8(a, w8, C, 256, None) == 4            # dtype
     assert lib.qgemm_mxfp8(a, b, C, 128, None) == 1             # ldc < N
-    assert lib.qgemm_mxfp8(a, b, ctypes.c_void_p(FAKE + 2), 256, None) == 3   # C misaligned
+    assert lib.qgemm_mxfp8(a, b, ctypes.c_void_p(FAKE + 1), 256, None) == 3   # C misaligned
     assert lib.qgemm_mxfp8(a, misal, C, 256, None) == 3         # data misaligned
     assert lib.qgemm_mxfp8(None, b, C, 256, None) == 1
     assert lib.gemm_f16(C, 20, C, 256, C, 256, 16, 256, 20, None) == 3        # lda % 8
