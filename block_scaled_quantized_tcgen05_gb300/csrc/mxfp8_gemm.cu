@@ -9,13 +9,16 @@
 //
 // One persistent CTA per SM walks output tiles of 128 x BN.  Warp roles:
 //   warp 0     producer: TMA loads of the A / B k-tiles (128 B of K per row, 128-byte swizzle)
-//              and cp.async loads of their scale bytes, rearranged on the fly into the
-//              32-row x 16-byte layout that tcgen05.cp.32x128b.warpx4 expects.
+//              and of their scale bytes, which it lays out per k-tile in the 32-line x 16-byte
+//              form that tcgen05.cp.32x128b.warpx4 copies into TMEM (line i, word c = row
+//              32 c + i of a 128-row group).
 //   warp 1     TMEM owner and MMA issuer: per k-tile it copies the scale bytes into TMEM,
 //              then issues four 128 x BN x 32 block-scaled MMAs (scale-factor id = K step).
 //   warps 2-5  epilogue: TMEM -> registers -> fp16 (round to nearest even) -> global.
-// Stages are handed over with mbarriers (full: TMA bytes + 32 cp.async arrivals; empty:
-// tcgen05.commit).  Every wait is bounded by the caller's timeout.
+// Scale bytes reach shared memory by one of three routes, chosen from the scale planes'
+// alignment: SFM_TMA (16-byte aligned rows: one 16-byte x rows TMA box per 4 k-tiles, staged
+// twice-buffered and rearranged from registers), SFM_CPASYNC (4-byte aligned: 4-byte cp.async per
+// row and k-tile), SFM_BYTES (any alignment: byte loads).  Every wait is bounded.
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -30,6 +33,9 @@ constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;           // TMEM column of the first scale-factor slot
 constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA: 4 columns, SFB: 4 per 128 rows of B
+constexpr int SF_GROUP = 4;                 // k-tiles per 16-byte scale group (SFM_TMA)
+
+enum { SFM_BYTES = 0, SFM_CPASYNC = 1, SFM_TMA = 2 };
 
 template <int BN>
 struct Cfg {
@@ -38,16 +44,20 @@ struct Cfg {
     static constexpr uint32_t B_BYTES = BN * BK;
     static constexpr uint32_t SFA_BYTES = BM * 4;
     static constexpr uint32_t SFB_BYTES = BN * 4;
+    static constexpr uint32_t STG_A = BM * 16;     // one scale group of A (16 bytes per row)
+    static constexpr uint32_t STG_B = BN * 16;
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    // full[S], empty[S], tmem_full, tmem_empty, drain, then the TMEM address slot
-    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr uint32_t OFF_STG = OFF_SFB + STAGES * SFB_BYTES;   // 2 x (STG_A + STG_B)
+    static constexpr uint32_t OFF_BAR = OFF_STG + 2 * (STG_A + STG_B);
+    // full[S], empty[S], tmem_full, tmem_empty, drain, sf_full[2], then the TMEM address slot
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 5) * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
     static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(BN <= 256 && BN % 128 == 0, "BN");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 // Instruction descriptor, kind::mxf8f6f4: A, B E4M3 (format 0), K-major, D fp32 (implicit),
@@ -69,10 +79,28 @@ __device__ __forceinline__ uint32_t load_scale_word(const uint8_t *p, uint32_t n
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int j) {
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
 
-template <int BN, bool SF_VEC>
+template <int BN, int SFM>
 __global__ void __launch_bounds__(THREADS, 1)
 mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                   const uint8_t *__restrict__ sfa, int64_t lds_a, const uint8_t *__restrict__ sfb,
                   int64_t lds_b, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
                   unsigned *err, uint64_t timeout_ns) {
@@ -89,25 +117,33 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t tmem_full = sb + G::OFF_BAR + 8u * (2 * S);
     const uint32_t tmem_empty = tmem_full + 8;
     const uint32_t drain_bar = tmem_full + 16;
+    auto sf_full = [&](int i) { return tmem_full + 24 + 8u * i; };
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_SLOT);
 
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
     const int KT = (K + BK - 1) / BK;
-    const int nkb = K / 32;  // scale blocks per row
+    const int nkb = K / 32;                          // scale blocks per row
+    const int ngk = (KT + SF_GROUP - 1) / SF_GROUP;  // scale groups per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1 + 32);  // producer's expect_tx arrival + 32 cp.async arrivals
+            mbar_init(full_bar(s), 1 + 32);  // producer's expect_tx arrival + 32 scale arrivals
             mbar_init(empty_bar(s), 1);      // tcgen05.commit
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 128);          // every epilogue thread
         mbar_init(drain_bar, 1);
+        mbar_init(sf_full(0), 1);
+        mbar_init(sf_full(1), 1);
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (SFM == SFM_TMA) {
+            tma_prefetch_desc(&tmSA);
+            tma_prefetch_desc(&tmSB);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
@@ -122,12 +158,52 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ---------------------------------------------------------------- producer
         uint32_t stage = 0, phase = 0;
         int issued = 0;
+        int sf_issued = 0;       // scale groups requested (SFM_TMA), in CTA-local sequence
+        int sf_waited = 0;       // scale groups whose arrival this warp has observed
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        // Request scale group q (sequence over this CTA's tiles) into staging slot q & 1.
+        auto issue_sf = [&](int q) {
+            const int tile = blockIdx.x + (q / ngk) * gridDim.x;
+            if (tile >= num_tiles) return;
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            const int g = q % ngk;
+            const uint32_t stg = sb + G::OFF_STG + (q & 1) * (G::STG_A + G::STG_B);
+            mbar_arrive_expect_tx(sf_full(q & 1), G::STG_A + G::STG_B);
+            tma_load_2d(stg, &tmSA, sf_full(q & 1), 16 * g, mb * BM);
+            tma_load_2d(stg + G::STG_A, &tmSB, sf_full(q & 1), 16 * g, nb * BN);
+            sf_issued = q + 1;
+        };
+        uint4 ra[4], rb[BN / 128][4];   // current scale group, lines lane + 32 c (+ 128 h)
+        int tile_iter = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tile_iter) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const int m0 = mb * BM, n0 = nb * BN;
             for (int kt = 0; kt < KT; ++kt) {
+                if constexpr (SFM == SFM_TMA) {
+                    if (kt % SF_GROUP == 0) {
+                        const int q = tile_iter * ngk + kt / SF_GROUP;
+                        if (lane == 0) {
+                            if (q == 0) issue_sf(0);
+                            issue_sf(q + 1);      // prefetch the next group (maybe next tile)
+                        }
+                        if (!mbar_wait(sf_full(q & 1), (q >> 1) & 1, timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        sf_waited = q + 1;
+                        const uint32_t stg = sb + G::OFF_STG + (q & 1) * (G::STG_A + G::STG_B);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) ra[c] = ld_shared_v4(stg + (lane + 32 * c) * 16);
+#pragma unroll
+                        for (int h = 0; h < BN / 128; ++h)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                rb[h][c] = ld_shared_v4(stg + G::STG_A +
+                                                        (lane + 32 * c + 128 * h) * 16);
+                    }
+                }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
                     ok = false;
                     break;
@@ -145,7 +221,18 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t nbytes = static_cast<uint32_t>(min(4, nkb - kb0));
                 const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
                 const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
-                if constexpr (SF_VEC) {
+                if constexpr (SFM == SFM_TMA) {
+                    const int j = kt % SF_GROUP;
+                    st_shared_v4(sSFA + lane * 16, word_of(ra[0], j), word_of(ra[1], j),
+                                 word_of(ra[2], j), word_of(ra[3], j));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        st_shared_v4(sSFB + h * 512 + lane * 16, word_of(rb[h][0], j),
+                                     word_of(rb[h][1], j), word_of(rb[h][2], j),
+                                     word_of(rb[h][3], j));
+                    fence_proxy_async_smem();
+                    mbar_arrive(full_bar(stage));
+                } else if constexpr (SFM == SFM_CPASYNC) {
                     // 4-byte aligned scale rows: asynchronous copies, arrival when they land
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -171,7 +258,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int r = m0 + 32 * c + static_cast<int>(lane);
-                        const uint32_t w = r < M ? load_scale_word(sfa + static_cast<int64_t>(r) * lds_a + kb0, nbytes) : 0u;
+                        const uint32_t w =
+                            r < M ? load_scale_word(sfa + static_cast<int64_t>(r) * lds_a + kb0, nbytes) : 0u;
                         st_shared_u32(sSFA + lane * 16 + c * 4, w);
                     }
 #pragma unroll
@@ -179,7 +267,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
-                            const uint32_t w = r < N ? load_scale_word(sfb + static_cast<int64_t>(r) * lds_b + kb0, nbytes) : 0u;
+                            const uint32_t w =
+                                r < N ? load_scale_word(sfb + static_cast<int64_t>(r) * lds_b + kb0, nbytes) : 0u;
                             st_shared_u32(sSFB + h * 512 + lane * 16 + c * 4, w);
                         }
                     }
@@ -201,6 +290,15 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
         }
+        if constexpr (SFM == SFM_TMA) {
+            // groups requested but never waited for (at most the one prefetched ahead)
+            const int last = __shfl_sync(0xffffffffu, sf_issued, 0);
+            for (int q = sf_waited; q < last; ++q)
+                if (!mbar_wait(sf_full(q & 1), (q >> 1) & 1, timeout_ns)) {
+                    if (lane == 0) atomicOr(err, ERR_DRAIN);
+                    break;
+                }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
         uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -219,7 +317,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.cp reads
+                    if constexpr (SFM == SFM_CPASYNC)
+                        fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.cp reads
                     const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
                     const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
                     const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
@@ -290,29 +389,47 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int BN, bool SF_VEC>
+template <int BN, int SFM>
 cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                       const qgi::LaunchCtx &ctx, bool *encode_ok) {
     using G = Cfg<BN>;
     const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
               K = static_cast<int>(A->k);
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmSA, tmSB;
     *encode_ok = qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, K, M, A->ld, BK,
                                     BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
                  qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, K, N, B->ld, BK,
                                     BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (*encode_ok && SFM == SFM_TMA)
+        *encode_ok = qgi::encode_tma_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->scales, K / 32, M,
+                                        A->lds, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                     qgi::encode_tma_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->scales, K / 32, N,
+                                        B->lds, 16, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+        tmSA = tmA, tmSB = tmB;   // unused by the other scale routes
     if (!*encode_ok) return cudaErrorInvalidValue;
-    auto kern = mxfp8_gemm_kernel<BN, SF_VEC>;
+    auto kern = mxfp8_gemm_kernel<BN, SFM>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
-    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, A->scales, A->lds, B->scales,
-                                                        B->lds, C, ldc, c_vec, M, N, K, ctx.err,
-                                                        ctx.timeout_ns);
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, tmSA, tmSB, A->scales, A->lds,
+                                                        B->scales, B->lds, C, ldc, c_vec, M, N, K,
+                                                        ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_sfm(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                       const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    auto al = [](const qgemm_tensor *t, int a) {
+        return reinterpret_cast<uintptr_t>(t->scales) % a == 0 && t->lds % a == 0;
+    };
+    if (al(A, 16) && al(B, 16)) return launch_bn<BN, SFM_TMA>(A, B, C, ldc, ctx, encode_ok);
+    if (al(A, 4) && al(B, 4)) return launch_bn<BN, SFM_CPASYNC>(A, B, C, ldc, ctx, encode_ok);
+    return launch_bn<BN, SFM_BYTES>(A, B, C, ldc, ctx, encode_ok);
 }
 
 }  // namespace
@@ -321,15 +438,8 @@ namespace qgi {
 
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                          const LaunchCtx &ctx, bool *encode_ok) {
-    auto al4 = [](const qgemm_tensor *t) {
-        return reinterpret_cast<uintptr_t>(t->scales) % 4 == 0 && t->lds % 4 == 0;
-    };
-    const bool vec = al4(A) && al4(B);
-    if (B->rows > 128)
-        return vec ? launch_bn<256, true>(A, B, C, ldc, ctx, encode_ok)
-                   : launch_bn<256, false>(A, B, C, ldc, ctx, encode_ok);
-    return vec ? launch_bn<128, true>(A, B, C, ldc, ctx, encode_ok)
-               : launch_bn<128, false>(A, B, C, ldc, ctx, encode_ok);
+    if (B->rows > 128) return launch_sfm<256>(A, B, C, ldc, ctx, encode_ok);
+    return launch_sfm<128>(A, B, C, ldc, ctx, encode_ok);
 }
 
 }  // namespace qgi

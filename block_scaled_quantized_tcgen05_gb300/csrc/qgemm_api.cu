@@ -344,8 +344,8 @@ qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgem
         if (ldx < K) return fail(QGEMM_ERR_INVALID_ARG, "ldx < K");
         if (!aligned(X_f16, 16) || ldx % 8)
             return fail(QGEMM_ERR_MISALIGNED, "X must be 16-byte aligned, ldx %% 8 == 0");
-        if (!aligned(W->data, 8) || W->ld % 8)
-            return fail(QGEMM_ERR_MISALIGNED, "int8 data must be 8-byte aligned, stride %% 8 == 0");
+        if (!aligned(W->data, 16) || W->ld % 16)
+            return fail(QGEMM_ERR_MISALIGNED, "int8 data must be 16-byte aligned, stride %% 16 == 0");
     }
     qgi::LaunchCtx ctx;
     qgemm_status st = get_ctx(stream, &ctx);
@@ -355,8 +355,10 @@ qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgem
         e = qgi::launch_fill_zero_f16(static_cast<__half *>(Y_f16), ldy, M, N, ctx);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
     }
+    bool enc = true;
     e = qgi::launch_w8_gemv(static_cast<const __half *>(X_f16), ldx, (int)M, W,
-                            static_cast<__half *>(Y_f16), ldy, ctx);
+                            static_cast<__half *>(Y_f16), ldy, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w8_gemv launch");
 }
 

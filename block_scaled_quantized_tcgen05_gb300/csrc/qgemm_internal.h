@@ -47,7 +47,7 @@ cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64
 cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
                          int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
-                           __half *Y, int64_t ldy, const LaunchCtx &ctx);
+                           __half *Y, int64_t ldy, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);
 cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
                                  const LaunchCtx &ctx);

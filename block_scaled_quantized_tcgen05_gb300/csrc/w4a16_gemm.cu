@@ -11,7 +11,7 @@
 //   warp 0     TMA producer for the activation tile A (128 rows x 64 k, 128-byte swizzle).
 //   warp 1     TMEM owner + MMA issuer (kind::f16, both operands K-major).
 //   warps 2-5  epilogue (TMEM -> fp16 -> global).
-//   warps 6-9  converters: cp.async the packed int4 bytes and scale words of future k-tiles into
+//   warps 6-13 converters: cp.async the packed int4 bytes and scale words of future k-tiles into
 //              a private ring (each thread consumes only what it copied), then per 32-block
 //              turn 32 nibbles into fp16 (q + 8 placed in the mantissa of 1024, minus 1032; the
 //              high nibble as 1024 + 16 (q + 8), times 1/16, minus 72), multiply by the fp16
@@ -30,10 +30,10 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int RAW = 3;            // k-tiles of int4 prefetched ahead by each converter thread
-constexpr int CONV_THREADS = 128;
+constexpr int CONV_THREADS = 256;
 constexpr int THREADS = 192 + CONV_THREADS;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr int UNITS = 4;          // (row, 32-block) units per converter thread per k-tile
+constexpr int UNITS = 2;          // (row, 32-block) units per converter thread per k-tile
 
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
@@ -92,6 +92,32 @@ __device__ __forceinline__ uint32_t ue8m0_to_f16x2(uint32_t e) {
     else if (x >= -24) h = 1u << (x + 24);
     else h = 0u;
     return h | (h << 16);
+}
+
+// Fused path, exact for scale exponents x = e - 127 in [-10, 5]: byte j of the biased word is
+// spread to both halves, the low nibble as 1024 + u and the high nibble as 1024 + 16 u, and one
+// fp16x2 FMA with per-half constants (s, s/16) and (-1032 s, -72 s) gives (q_lo s, q_hi s).
+__device__ __forceinline__ bool fused_ok(uint32_t e) { return e >= 117u && e <= 132u; }
+
+__device__ __forceinline__ void fused_consts(uint32_t e, uint32_t &s2, uint32_t &c2) {
+    const uint32_t x15 = e - 112u;                          // x + 15
+    const uint32_t s = x15 << 10, s16 = (x15 - 4u) << 10;   // 2^x, 2^(x-4)
+    const uint32_t c1032 = 0x8000u | ((x15 + 10u) << 10) | 8u;    // -1032 * 2^x
+    const uint32_t c72 = 0x8000u | ((x15 + 6u) << 10) | 128u;     // -72 * 2^x
+    s2 = s | (s16 << 16);
+    c2 = c1032 | (c72 << 16);
+}
+
+__device__ __forceinline__ void i4x8_to_f16_fused(uint32_t v, uint32_t s2, uint32_t c2,
+                                                  uint32_t (&o)[4]) {
+    const uint32_t u = v ^ 0x88888888u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = __byte_perm(u, 0u, 0x4040u | (j << 8) | j);   // byte j in both halves
+        uint32_t tv;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(tv) : "r"(b), "r"(0x00F0000Fu), "r"(0x64006400u));
+        o[j] = h2_fma(tv, s2, c2);
+    }
 }
 
 // 8 int4 (one 32-bit word, k = 8w .. 8w+7, even k in low nibbles) times the fp16x2 scale ->
@@ -260,14 +286,14 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
         }
     } else {
         // ----------------------------------------------------------------- converters
-        const int ct = static_cast<int>(threadIdx.x) - 192;   // 0..127
+        const int ct = static_cast<int>(threadIdx.x) - 192;   // 0..CONV_THREADS-1
         const int h = ct & 1;                                   // which 32-block of the k-tile
-        const int rsub = ct >> 1;                               // row within each 64-row group
+        const int rsub = ct >> 1;                               // row within each row group
+        constexpr int ROW_STEP = CONV_THREADS / 2;              // rows between a thread's units
         const int my_tiles = (num_tiles > static_cast<int>(blockIdx.x))
                                  ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                                  : 0;
         const int total = my_tiles * KT;
-        // Issue the copies of iteration `it` (tile index, k-tile) into raw slot it % RAW.
         auto issue = [&](int it) {
             if (it < total) {
                 const int tile = blockIdx.x + (it / KT) * gridDim.x;
@@ -278,7 +304,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                 const int blk = kt * 2 + h;                     // scale block index along K
 #pragma unroll
                 for (int i = 0; i < UNITS; ++i) {
-                    int n = nb * BN + 64 * i + rsub;
+                    int n = nb * BN + ROW_STEP * i + rsub;
                     n = n < N ? n : N - 1;                      // rows past N are never stored
                     const uint8_t *src = W + static_cast<int64_t>(n) * ldw + kt * (BK / 2) + 16 * h;
                     cp_async_16(rs + (i * CONV_THREADS + ct) * 16, src);
@@ -319,17 +345,21 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                         rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4);
                     e = (sw >> (8 * (blk & 3))) & 0xFF;
                 } else {
-                    int n = nb_cur * BN + 64 * i + rsub;
+                    int n = nb_cur * BN + ROW_STEP * i + rsub;
                     n = n < N ? n : N - 1;
                     e = __ldg(SW + static_cast<int64_t>(n) * ldsw + blk);
                 }
-                const uint32_t s2 = ue8m0_to_f16x2(e);
-                const int r = 64 * i + rsub;                     // row inside the 256-row tile
+                const int r = ROW_STEP * i + rsub;               // row inside the 256-row tile
                 const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+                const bool fast = fused_ok(e);
+                uint32_t s2, c2;
+                if (fast) fused_consts(e, s2, c2);
+                else s2 = ue8m0_to_f16x2(e);
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t o[4];
-                    i4x8_to_f16(words[w], s2, o);
+                    if (fast) i4x8_to_f16_fused(words[w], s2, c2, o);
+                    else i4x8_to_f16(words[w], s2, o);
                     const int c = 4 * h + w;                     // 16-byte chunk (8 k) in the row
                     const uint32_t dst = sB + r * 128 + ((c ^ (r & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]),

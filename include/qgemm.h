@@ -148,7 +148,7 @@ qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_
  *   W   QGEMM_INT8 view [N, K] with UE8M0 scales [N, K / 32].
  *   Y   device fp16 [M, N], row stride ldy elements.
  * Requirements: 1 <= M <= 16; K % 32 == 0; X 16-byte aligned, ldx multiple of 8; W data and row
- * stride 8-byte aligned; Y 2-byte aligned.
+ * stride 16-byte aligned; scale plane any alignment; Y 2-byte aligned.
  * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA. */
 qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
                            void *Y_f16, int64_t ldy, void *stream);
