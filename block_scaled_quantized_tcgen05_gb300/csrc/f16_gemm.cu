@@ -30,9 +30,11 @@ struct Cfg {
     static constexpr uint32_t B_BYTES = (BN / 64) * B_ATOM_BYTES;
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_BYTES;   // 4 warps x 2 KB
+    static constexpr uint32_t OFF_BAR = OFF_EPI + 4 * 2048;
     static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (format 0),
@@ -181,17 +183,8 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 break;
             }
             tc_fence_after();
-            const int row = mb * BM + static_cast<int>(q * 32 + lane);
-            __half *crow = C + static_cast<int64_t>(row) * ldc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
-                tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
-            }
-            tc_fence_before();
-            mbar_arrive(tmem_empty);
+            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty, sb + G::OFF_EPI + (warp - 2) * 2048);
             acc_phase ^= 1;
         }
     }

@@ -16,7 +16,7 @@
 //              then issues four 128 x BN x 32 block-scaled MMAs (scale-factor id = K step).
 //   warps 2-5  epilogue: TMEM -> registers -> fp16 (round to nearest even) -> global.
 // Scale bytes reach shared memory by one of three routes, chosen from the scale planes'
-// alignment: SFM_TMA (16-byte aligned rows: one 16-byte x rows TMA box per 4 k-tiles, staged
+// alignment: SFM_TMA (16-byte aligned rows: one 32-byte x rows TMA box per 8 k-tiles, staged
 // twice-buffered and rearranged from registers), SFM_CPASYNC (4-byte aligned: 4-byte cp.async per
 // row and k-tile), SFM_BYTES (any alignment: byte loads).  Every wait is bounded.
 #include "qgemm_common.cuh"
@@ -33,7 +33,14 @@ constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;           // TMEM column of the first scale-factor slot
 constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA: 4 columns, SFB: 4 per 128 rows of B
-constexpr int SF_GROUP = 4;                 // k-tiles per 16-byte scale group (SFM_TMA)
+#ifndef QG_MX_SF_GROUP
+#define QG_MX_SF_GROUP 8
+#endif
+#ifndef QG_MX_EPI_STAGED
+#define QG_MX_EPI_STAGED 0
+#endif
+constexpr int SF_GROUP = QG_MX_SF_GROUP;    // k-tiles per scale group (SFM_TMA): 4 or 8
+constexpr uint32_t SF_ROW = SF_GROUP * 4;   // bytes of one row's scales per group
 
 enum { SFM_BYTES = 0, SFM_CPASYNC = 1, SFM_TMA = 2 };
 
@@ -44,14 +51,15 @@ struct Cfg {
     static constexpr uint32_t B_BYTES = BN * BK;
     static constexpr uint32_t SFA_BYTES = BM * 4;
     static constexpr uint32_t SFB_BYTES = BN * 4;
-    static constexpr uint32_t STG_A = BM * 16;     // one scale group of A (16 bytes per row)
-    static constexpr uint32_t STG_B = BN * 16;
+    static constexpr uint32_t STG_A = BM * SF_ROW;  // one scale group of A
+    static constexpr uint32_t STG_B = BN * SF_ROW;
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr uint32_t OFF_STG = OFF_SFB + STAGES * SFB_BYTES;   // 2 x (STG_A + STG_B)
-    static constexpr uint32_t OFF_BAR = OFF_STG + 2 * (STG_A + STG_B);
+    static constexpr uint32_t OFF_EPI = OFF_STG + 2 * (STG_A + STG_B);   // 4 warps x 2 KB
+    static constexpr uint32_t OFF_BAR = OFF_EPI + (QG_MX_EPI_STAGED ? 4 * 2048 : 0);
     // full[S], empty[S], tmem_full, tmem_empty, drain, sf_full[2], then the TMEM address slot
     static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 5) * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
@@ -170,8 +178,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int g = q % ngk;
             const uint32_t stg = sb + G::OFF_STG + (q & 1) * (G::STG_A + G::STG_B);
             mbar_arrive_expect_tx(sf_full(q & 1), G::STG_A + G::STG_B);
-            tma_load_2d(stg, &tmSA, sf_full(q & 1), 16 * g, mb * BM);
-            tma_load_2d(stg + G::STG_A, &tmSB, sf_full(q & 1), 16 * g, nb * BN);
+            tma_load_2d(stg, &tmSA, sf_full(q & 1), SF_ROW * g, mb * BM);
+            tma_load_2d(stg + G::STG_A, &tmSB, sf_full(q & 1), SF_ROW * g, nb * BN);
             sf_issued = q + 1;
         };
         uint4 ra[4], rb[BN / 128][4];   // current scale group, lines lane + 32 c (+ 128 h)
@@ -182,8 +190,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int m0 = mb * BM, n0 = nb * BN;
             for (int kt = 0; kt < KT; ++kt) {
                 if constexpr (SFM == SFM_TMA) {
+                    const int q = tile_iter * ngk + kt / SF_GROUP;
                     if (kt % SF_GROUP == 0) {
-                        const int q = tile_iter * ngk + kt / SF_GROUP;
                         if (lane == 0) {
                             if (q == 0) issue_sf(0);
                             issue_sf(q + 1);      // prefetch the next group (maybe next tile)
@@ -193,15 +201,19 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             break;
                         }
                         sf_waited = q + 1;
-                        const uint32_t stg = sb + G::OFF_STG + (q & 1) * (G::STG_A + G::STG_B);
+                    }
+                    if (kt % 4 == 0) {
+                        // 16 bytes (4 k-tiles) of each row of the current group
+                        const uint32_t stg = sb + G::OFF_STG + (q & 1) * (G::STG_A + G::STG_B) +
+                                             16 * ((kt % SF_GROUP) / 4);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) ra[c] = ld_shared_v4(stg + (lane + 32 * c) * 16);
+                        for (int c = 0; c < 4; ++c) ra[c] = ld_shared_v4(stg + (lane + 32 * c) * SF_ROW);
 #pragma unroll
                         for (int h = 0; h < BN / 128; ++h)
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
                                 rb[h][c] = ld_shared_v4(stg + G::STG_A +
-                                                        (lane + 32 * c + 128 * h) * 16);
+                                                        (lane + 32 * c + 128 * h) * SF_ROW);
                     }
                 }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
@@ -222,7 +234,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
                 const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
                 if constexpr (SFM == SFM_TMA) {
-                    const int j = kt % SF_GROUP;
+                    const int j = kt % 4;
                     st_shared_v4(sSFA + lane * 16, word_of(ra[0], j), word_of(ra[1], j),
                                  word_of(ra[2], j), word_of(ra[3], j));
 #pragma unroll
@@ -368,17 +380,9 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            const int row = mb * BM + static_cast<int>(q * 32 + lane);
-            __half *crow = C + static_cast<int64_t>(row) * ldc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
-                tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
-            }
-            tc_fence_before();
-            mbar_arrive(tmem_empty);
+            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty,
+                              QG_MX_EPI_STAGED ? sb + G::OFF_EPI + (warp - 2) * 2048 : 0u);
             acc_phase ^= 1;
         }
     }
@@ -402,9 +406,9 @@ cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, i
                                     BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (*encode_ok && SFM == SFM_TMA)
         *encode_ok = qgi::encode_tma_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->scales, K / 32, M,
-                                        A->lds, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                                        A->lds, SF_ROW, BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
                      qgi::encode_tma_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->scales, K / 32, N,
-                                        B->lds, 16, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+                                        B->lds, SF_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
     else
         tmSA = tmA, tmSB = tmB;   // unused by the other scale routes
     if (!*encode_ok) return cudaErrorInvalidValue;

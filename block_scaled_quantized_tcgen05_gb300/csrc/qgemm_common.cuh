@@ -52,4 +52,74 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
     }
 }
 
+// Drain one 128 x BN fp32 accumulator tile to fp16 global memory.  The warp reads its TMEM lane
+// quarter q (rows 32 q .. 32 q + 31 of the tile, one row per lane) 32 columns at a time.
+// Direct form: each lane stores its own row (16-byte stores).  Staged form (`stage` = 2 KB of
+// shared memory owned by this warp): the 32 x 32 fp16 chunk goes through shared memory (16-byte
+// chunks swizzled by row pair, conflict-free both ways) so that each store instruction writes
+// 8 rows x 64 contiguous bytes, i.e. whole 32-byte sectors.  The accumulator is released
+// (arrival on `tmem_empty`) after its last column has been read.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, uint32_t lane,
+                                              __half *C, int64_t ldc, int m0, int n0, int M,
+                                              int N, bool vec, uint32_t tmem_empty,
+                                              uint32_t stage) {
+    const int row = m0 + static_cast<int>(q * 32 + lane);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+        }
+        const int col0 = n0 + ch * 32;
+        if (stage == 0u || !vec) {
+            if (row < M) store_row_chunk32(C + static_cast<int64_t>(row) * ldc, col0, N, vec, v);
+            continue;
+        }
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            p[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t a = stage + lane * 64 + ((j ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(p[4 * j]),
+                         "r"(p[4 * j + 1]), "r"(p[4 * j + 2]), "r"(p[4 * j + 3])
+                         : "memory");
+        }
+        __syncwarp();
+        const uint32_t c16 = lane & 3;           // 16-byte chunk of the row this lane stores
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t r = (lane >> 2) + 8 * i;                    // row within the 32
+            uint4 w;
+            const uint32_t a = stage + r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                         : "r"(a)
+                         : "memory");
+            const int grow = m0 + static_cast<int>(q * 32 + r);
+            const int gcol = col0 + static_cast<int>(8 * c16);
+            if (grow < M) {
+                __half *dst = C + static_cast<int64_t>(grow) * ldc + gcol;
+                if (gcol + 8 <= N) {
+                    *reinterpret_cast<uint4 *>(dst) = w;
+                } else {
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (gcol + e < N)
+                            reinterpret_cast<uint16_t *>(dst)[e] =
+                                static_cast<uint16_t>((ww[e >> 1] >> ((e & 1) * 16)) & 0xFFFF);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace qg

@@ -271,17 +271,8 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                 break;
             }
             tc_fence_after();
-            const int row = mb * BM + static_cast<int>(q * 32 + lane);
-            __half *crow = C + static_cast<int64_t>(row) * ldc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
-                tmem_wait_ld();
-                if (row < M) store_row_chunk32(crow, nb * BN + ch * 32, N, c_vec != 0, v);
-            }
-            tc_fence_before();
-            mbar_arrive(tmem_empty);
+            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty, 0u);
             acc_phase ^= 1;
         }
     } else {
@@ -385,6 +376,252 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ------------------------------------------------------------------------------------------
+// TMA-fed variant (weights and scale rows 16-byte aligned).  The producer also loads the packed
+// int4 tile of each k-tile (256 rows x 32 bytes, into the last 8 KB of that stage's fp16 B
+// buffer) and, every 8 k-tiles, the 16 scale bytes per row that cover them (into one of two
+// staging slots).  Converter threads read their two (row, 32-block) units and scale bytes from
+// shared memory, meet at a named barrier (all packed bytes read before anyone overwrites the
+// buffer), then write the dequantised fp16 tile over the whole buffer.
+constexpr int T_CONV = 256;
+constexpr int T_THREADS = 192 + T_CONV;
+constexpr int T_UNITS = 2;
+constexpr int T_SF_GROUP = 8;                          // k-tiles per 16-byte scale group
+constexpr uint32_t T_RAW_BYTES = BN * (BK / 2);        // 8 KB packed int4 per k-tile
+constexpr uint32_t T_RAW_OFF = B_BYTES - T_RAW_BYTES;  // inside the stage's B buffer
+constexpr uint32_t T_STG = BN * 16;                    // 4 KB scale group
+constexpr uint32_t T_OFF_STG = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t T_OFF_EPI = T_OFF_STG + 2 * T_STG;   // 4 epilogue warps x 2 KB
+constexpr uint32_t T_OFF_BAR = T_OFF_EPI + 4 * 2048;
+// raw_full[S], conv_full[S], empty[S], tmem_full, tmem_empty, drain, then the TMEM slot
+constexpr uint32_t T_OFF_SLOT = T_OFF_BAR + (3 * STAGES + 3) * 8;
+constexpr uint32_t T_SMEM_BYTES = T_OFF_SLOT + 16 + 1024;
+static_assert(T_SMEM_BYTES <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(T_THREADS, 1)
+w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                 const __grid_constant__ CUtensorMap tmS, __half *__restrict__ C, int64_t ldc,
+                 int c_vec, int M, int N, int K, unsigned *err, uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    auto raw_full = [&](int s) { return sb + T_OFF_BAR + 8u * s; };
+    auto conv_full = [&](int s) { return sb + T_OFF_BAR + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return sb + T_OFF_BAR + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = sb + T_OFF_BAR + 8u * (3 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + T_OFF_SLOT);
+
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = K / BK;
+    const int ngk = (KT + T_SF_GROUP - 1) / T_SF_GROUP;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(raw_full(s), 1);          // producer's expect_tx arrival
+            mbar_init(conv_full(s), T_CONV);    // every converter thread
+            mbar_init(empty_bar(s), 1);         // tcgen05.commit
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmS);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        // ------------------------------------------- producer: A, packed W, scale groups
+        uint32_t stage = 0, phase = 0;
+        int issued = 0;
+        bool ok = true;
+        int tile_iter = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tile_iter) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const bool grp = (kt % T_SF_GROUP) == 0;
+                    const int q = tile_iter * ngk + kt / T_SF_GROUP;
+                    const uint32_t sB = sb + OFF_B + stage * B_BYTES;
+                    mbar_arrive_expect_tx(raw_full(stage),
+                                          A_BYTES + T_RAW_BYTES + (grp ? T_STG : 0u));
+                    tma_load_2d(sb + OFF_A + stage * A_BYTES, &tmA, raw_full(stage), kt * BK,
+                                mb * BM);
+                    tma_load_2d(sB + T_RAW_OFF, &tmW, raw_full(stage), kt * (BK / 2), nb * BN);
+                    if (grp)
+                        tma_load_2d(sb + T_OFF_STG + (q & 1) * T_STG, &tmS, raw_full(stage),
+                                    16 * (kt / T_SF_GROUP), nb * BN);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+        for (int i = max(0, issued - STAGES); i < issued; ++i) {
+            if (!mbar_wait(raw_full(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(raw_full(stage), phase, timeout_ns) ||
+                    !mbar_wait(conv_full(stage), phase, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t adesc = smem_desc(sb + OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
+                    const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
+#pragma unroll
+                    for (uint32_t j = 0; j < BK / 16; ++j)
+                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 2 * j, IDESC,
+                                (kt > 0 || j > 0) ? 1u : 0u);
+                    tc_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(tmem_full);
+            __syncwarp();
+            acc_phase ^= 1;
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
+        if (lane == 0) tc_commit(drain_bar);
+        __syncwarp();
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------- epilogue
+        const uint32_t q = warp & 3;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty, sb + T_OFF_EPI + (warp - 2) * 2048);
+            acc_phase ^= 1;
+        }
+    } else {
+        // ----------------------------------------------------------------- converters
+        const int ct = static_cast<int>(threadIdx.x) - 192;     // 0 .. T_CONV-1
+        const int h = ct & 1;                                     // 32-block of the k-tile
+        const int rsub = ct >> 1;                                 // rows rsub, rsub + 128
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        int tile_iter = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tile_iter) {
+            for (int kt = 0; kt < KT; ++kt) {
+                const bool got = mbar_wait(raw_full(stage), phase, timeout_ns);
+                const int qg = tile_iter * ngk + kt / T_SF_GROUP;
+                const uint8_t *stg = smem + T_OFF_STG + (qg & 1) * T_STG;
+                const uint8_t *bufp = smem + OFF_B + stage * B_BYTES;
+                const int sbyte = (kt % T_SF_GROUP) * 2 + h;     // scale byte within the group
+                uint4 d[T_UNITS];
+                uint32_t e[T_UNITS];
+#pragma unroll
+                for (int i = 0; i < T_UNITS; ++i) {
+                    const int r = rsub + 128 * i;
+                    if (got) {
+                        d[i] = *reinterpret_cast<const uint4 *>(bufp + T_RAW_OFF + r * 32 + 16 * h);
+                        e[i] = stg[r * 16 + sbyte];
+                    }
+                }
+                // Every converter has its packed bytes before the buffer is overwritten.  All of
+                // them always reach this barrier; if any wait ran out, all of them stop.
+                uint32_t all_ok;
+                asm volatile(
+                    "{\n\t.reg .pred p, q;\n\t"
+                    "setp.ne.u32 p, %1, 0;\n\t"
+                    "bar.red.and.pred q, 1, %2, p;\n\t"
+                    "selp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(all_ok)
+                    : "r"(got ? 1u : 0u), "n"(T_CONV)
+                    : "memory");
+                if (!all_ok) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sB = sb + OFF_B + stage * B_BYTES;
+#pragma unroll
+                for (int i = 0; i < T_UNITS; ++i) {
+                    const int r = rsub + 128 * i;
+                    const bool fast = fused_ok(e[i]);
+                    uint32_t s2, c2 = 0;
+                    if (fast) fused_consts(e[i], s2, c2);
+                    else s2 = ue8m0_to_f16x2(e[i]);
+                    const uint32_t words[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t o[4];
+                        if (fast) i4x8_to_f16_fused(words[w], s2, c2, o);
+                        else i4x8_to_f16(words[w], s2, o);
+                        const int c = 4 * h + w;
+                        const uint32_t dst = sB + r * 128 + ((c ^ (r & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(conv_full(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
 }  // namespace
 
 namespace qgi {
@@ -396,14 +633,31 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
     *encode_ok = encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    // TMA route: 16-byte aligned scale rows and whole 8-k-tile scale groups (K % 512 == 0), so a
+    // staging slot is never refilled while converters still read it.
+    if (reinterpret_cast<uintptr_t>(W->scales) % 16 == 0 && W->lds % 16 == 0 && K % 512 == 0) {
+        CUtensorMap tmW, tmS;
+        *encode_ok = encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K / 2, N, W->ld,
+                                   BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                     encode_tma_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->scales, K / 32, N,
+                                   W->lds, 16, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!*encode_ok) return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(w4a16_tma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             T_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        w4a16_tma_kernel<<<grid, T_THREADS, T_SMEM_BYTES, ctx.stream>>>(
+            tmA, tmW, tmS, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+        return cudaGetLastError();
+    }
     const bool sf_vec = reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0;
     auto kern = sf_vec ? w4a16_gemm_kernel<true> : w4a16_gemm_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     kern<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(tmA, W->data, W->ld, W->scales, W->lds, C,
                                                     ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
