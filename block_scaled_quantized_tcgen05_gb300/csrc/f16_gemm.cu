@@ -20,7 +20,7 @@ using namespace qg;
 constexpr int BM = 128;
 constexpr int BK = 64;         // fp16 elements of K per k-tile (one 128-byte swizzle row)
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+
 
 template <int BN>
 struct Cfg {
@@ -32,7 +32,8 @@ struct Cfg {
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_BYTES;   // 4 warps x 2 KB
     static constexpr uint32_t OFF_BAR = OFF_EPI + 4 * 2048;
-    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 5) * 8;
+    static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // two accumulators
     static constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -59,9 +60,11 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     auto full_bar = [&](int s) { return sb + G::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + G::OFF_BAR + 8u * (S + s); };
-    const uint32_t tmem_full = sb + G::OFF_BAR + 8u * (2 * S);
-    const uint32_t tmem_empty = tmem_full + 8;
-    const uint32_t drain_bar = tmem_full + 16;
+    // accumulator double buffer: tmem_full[2], tmem_empty[2], then the drain barrier
+    const uint32_t acc_bar0 = sb + G::OFF_BAR + 8u * (2 * S);
+    auto tmem_full = [&](uint32_t b) { return acc_bar0 + 8u * b; };
+    auto tmem_empty = [&](uint32_t b) { return acc_bar0 + 16u + 8u * b; };
+    const uint32_t drain_bar = acc_bar0 + 32;
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + G::OFF_SLOT);
 
     const int tiles_m = (M + BM - 1) / BM;
@@ -74,15 +77,17 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_full(0), 1);
+        mbar_init(tmem_full(1), 1);
+        mbar_init(tmem_empty(0), 128);             // every epilogue thread
+        mbar_init(tmem_empty(1), 128);
         mbar_init(drain_bar, 1);
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(slot)), G::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -128,11 +133,12 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
         }
     } else if (warp == 1) {
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         const uint32_t idesc = f16_idesc(BN);
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
+            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -152,7 +158,7 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j) {
                         // A: 16 halves = 32 bytes along the swizzle row; B: 16 k-rows = 2 KB
-                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 128 * j, idesc,
+                        mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 128 * j, idesc,
                                 (kt > 0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
@@ -164,9 +170,9 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full);
+            if (lane == 0) tc_commit(tmem_full(ab));
             __syncwarp();
-            acc_phase ^= 1;
+            ++acc_it;
         }
         if (!ok && lane == 0) atomicOr(err, ERR_MMA);
         if (lane == 0) tc_commit(drain_bar);
@@ -174,25 +180,26 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
     } else {
         const uint32_t q = warp & 3;
-        uint32_t acc_phase = 0;
+        uint32_t acc_it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;
+            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty, sb + G::OFF_EPI + (warp - 2) * 2048);
-            acc_phase ^= 1;
+            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048);
+            ++acc_it;
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem_base, G::TMEM_COLS);
 }
 
 template <int BN>

@@ -42,8 +42,8 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
     if (vec && col0 + 32 <= N) {
         uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2],
-                                                        p[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+            st_global_stream(dst + i, make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]));
     } else {
         uint16_t *dst = reinterpret_cast<uint16_t *>(crow + col0);
 #pragma unroll
@@ -107,7 +107,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
             if (grow < M) {
                 __half *dst = C + static_cast<int64_t>(grow) * ldc + gcol;
                 if (gcol + 8 <= N) {
-                    *reinterpret_cast<uint4 *>(dst) = w;
+                    st_global_stream(dst, w);
                 } else {
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll

@@ -32,7 +32,7 @@ constexpr int STAGES = 4;
 constexpr int RAW = 3;            // k-tiles of int4 prefetched ahead by each converter thread
 constexpr int CONV_THREADS = 256;
 constexpr int THREADS = 192 + CONV_THREADS;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr int UNITS = 2;          // (row, 32-block) units per converter thread per k-tile
 
 constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -44,7 +44,7 @@ constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_RAW = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_BAR = OFF_RAW + RAW * RAW_SLOT_BYTES;
-constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 3) * 8;
+constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 5) * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -156,9 +156,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
 
     auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
-    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
-    const uint32_t tmem_empty = tmem_full + 8;
-    const uint32_t drain_bar = tmem_full + 16;
+    // accumulator double buffer: tmem_full[2], tmem_empty[2], then the drain barrier
+    const uint32_t acc_bar0 = sb + OFF_BAR + 8u * (2 * STAGES);
+    auto tmem_full = [&](uint32_t b) { return acc_bar0 + 8u * b; };
+    auto tmem_empty = [&](uint32_t b) { return acc_bar0 + 16u + 8u * b; };
+    const uint32_t drain_bar = acc_bar0 + 32;
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
 
     const int tiles_m = (M + BM - 1) / BM;
@@ -171,8 +173,10 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             mbar_init(full_bar(s), 1 + CONV_THREADS);  // TMA arrival + every converter thread
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_full(0), 1);
+        mbar_init(tmem_full(1), 1);
+        mbar_init(tmem_empty(0), 128);             // every epilogue thread
+        mbar_init(tmem_empty(1), 128);
         mbar_init(drain_bar, 1);
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -221,10 +225,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
+            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -240,7 +245,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                     const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j)
-                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 2 * j, IDESC,
+                        mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 2 * j, IDESC,
                                 (kt > 0 || j > 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));
                 }
@@ -251,9 +256,9 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full);
+            if (lane == 0) tc_commit(tmem_full(ab));
             __syncwarp();
-            acc_phase ^= 1;
+            ++acc_it;
         }
         if (!ok && lane == 0) atomicOr(err, ERR_MMA);
         if (lane == 0) tc_commit(drain_bar);
@@ -262,18 +267,19 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
     } else if (warp < 6) {
         // ------------------------------------------------------------------- epilogue
         const uint32_t q = warp & 3;
-        uint32_t acc_phase = 0;
+        uint32_t acc_it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;
+            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty, 0u);
-            acc_phase ^= 1;
+            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty(ab), 0u);
+            ++acc_it;
         }
     } else {
         // ----------------------------------------------------------------- converters
@@ -393,8 +399,8 @@ constexpr uint32_t T_STG = BN * 16;                    // 4 KB scale group
 constexpr uint32_t T_OFF_STG = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t T_OFF_EPI = T_OFF_STG + 2 * T_STG;   // 4 epilogue warps x 2 KB
 constexpr uint32_t T_OFF_BAR = T_OFF_EPI + 4 * 2048;
-// raw_full[S], conv_full[S], empty[S], tmem_full, tmem_empty, drain, then the TMEM slot
-constexpr uint32_t T_OFF_SLOT = T_OFF_BAR + (3 * STAGES + 3) * 8;
+// raw_full[S], conv_full[S], empty[S], tmem_full[2], tmem_empty[2], drain, then the TMEM slot
+constexpr uint32_t T_OFF_SLOT = T_OFF_BAR + (3 * STAGES + 5) * 8;
 constexpr uint32_t T_SMEM_BYTES = T_OFF_SLOT + 16 + 1024;
 static_assert(T_SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -411,9 +417,11 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     auto raw_full = [&](int s) { return sb + T_OFF_BAR + 8u * s; };
     auto conv_full = [&](int s) { return sb + T_OFF_BAR + 8u * (STAGES + s); };
     auto empty_bar = [&](int s) { return sb + T_OFF_BAR + 8u * (2 * STAGES + s); };
-    const uint32_t tmem_full = sb + T_OFF_BAR + 8u * (3 * STAGES);
-    const uint32_t tmem_empty = tmem_full + 8;
-    const uint32_t drain_bar = tmem_full + 16;
+    // accumulator double buffer: tmem_full[2], tmem_empty[2], then the drain barrier
+    const uint32_t acc_bar0 = sb + T_OFF_BAR + 8u * (3 * STAGES);
+    auto tmem_full = [&](uint32_t b) { return acc_bar0 + 8u * b; };
+    auto tmem_empty = [&](uint32_t b) { return acc_bar0 + 16u + 8u * b; };
+    const uint32_t drain_bar = acc_bar0 + 32;
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + T_OFF_SLOT);
 
     const int tiles_m = (M + BM - 1) / BM;
@@ -428,8 +436,10 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(conv_full(s), T_CONV);    // every converter thread
             mbar_init(empty_bar(s), 1);         // tcgen05.commit
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_full(0), 1);
+        mbar_init(tmem_full(1), 1);
+        mbar_init(tmem_empty(0), 128);             // every epilogue thread
+        mbar_init(tmem_empty(1), 128);
         mbar_init(drain_bar, 1);
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -489,10 +499,11 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
+            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -509,7 +520,7 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j)
-                        mma_f16(tmem_base, adesc + 2 * j, bdesc + 2 * j, IDESC,
+                        mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 2 * j, IDESC,
                                 (kt > 0 || j > 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));
                 }
@@ -520,9 +531,9 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full);
+            if (lane == 0) tc_commit(tmem_full(ab));
             __syncwarp();
-            acc_phase ^= 1;
+            ++acc_it;
         }
         if (!ok && lane == 0) atomicOr(err, ERR_MMA);
         if (lane == 0) tc_commit(drain_bar);
@@ -531,18 +542,19 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp < 6) {
         // ------------------------------------------------------------------- epilogue
         const uint32_t q = warp & 3;
-        uint32_t acc_phase = 0;
+        uint32_t acc_it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+            const uint32_t ab = acc_it & 1;
+            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty, sb + T_OFF_EPI + (warp - 2) * 2048);
-            acc_phase ^= 1;
+            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
+                              tmem_empty(ab), sb + T_OFF_EPI + (warp - 2) * 2048);
+            ++acc_it;
         }
     } else {
         // ----------------------------------------------------------------- converters

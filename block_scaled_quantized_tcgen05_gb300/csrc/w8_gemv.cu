@@ -78,6 +78,71 @@ __device__ __forceinline__ uint32_t scale_word(const uint8_t *row, int c, int nb
     return w;
 }
 
+// True if some byte of w is 0x00 or 0xFF (the scale codes the shift decode does not cover).
+__device__ __forceinline__ bool has_special_byte(uint32_t w) {
+    const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;     // a zero byte
+    const uint32_t n = ~w;
+    const uint32_t f = (n - 0x01010101u) & ~n & 0x80808080u;     // a 0xFF byte
+    return (z | f) != 0u;
+}
+
+// 2^(byte b of w - 127) as fp32 for bytes 1..254: the byte moved into the exponent field.
+template <int B>
+__device__ __forceinline__ float scale_fast(uint32_t w) {
+    const uint32_t bits = (B < 3 ? (w << (23 - 8 * B)) : (w >> 1)) & 0x7F800000u;
+    return __uint_as_float(bits);
+}
+
+// One 64-row x 128-k stage: four 32-blocks, each two MMAs per activation half, the block's fp32
+// partial sum scaled by its power of two.
+template <int NH, bool EXACT>
+__device__ __forceinline__ void consume_stage(float (&acc)[NH][4], const uint8_t *st,
+                                              const uint8_t *xs, int r0, uint32_t sw, int g, int t,
+                                              uint32_t e0w, uint32_t e1w) {
+    using G = GCfg<NH>;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        // weights: bytes 32 b + 8 t .. +8 of rows r0, r0 + 8 (16-byte chunk 2b + t/2)
+        const uint32_t wc = ((static_cast<uint32_t>(2 * b + (t >> 1)) ^ sw) << 4) +
+                            static_cast<uint32_t>((t & 1) * 8);
+        const uint2 wa = *reinterpret_cast<const uint2 *>(st + r0 * 128 + wc);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(st + (r0 + 8) * 128 + wc);
+        // activations: halves 32 b + 8 t .. +8 of X rows g (and g + 8)
+        const uint8_t *xhalf = xs + static_cast<uint32_t>(b >> 1) * G::X_HALF;
+        const uint32_t xc = static_cast<uint32_t>(4 * (b & 1) + t);
+        const uint32_t xo = (xc ^ static_cast<uint32_t>(g & 7)) << 4;
+        const uint4 xa = *reinterpret_cast<const uint4 *>(xhalf + g * 128 + xo);
+        uint32_t a0[4], a1[4];
+        i8x4_to_f16x2(wa.x, a0[0], a0[2]);
+        i8x4_to_f16x2(wb.x, a0[1], a0[3]);
+        i8x4_to_f16x2(wa.y, a1[0], a1[2]);
+        i8x4_to_f16x2(wb.y, a1[1], a1[3]);
+        float sa, sbv;
+        if constexpr (EXACT) {
+            sa = ue8m0_to_f32((e0w >> (8 * b)) & 0xFF);
+            sbv = ue8m0_to_f32((e1w >> (8 * b)) & 0xFF);
+        } else {
+            sa = b == 0 ? scale_fast<0>(e0w) : b == 1 ? scale_fast<1>(e0w)
+                                             : b == 2 ? scale_fast<2>(e0w) : scale_fast<3>(e0w);
+            sbv = b == 0 ? scale_fast<0>(e1w) : b == 1 ? scale_fast<1>(e1w)
+                                              : b == 2 ? scale_fast<2>(e1w) : scale_fast<3>(e1w);
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            uint4 xv = xa;
+            if (h == 1) xv = *reinterpret_cast<const uint4 *>(xhalf + (g + 8) * 128 + xo);
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            float p[4], q[4];
+            mma_16816(p, a0, xv.x, xv.y, z);
+            mma_16816(q, a1, xv.z, xv.w, p);
+            acc[h][0] = fmaf(sa, q[0], acc[h][0]);
+            acc[h][1] = fmaf(sa, q[1], acc[h][1]);
+            acc[h][2] = fmaf(sbv, q[2], acc[h][2]);
+            acc[h][3] = fmaf(sbv, q[3], acc[h][3]);
+        }
+    }
+}
+
 // NH = number of 8-column activation halves (1 for M <= 8, 2 for M <= 16).
 template <int NH>
 __global__ void __launch_bounds__(THREADS)
@@ -184,39 +249,14 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             }
             const uint8_t *st = smem + stage * G::STAGE;   // plain shared loads, schedulable
             const uint8_t *xs = st + G::W_BYTES;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                // weights: bytes 32 b + 8 t .. +8 of rows r0, r0 + 8 (16-byte chunk 2b + t/2)
-                const uint32_t wc = ((static_cast<uint32_t>(2 * b + (t >> 1)) ^ sw) << 4) +
-                                    static_cast<uint32_t>((t & 1) * 8);
-                const uint2 wa = *reinterpret_cast<const uint2 *>(st + r0 * 128 + wc);
-                const uint2 wb = *reinterpret_cast<const uint2 *>(st + (r0 + 8) * 128 + wc);
-                // activations: halves 32 b + 8 t .. +8 of X rows g (and g + 8)
-                const uint8_t *xhalf = xs + static_cast<uint32_t>(b >> 1) * G::X_HALF;
-                const uint32_t xc = static_cast<uint32_t>(4 * (b & 1) + t);
-                const uint32_t xo = (xc ^ static_cast<uint32_t>(g & 7)) << 4;
-                const uint4 xa = *reinterpret_cast<const uint4 *>(xhalf + g * 128 + xo);
-                uint32_t a0[4], a1[4];
-                i8x4_to_f16x2(wa.x, a0[0], a0[2]);
-                i8x4_to_f16x2(wb.x, a0[1], a0[3]);
-                i8x4_to_f16x2(wa.y, a1[0], a1[2]);
-                i8x4_to_f16x2(wb.y, a1[1], a1[3]);
-                const float sa = ue8m0_to_f32((e0w >> (8 * b)) & 0xFF);
-                const float sbv = ue8m0_to_f32((e1w >> (8 * b)) & 0xFF);
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    uint4 xv = xa;
-                    if (h == 1) xv = *reinterpret_cast<const uint4 *>(xhalf + (g + 8) * 128 + xo);
-                    const float z[4] = {0.f, 0.f, 0.f, 0.f};
-                    float p[4], q[4];
-                    mma_16816(p, a0, xv.x, xv.y, z);
-                    mma_16816(q, a1, xv.z, xv.w, p);
-                    acc[h][0] = fmaf(sa, q[0], acc[h][0]);
-                    acc[h][1] = fmaf(sa, q[1], acc[h][1]);
-                    acc[h][2] = fmaf(sbv, q[2], acc[h][2]);
-                    acc[h][3] = fmaf(sbv, q[3], acc[h][3]);
-                }
-            }
+            // Scale words of this stage: the fast decode builds 2^(e-127) by shifting the byte into
+            // the fp32 exponent field; codes 0x00 (subnormal 2^-127) and 0xFF (NaN) take the exact
+            // decode, chosen for the whole warp so the branch stays uniform.
+            const bool exact = __any_sync(0xffffffffu, has_special_byte(e0w) || has_special_byte(e1w));
+            if (exact)
+                consume_stage<NH, true>(acc, st, xs, r0, sw, g, t, e0w, e1w);
+            else
+                consume_stage<NH, false>(acc, st, xs, r0, sw, g, t, e0w, e1w);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(stage));
             if (++stage == STAGES) {

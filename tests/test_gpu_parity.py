@@ -28,9 +28,10 @@ def dev():
 
 
 def _check(got: torch.Tensor, res, orc, rows=None, what=""):
+    code = q.qgemm_poll_device_error()
+    assert code == 0, f"{what}: a device wait timed out (error word {code:#x})"
     ok, worst, info = orc.within_tolerance(got.float().cpu().numpy(), res, REL, rows)
     assert ok, f"{what}: {info}"
-    assert q.qgemm_poll_device_error() == 0, f"{what}: device wait timed out"
     return worst
 
 
@@ -252,11 +253,15 @@ def test_w8_gemv_extreme_scales(dev, orc):
     M, N, K = 4, 64, 256
     d = synth.w8_inputs(M, N, K, seed=99)
     sw = torch.randint(60, 200, d["sw"].shape, generator=synth.generator(5), dtype=torch.uint8)
+    sw[3, 2] = 255          # NaN scale: row 3 of W poisons column 3 of Y
+    sw[5, 0] = 0            # subnormal 2^-127 scale
+    sw[9, 7] = 254
     W = q.qgemm_create_tensor(q.INT8, d["w"].to(dev), sw.to(dev))
     Y = torch.empty(M, N, dtype=torch.float16, device=dev)
     q.qgemm_w8_gemv(d["x"].to(dev), W, Y)
     res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy(), sw.numpy())
     _check(Y, res, orc, what="w8 gemv extreme scales")
+    assert torch.isnan(Y[:, 3].cpu()).all() and not torch.isnan(Y[:, 4].cpu()).any()
 
 
 @pytest.mark.parametrize("M", [1, 8, 16])
