@@ -9,6 +9,7 @@
 //   warp 1     TMEM owner + MMA issuer: four 128 x BN x 16 MMAs per k-tile; B is described
 //              as MN-major (64-element swizzle atoms BN/64 apart, 8-row k groups 1 KB apart).
 //   warps 2-5  epilogue: TMEM -> fp16 -> global, masked at the M / N edges.
+// Shapes with more than one 128-row and one 128-column block use the CTA-pair kernel below.
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -225,13 +226,222 @@ cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2): a cluster of two CTAs computes a 256 x 256 tile; each
+// CTA stages its own 128 rows of A and 128 columns of B (six stages fit) and holds its 128
+// accumulator rows in TMEM (two accumulators).  The leader (rank 0) arms each stage's full
+// barrier with both CTAs' bytes and issues the MMAs; its commits are multicast to both CTAs'
+// barriers; one lane per epilogue warp of both CTAs releases an accumulator on the leader.
+constexpr int P_BM = 128;       // rows per CTA (the pair covers 256)
+constexpr int P_BN = 256;       // columns per pair tile (128 stored per CTA)
+constexpr int P_BK = 64;
+constexpr int P_STAGES = 6;
+constexpr int P_THREADS = 192;
+constexpr uint32_t P_TMEM_COLS = 512;      // two 256-column accumulators
+constexpr uint32_t P_A_BYTES = P_BM * P_BK * 2;          // 16 KB
+constexpr uint32_t P_B_ATOM = P_BK * 64 * 2;           // 8 KB
+constexpr uint32_t P_B_BYTES = 2 * P_B_ATOM;           // this CTA's 128 columns
+constexpr uint32_t P_OFF_A = 0;
+constexpr uint32_t P_OFF_B = P_OFF_A + P_STAGES * P_A_BYTES;
+constexpr uint32_t P_OFF_EPI = P_OFF_B + P_STAGES * P_B_BYTES;
+constexpr uint32_t P_OFF_BAR = P_OFF_EPI + 4 * 2048;
+// full[S] (leader), empty[S], tmem_full[2], tmem_empty[2] (leader), drain
+constexpr uint32_t P_OFF_SLOT = P_OFF_BAR + (2 * P_STAGES + 5) * 8;
+constexpr uint32_t P_SMEM_BYTES = P_OFF_SLOT + 16 + 1024;
+static_assert(P_SMEM_BYTES <= 232448, "smem");
+
+// kind::f16, D fp32, A K-major, B MN-major, N = 256, M = 256 (pair)
+constexpr uint32_t P_IDESC = (1u << 4) | (1u << 16) | (static_cast<uint32_t>(P_BN >> 3) << 17) |
+                           (static_cast<uint32_t>(256 >> 4) << 24);
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
+                     unsigned *err, uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();          // 0 = leader (issues the MMAs)
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return sb + P_OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + P_OFF_BAR + 8u * (P_STAGES + s); };
+    const uint32_t acc_bar0 = sb + P_OFF_BAR + 8u * (2 * P_STAGES);
+    auto tmem_full = [&](uint32_t b) { return acc_bar0 + 8u * b; };
+    auto tmem_empty = [&](uint32_t b) { return acc_bar0 + 16u + 8u * b; };
+    const uint32_t drain_bar = acc_bar0 + 32;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + P_OFF_SLOT);
+
+    const int tiles_m = (M + 2 * P_BM - 1) / (2 * P_BM);
+    const int tiles_n = (N + P_BN - 1) / P_BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = (K + P_BK - 1) / P_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);     // the leader's expect_tx for both CTAs' bytes
+            mbar_init(empty_bar(s), 1);    // the leader's multicast commit
+        }
+        mbar_init(tmem_full(0), 1);
+        mbar_init(tmem_full(1), 1);
+        mbar_init(tmem_empty(0), 8);       // one lane of each epilogue warp of both CTAs
+        mbar_init(tmem_empty(1), 8);
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(slot)), P_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                        // peer barriers initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, mb, nb);
+                const int m0 = mb * 2 * P_BM + static_cast<int>(rank) * P_BM;
+                const int nh = nb * P_BN + static_cast<int>(rank) * (P_BN / 2);
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (P_A_BYTES + P_B_BYTES));
+                    const uint32_t sA = sb + P_OFF_A + stage * P_A_BYTES;
+                    const uint32_t sB = sb + P_OFF_B + stage * P_B_BYTES;
+                    tma_load_2d_pair(sA, &tmA, lead_full, kt * P_BK, m0);
+                    tma_load_2d_pair(sB, &tmB, lead_full, nh, kt * P_BK);
+                    tma_load_2d_pair(sB + P_B_ATOM, &tmB, lead_full, nh + 64, kt * P_BK);
+                    ++issued;
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) atomicOr(err, ERR_PRODUCER);
+            if (rank == 0)   // the leader's full barriers count both CTAs' bytes
+                for (int i = max(0, issued - P_STAGES); i < issued; ++i)
+                    if (!mbar_wait_cluster(full_bar(i % P_STAGES), (i / P_STAGES) & 1, timeout_ns)) {
+                        atomicOr(err, ERR_DRAIN);
+                        break;
+                    }
+        }
+    } else if (warp == 1) {
+        if (rank == 0) {
+            uint32_t stage = 0, phase = 0, acc_it = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                const uint32_t ab = acc_it & 1;
+                if (!mbar_wait_cluster(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait_cluster(full_bar(stage), phase, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t adesc = smem_desc(sb + P_OFF_A + stage * P_A_BYTES, 16, 1024, SWZ_128B);
+                        const uint64_t bdesc = smem_desc(sb + P_OFF_B + stage * P_B_BYTES, P_B_ATOM, 1024, SWZ_128B);
+#pragma unroll
+                        for (uint32_t j = 0; j < P_BK / 16; ++j)
+                            mma_f16_pair(tmem_base + ab * P_BN, adesc + 2 * j, bdesc + 128 * j, P_IDESC,
+                                         (kt > 0 || j > 0) ? 1u : 0u);
+                        tc_commit_pair(empty_bar(stage), 3);
+                    }
+                    __syncwarp();
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) tc_commit_pair(tmem_full(ab), 3);
+                __syncwarp();
+                ++acc_it;
+            }
+            if (!ok && lane == 0) atomicOr(err, ERR_MMA);
+            if (lane == 0) tc_commit_pair(drain_bar, 3);
+            __syncwarp();
+        }
+        // both CTAs: every pair MMA writing this CTA's TMEM has completed
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else {
+        const uint32_t q = warp & 3;
+        uint32_t acc_it = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            const uint32_t ab = acc_it & 1;
+            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            epilogue_tile<P_BN, 2>(tmem_base + ab * P_BN, q, lane, C, ldc,
+                                 mb * 2 * P_BM + static_cast<int>(rank) * P_BM, nb * P_BN, M, N,
+                                 c_vec != 0, map_to_cta(tmem_empty(ab), 0),
+                                 sb + P_OFF_EPI + (warp - 2) * 2048);
+            ++acc_it;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                        // no remote arrival or multicast targets an exited CTA
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, P_TMEM_COLS);
+}
+
 }  // namespace
 
 namespace qgi {
 
+static cudaError_t launch_gemm_f16_pair(const __half *A, int64_t lda, const __half *B,
+                                        int64_t ldb, __half *C, int64_t ldc, int M, int N, int K,
+                                        const LaunchCtx &ctx, bool *encode_ok) {
+    CUtensorMap tmA, tmB;
+    *encode_ok = encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, P_BK, P_BM,
+                               CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, ldb * 2, 64, P_BK,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + 2 * P_BM - 1) / (2 * P_BM)) * ((N + P_BN - 1) / P_BN);
+    int pairs = ctx.num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    gemm_f16_pair_kernel<<<2 * pairs, P_THREADS, P_SMEM_BYTES, ctx.stream>>>(
+        tmA, tmB, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64_t ldb,
                             __half *C, int64_t ldc, int M, int N, int K, const LaunchCtx &ctx,
                             bool *encode_ok) {
+    // CTA pairs once there are at least two 128-row blocks and more than one 128-column block.
+    if (M > 128 && N > 128)
+        return launch_gemm_f16_pair(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
     if (N > 128) return launch_bn<256>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
     return launch_bn<128>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
 }

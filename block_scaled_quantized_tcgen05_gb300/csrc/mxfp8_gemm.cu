@@ -458,7 +458,17 @@ namespace qgi {
 
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                          const LaunchCtx &ctx, bool *encode_ok) {
-    // BN = 256 with one accumulator measured faster than BN = 224 with two at 8192^3.
+    // CTA pairs (mxfp8_pair.cu, scales repacked into pooled scratch) when both operands span
+    // more than one 128-row block; otherwise one CTA per tile.  BN = 256 with one accumulator
+    // measured faster than BN = 224 with two at 8192^3.
+    if (mxfp8_pair_eligible(A, B)) {
+        void *scratch = nullptr;
+        cudaError_t e = scratch_alloc(mxfp8_pair_scratch_bytes(A, B), ctx, &scratch);
+        if (e != cudaSuccess) return e;
+        e = launch_mxfp8_pair(A, B, C, ldc, scratch, ctx, encode_ok);
+        const cudaError_t f = scratch_free(scratch, ctx);
+        return e != cudaSuccess ? e : f;
+    }
     if (B->rows > 128) return launch_sfm<256>(A, B, C, ldc, ctx, encode_ok);
     return launch_sfm<128>(A, B, C, ldc, ctx, encode_ok);
 }

@@ -1,0 +1,374 @@
+// mxfp8_pair.cu -- block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// Same product as mxfp8_gemm.cu (E4M3 data, UE8M0 scale per 32 along K, fp32 accumulation,
+// fp16 output), with one MMA spanning two SMs: a cluster of two CTAs computes a 256 x 256 output
+// tile; each CTA keeps its own 128 rows of A and its own 128 columns of B in shared memory and
+// holds its 128 rows of the accumulator in its TMEM.  Halving the B bytes each SM stages lets six
+// stages fit.
+//
+// Scale factors take two steps.
+//  1. sf_pack_kernel rewrites both scale planes into a scratch buffer in the order tcgen05.cp
+//     reads them: for each k-tile of 128 and each block of 128 rows, 512 contiguous bytes, 32
+//     lines of 16 bytes, line i holding the four scale bytes of rows i, i + 32, i + 64 and i + 96
+//     (one 32-bit word per row, byte j = k-block j of the k-tile).  Rows and k-blocks past the
+//     operand are written as 0 (scale 2^-127 on zero data).  The row blocks are padded to an even
+//     count, so a pair tile never reads past the buffer.
+//  2. Each CTA fetches a stage's scales by TMA (its own 128 rows of A scales, all 256 rows of B
+//     scales) onto a barrier of its own, and four scale warps -- one per TMEM lane quarter -- move
+//     them from shared memory into this CTA's TMEM with tcgen05.st, in the replicated layout the
+//     block-scaled MMA reads (lane 32 q + i, column c: row 32 c + i).  A tcgen05.cp in the MMA
+//     stream would sit in the tensor pipe's in-order queue in front of the MMAs; written from
+//     registers, the scales never enter that queue.
+//
+// Hand-off: only the leader (rank 0) issues MMAs, from one thread whose loop is the kernel's
+// critical path (a pair MMA takes about as long to issue as the tensor cores take to run it), so
+// that loop does one CTA-scope barrier wait per stage and nothing else but the four MMAs and a
+// commit.  Each stage's full barrier lives in the leader and collects everything the stage needs:
+// the leader's arrival with both CTAs' data bytes, both CTAs' data loads, and one arrival from
+// each scale warp of both CTAs once its tcgen05.st have completed (tcgen05.wait::st; the arrival
+// itself is relaxed -- a release at cluster scope costs about a microsecond per stage).  Commits
+// are multicast to the empty, accumulator-full and drain barriers of both CTAs; each epilogue
+// warp of both CTAs releases the accumulator with one arrival on the leader's barrier.  Every
+// wait is bounded.
+#include "qgemm_common.cuh"
+#include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
+
+namespace {
+
+using namespace qg;
+
+constexpr int BM = 128;                     // rows per CTA (256 per pair)
+constexpr int BN = 256;                     // columns per pair tile (128 of B per CTA)
+constexpr int BK = 128;                     // E4M3 bytes of K per stage
+constexpr int STAGES = 6;
+constexpr int THREADS = 320;                // producer, MMA, 4 epilogue, 4 scale warps
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_COL0 = 256;           // scale slots after the 256-column accumulator
+constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA 4 + SFB 8 (+4 spare)
+
+constexpr uint32_t A_BYTES = BM * BK;                 // 16 KB
+constexpr uint32_t B_BYTES = (BN / 2) * BK;           // 16 KB (this CTA's half)
+constexpr uint32_t SFA_BYTES = 512;                   // 128 rows x 4 bytes
+constexpr uint32_t SFB_BYTES = 1024;                  // 256 rows x 4 bytes
+constexpr uint32_t STAGE_TX = 2 * (A_BYTES + B_BYTES);   // both CTAs' data, on the leader
+constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;          // this CTA's scales, locally
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr uint32_t OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+constexpr uint32_t OFF_BAR = OFF_EPI + 4 * 2048;
+// full[S] (leader), empty[S], sf_full[S], tmem_full, tmem_empty (leader), drain, then the slot
+constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
+constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+
+// kind::mxf8f6f4 block-scaled descriptor: E4M3 x E4M3, K-major, N = 256, UE8M0 scales, M = 256.
+constexpr uint32_t IDESC = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+                           (static_cast<uint32_t>(256 >> 7) << 27);
+
+// ------------------------------------------------------------------------ scale repacking
+constexpr int PACK_KT = 8;                  // k-tiles per packing block
+constexpr int PACK_ROW = PACK_KT * 4 + 4;   // bytes per staged row (+4 keeps banks apart)
+
+struct SfPackOperand {
+    const uint8_t *scales;   // [rows, kcols] UE8M0, row stride lds bytes, any alignment
+    int64_t lds;
+    int rows;
+    int kcols;               // K / 32
+    int rbp;                 // padded count of 128-row blocks (even)
+    uint8_t *out;            // [KT][rbp][32 lines][16 bytes]
+};
+
+// grid (max rbp, ceil(KT / 8), 2 operands) x 256 threads.  Stage 128 rows x 32 scale bytes with
+// row-contiguous (coalesced) byte loads, then write 8 k-tiles x 32 lines of 16 bytes.
+__global__ void __launch_bounds__(256)
+sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
+    __shared__ __align__(16) uint8_t tile[128 * PACK_ROW];
+    const SfPackOperand &op = blockIdx.z == 0 ? opA : opB;
+    const int rb = blockIdx.x;
+    if (rb >= op.rbp) return;
+    const int kt0 = blockIdx.y * PACK_KT;
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int idx = t + 256 * j;              // 128 rows x 32 bytes
+        const int row = idx >> 5, col = idx & 31;
+        const int r = rb * 128 + row, c = kt0 * 4 + col;
+        uint8_t v = 0;
+        if (r < op.rows && c < op.kcols) v = op.scales[static_cast<int64_t>(r) * op.lds + c];
+        tile[row * PACK_ROW + col] = v;
+    }
+    __syncthreads();
+    const int ktl = t >> 5, i = t & 31;
+    const int kt = kt0 + ktl;
+    if (kt >= KT) return;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(tile);
+    constexpr int WPR = PACK_ROW / 4;             // words per staged row
+    uint4 v;
+    v.x = w[i * WPR + ktl];
+    v.y = w[(i + 32) * WPR + ktl];
+    v.z = w[(i + 64) * WPR + ktl];
+    v.w = w[(i + 96) * WPR + ktl];
+    uint8_t *dst = op.out + ((static_cast<int64_t>(kt) * op.rbp + rb) * 32 + i) * 16;
+    *reinterpret_cast<uint4 *>(dst) = v;
+}
+
+// -------------------------------------------------------------------------------- the GEMM
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                  int rbpA, int rbpB, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N,
+                  int K, unsigned *err, uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();      // 0 = leader
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    auto sf_full = [&](int s) { return sb + OFF_BAR + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (3 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
+
+    const int tiles_m = (M + 2 * BM - 1) / (2 * BM);
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int KT = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 9);   // leader's expect_tx + one lane of each scale warp (x8)
+            mbar_init(empty_bar(s), 1);  // leader's multicast commit
+            mbar_init(sf_full(s), 1);    // this CTA's scale TMA
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 8);        // one lane of each epilogue warp of both CTAs
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                   // barriers of both CTAs initialised before remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            bool ok = true;
+            const uint64_t keep = l2_policy_evict_last();   // B panels are re-read by many tiles
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, mb, nb);
+                const int m0 = mb * 2 * BM + static_cast<int>(rank) * BM;
+                const int nh = nb * BN + static_cast<int>(rank) * (BN / 2);
+                const int la = (2 * mb + static_cast<int>(rank)) * 32;   // packed A line
+                const int lb = 2 * nb * 32;                               // packed B line
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+                    tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
+                    tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, &tmB, lead_full, kt * BK,
+                                          nh, keep);
+                    mbar_arrive_expect_tx(sf_full(stage), SF_TX);
+                    tma_load_2d(sb + OFF_SFA + stage * SFA_BYTES, &tmSA, sf_full(stage), 0,
+                                kt * rbpA * 32 + la);
+                    tma_load_2d(sb + OFF_SFB + stage * SFB_BYTES, &tmSB, sf_full(stage), 0,
+                                kt * rbpB * 32 + lb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) atomicOr(err, ERR_PRODUCER);
+            if (rank == 0)   // the leader's full barriers count both CTAs' loads
+                for (int i = max(0, issued - STAGES); i < issued; ++i)
+                    if (!mbar_wait_cluster(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
+                        atomicOr(err, ERR_DRAIN);
+                        break;
+                    }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (rank == 0 && lane == 0) {
+            // --------------------------------------------------------- MMA issuer
+            // descriptors of stage 0; stage s adds s * bytes / 16 to the start-address field
+            const uint64_t adesc0 = smem_desc(sb + OFF_A, 16, 1024, SWZ_128B);
+            const uint64_t bdesc0 = smem_desc(sb + OFF_B, 16, 1024, SWZ_128B);
+            uint32_t acc_phase = 0, stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
+                    const uint64_t adesc = adesc0 + stage * (A_BYTES >> 4);
+                    const uint64_t bdesc = bdesc0 + stage * (B_BYTES >> 4);
+                    mma_mxf8_pair(tmem_base, adesc, bdesc, IDESC, sf_col, sf_col + 4,
+                                  kt > 0 ? 1u : 0u);
+#pragma unroll
+                    for (uint32_t j = 1; j < BK / 32; ++j)
+                        mma_mxf8_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j,
+                                      IDESC | (j << 4) | (j << 29), sf_col, sf_col + 4, 1u);
+                    tc_commit_pair(empty_bar(stage), 3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(tmem_full, 3);
+                acc_phase ^= 1;
+            }
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit_pair(drain_bar, 3);
+        }
+        __syncwarp();
+        // both CTAs: every pair MMA writing this CTA's TMEM has completed before it is freed
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------- scale warps
+        // Lane i of the warp for lane quarter q writes TMEM lane 32 q + i of the stage's slot:
+        // columns 0..3 the A scales of rows i + 32 c, columns 4..11 the B scales of rows i + 32 c.
+        const uint32_t q = warp & 3;
+        const uint32_t lead_full = map_to_cta(full_bar(0), 0);
+        const int my_tiles = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
+        const int total = my_tiles * KT;
+        for (int it = 0; it < total; ++it) {
+            const uint32_t s = static_cast<uint32_t>(it % STAGES);
+            // the TMA of this stage was issued after the MMAs that last read this slot finished
+            if (!mbar_wait(sf_full(s), static_cast<uint32_t>(it / STAGES) & 1, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_PRODUCER);
+                break;
+            }
+            const uint8_t *sfa = smem + OFF_SFA + s * SFA_BYTES + lane * 16;
+            const uint8_t *sfb = smem + OFF_SFB + s * SFB_BYTES + lane * 16;
+            const uint4 va = *reinterpret_cast<const uint4 *>(sfa);
+            const uint4 vb0 = *reinterpret_cast<const uint4 *>(sfb);
+            const uint4 vb1 = *reinterpret_cast<const uint4 *>(sfb + 512);
+            const uint32_t col = tmem_base + ((q * 32) << 16) + SF_COL0 + s * SF_COLS_PER_STAGE;
+            tmem_st_32x32b_x4(col, va);
+            tmem_st_32x32b_x8(col + 4, vb0, vb1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * s);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const uint32_t q = warp & 3;
+        const uint32_t lead_empty = map_to_cta(tmem_empty, 0);
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs) {
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, mb, nb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            epilogue_tile<BN, 2>(tmem_base, q, lane, C, ldc,
+                                 mb * 2 * BM + static_cast<int>(rank) * BM, nb * BN, M, N,
+                                 c_vec != 0, lead_empty, sb + OFF_EPI + (warp - 2) * 2048);
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                   // no remote arrival or multicast targets an exited CTA
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+int padded_blocks(int64_t rows) { return static_cast<int>(2 * ((rows + 255) / 256)); }
+
+}  // namespace
+
+namespace qgi {
+
+bool mxfp8_pair_eligible(const qgemm_tensor *A, const qgemm_tensor *B) {
+    return A->rows > BM && B->rows > BN / 2;
+}
+
+size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
+    const int64_t KT = (A->k + BK - 1) / BK;
+    return static_cast<size_t>(KT) * (padded_blocks(A->rows) + padded_blocks(B->rows)) * 512;
+}
+
+cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                              int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok) {
+    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
+              K = static_cast<int>(A->k);
+    const int KT = (K + BK - 1) / BK;
+    const int rbpA = padded_blocks(M), rbpB = padded_blocks(N);
+    uint8_t *packA = static_cast<uint8_t *>(scratch);
+    uint8_t *packB = packA + static_cast<size_t>(KT) * rbpA * 512;
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    *encode_ok =
+        encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, K, M, A->ld, BK, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, K, N, B->ld, BK, BN / 2,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode_tma_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, packA, 16,
+                      static_cast<uint64_t>(KT) * rbpA * 32, 16, 16, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        encode_tma_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, packB, 16,
+                      static_cast<uint64_t>(KT) * rbpB * 32, 16, 16, 64,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+
+    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA};
+    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB};
+    const dim3 pgrid(static_cast<unsigned>(rbpA > rbpB ? rbpA : rbpB),
+                     static_cast<unsigned>((KT + PACK_KT - 1) / PACK_KT), 2);
+    sf_pack_kernel<<<pgrid, 256, 0, ctx.stream>>>(pa, pb, KT);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    e = cudaFuncSetAttribute(mxfp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+    int pairs = ctx.num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    mxfp8_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
+        tmA, tmB, tmSA, tmSB, rbpA, rbpB, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace qgi

@@ -27,6 +27,7 @@ struct DeviceInfo {
     bool ready = false;
     int num_sms = 0;
     unsigned *err = nullptr;
+    cudaMemPool_t pool = nullptr;   // scratch pool, created on first use
 };
 DeviceInfo g_dev[MAX_DEVICES];
 std::mutex g_dev_mutex;
@@ -67,6 +68,42 @@ qgemm_status get_ctx(void *stream, qgi::LaunchCtx *ctx) {
     ctx->device = dev;
     return QGEMM_OK;
 }
+
+}  // namespace
+
+namespace qgi {
+
+cudaError_t scratch_alloc(size_t bytes, const LaunchCtx &ctx, void **p) {
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        DeviceInfo &d = g_dev[ctx.device];
+        if (!d.pool) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = ctx.device;
+            cudaError_t e = cudaMemPoolCreate(&d.pool, &props);
+            if (e != cudaSuccess) {
+                d.pool = nullptr;
+                return e;
+            }
+            uint64_t keep = UINT64_MAX;   // never hand memory back at synchronisation points
+            e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            if (e != cudaSuccess) return e;
+        }
+        pool = d.pool;
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pool, ctx.stream);
+}
+
+cudaError_t scratch_free(void *p, const LaunchCtx &ctx) {
+    return p ? cudaFreeAsync(p, ctx.stream) : cudaSuccess;
+}
+
+}  // namespace qgi
+
+namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -59,7 +59,10 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
 // chunks swizzled by row pair, conflict-free both ways) so that each store instruction writes
 // 8 rows x 64 contiguous bytes, i.e. whole 32-byte sectors.  The accumulator is released
 // (arrival on `tmem_empty`) after its last column has been read.
-template <int BN>
+// RELEASE selects how the accumulator is released: 0 = every lane arrives on this CTA's barrier;
+// 2 = one lane per warp arrives on `tmem_empty` given as a shared::cluster address (a CTA pair
+// releases its accumulators on the MMA-issuing CTA's barrier).
+template <int BN, int RELEASE = 0>
 __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, uint32_t lane,
                                               __half *C, int64_t ldc, int m0, int n0, int M,
                                               int N, bool vec, uint32_t tmem_empty,
@@ -72,7 +75,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
         tmem_wait_ld();
         if (ch == BN / 32 - 1) {
             tc_fence_before();
-            mbar_arrive(tmem_empty);
+            if constexpr (RELEASE == 2) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tmem_empty);
+            } else {
+                mbar_arrive(tmem_empty);
+            }
         }
         const int col0 = n0 + ch * 32;
         if (stage == 0u || !vec) {

@@ -41,6 +41,17 @@ bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, u
 // Kernel launchers (one per translation unit).  Arguments are already validated.
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                          const LaunchCtx &ctx, bool *encode_ok);
+// CTA-pair MXFP8 path: scales are repacked into `scratch` (mxfp8_pair_scratch_bytes bytes,
+// 256-byte aligned device memory that stays untouched by anything else until the GEMM is done).
+bool mxfp8_pair_eligible(const qgemm_tensor *A, const qgemm_tensor *B);
+size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B);
+cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                              int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok);
+
+// Stream-ordered scratch from the library's per-device memory pool (memory is kept in the pool
+// between calls, so steady-state calls do not reach the driver's allocator).
+cudaError_t scratch_alloc(size_t bytes, const LaunchCtx &ctx, void **p);
+cudaError_t scratch_free(void *p, const LaunchCtx &ctx);
 cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64_t ldb,
                             __half *C, int64_t ldc, int M, int N, int K, const LaunchCtx &ctx,
                             bool *encode_ok);

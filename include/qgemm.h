@@ -106,10 +106,17 @@ qgemm_status qgemm_tensor_info(const qgemm_tensor *t, int32_t *dtype, int64_t *r
  * ("TensorOps: quantized matmul ...", "Kernel-phase findings", fact 2).
  *   A   QGEMM_E4M3 view [M, K];  B   QGEMM_E4M3 view [N, K] (same K).
  *   C   device fp16 [M, N] with row stride ldc elements (ldc >= N).
- * Requirements: K % 32 == 0; data pointers and byte strides 16-byte aligned; scale pointers and
- * scale strides 4-byte aligned; C and ldc * 2 16-byte aligned.  Any M, N >= 0 (ragged tiles are
- * masked); M or N == 0 writes nothing; K == 0 writes zeros.
- * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+ * Requirements: K % 32 == 0; data pointers and byte strides 16-byte aligned; scale planes any
+ * alignment; C 2-byte aligned (16-byte aligned C and ldc % 8 == 0 take the vector stores).  Any
+ * M, N >= 0 (ragged tiles are masked); M or N == 0 writes nothing; K == 0 writes zeros.
+ * Scratch: when M > 128 and N > 128 the call runs on CTA pairs and first rewrites both scale
+ * planes into the order the tensor cores read them, in (2 ceil(M/256) + 2 ceil(N/256)) *
+ * ceil(K/128) * 512 bytes of device scratch taken from a library-owned per-device memory pool
+ * with cudaMallocFromPoolAsync on `stream` and handed back with cudaFreeAsync on the same stream
+ * after the GEMM (two kernel launches).  The pool keeps its memory between calls, so steady-state
+ * calls do not reach the driver's allocator; it is released at process exit.
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA
+ * (including a failed scratch allocation). */
 qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                          void *stream);
 

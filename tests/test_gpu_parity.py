@@ -182,6 +182,28 @@ def test_mxfp8_edge_cases(dev, orc):
     assert ei.value.name == "QGEMM_ERR_INVALID_ARG"
 
 
+def test_mxfp8_many_tiles_offset_k(dev, orc):
+    """More output tiles than CTA pairs, a K window starting one scale byte into the planes and a
+    ragged last k-tile; two calls in a row give identical bits."""
+    M, N, K0, K = 2344, 2552, 32, 1056
+    d = synth.mxfp8_inputs(M, N, K0 + K, seed=77, row_variance=True)
+    A, B, _ = _mx_views(d, dev)
+    As = q.qgemm_tensor_slice(A, 0, M, K0, K)
+    Bs = q.qgemm_tensor_slice(B, 0, N, K0, K)
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(As, Bs, C)
+    C2 = torch.empty_like(C)
+    q.qgemm_mxfp8(As, Bs, C2)
+    assert torch.equal(C, C2)
+    rows = np.array([0, 1, 127, 128, 255, 256, 1000, 2047, 2048, 2303, 2304, 2343])
+    a = d["a"][:, K0:].contiguous()
+    sa = d["sa"][:, K0 // 32:].contiguous()
+    b = d["b"][:, K0:].contiguous()
+    sb = d["sb"][:, K0 // 32:].contiguous()
+    res = orc.mxfp8(a.numpy(), sa.numpy(), b.numpy(), sb.numpy(), rows=rows)
+    _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="mxfp8 many tiles, K offset")
+
+
 def test_mxfp8_full_size_sampled(dev, orc):
     """8192^3 with per-row variance 10^U(-2,2): full GPU product, oracle on sampled rows."""
     d = synth.workload("mxfp8_8192")
