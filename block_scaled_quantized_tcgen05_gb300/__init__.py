@@ -62,6 +62,7 @@ def load_library():
                                   ctypes.POINTER(I64), ctypes.POINTER(P), ctypes.POINTER(I64),
                                   ctypes.POINTER(P), ctypes.POINTER(I64)]),
         "qgemm_mxfp8": (S, [P, P, P, I64, P]),
+        "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
         "gemm_f16": (S, [P, I64, P, I64, P, I64, I64, I64, I64, P]),
         "qgemm_w4a16": (S, [P, I64, I64, P, P, I64, P]),
         "qgemm_w8_gemv": (S, [P, I64, I64, P, P, I64, P]),
@@ -175,6 +176,15 @@ def qgemm_destroy_tensor(t: QTensor):
 def qgemm_mxfp8(A: QTensor, B: QTensor, C, stream=None):
     _check(load_library().qgemm_mxfp8(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
            "qgemm_mxfp8")
+    return C
+
+
+def qgemm_mxfp8_noalloc(A: QTensor, B: QTensor, C, stream=None):
+    """qgemm_mxfp8 with its scale scratch in the library's fixed device buffer: allocates no
+    device memory (for callers that cannot allocate mid-run); shapes needing more than 8 MiB of
+    repacked scales are rejected; concurrent calls on one device must not overlap on the GPU."""
+    _check(load_library().qgemm_mxfp8_noalloc(A.handle, B.handle, _ptr(C), _ld(C),
+                                               _stream(stream)), "qgemm_mxfp8_noalloc")
     return C
 
 

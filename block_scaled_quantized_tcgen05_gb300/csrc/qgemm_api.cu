@@ -101,6 +101,8 @@ cudaError_t scratch_free(void *p, const LaunchCtx &ctx) {
     return p ? cudaFreeAsync(p, ctx.stream) : cudaSuccess;
 }
 
+qgemm_status launch_ctx(void *stream, LaunchCtx *ctx) { return get_ctx(stream, ctx); }
+
 }  // namespace qgi
 
 namespace {

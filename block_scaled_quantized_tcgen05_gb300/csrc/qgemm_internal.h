@@ -52,6 +52,10 @@ cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __ha
 // between calls, so steady-state calls do not reach the driver's allocator).
 cudaError_t scratch_alloc(size_t bytes, const LaunchCtx &ctx, void **p);
 cudaError_t scratch_free(void *p, const LaunchCtx &ctx);
+
+// Launch context on the current device (SM count, error word, wait bound), for entry points
+// defined outside qgemm_api.cu.
+qgemm_status launch_ctx(void *stream, LaunchCtx *ctx);
 cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64_t ldb,
                             __half *C, int64_t ldc, int M, int N, int K, const LaunchCtx &ctx,
                             bool *encode_ok);

@@ -120,6 +120,26 @@ qgemm_status qgemm_tensor_info(const qgemm_tensor *t, int32_t *dtype, int64_t *r
 qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                          void *stream);
 
+/* qgemm_mxfp8 without any device allocation.  The paper has no counterpart: this entry point
+ * exists for callers that cannot let a library allocate device memory while they run -- a serving
+ * process that reserves all device memory up front for its own allocator, or a latency-critical
+ * path that cannot risk an allocation that blocks or fails in the middle of a request.
+ * Same arguments, layouts, results and errors as qgemm_mxfp8.  Where qgemm_mxfp8 takes pooled
+ * scratch for the repacked scale planes (M > 128 and N > 128), this call uses a fixed 8 MiB
+ * device array compiled into the library instead (held on every device that loads the library
+ * until exit) and makes no cudaMalloc, pool allocation or other allocating call.
+ * Limits and rules:
+ *   - a shape whose repacked scales need more than 8 MiB ((2 ceil(M/256) + 2 ceil(N/256)) *
+ *     ceil(K/128) * 512 bytes, e.g. more than M = N = 16384 at K = 8192) is rejected with
+ *     QGEMM_ERR_UNSUPPORTED_SHAPE and nothing is launched;
+ *   - all calls on one device share the array: calls that overlap on the GPU race on it and give
+ *     wrong results -- issue them on one stream or synchronise between them;
+ *   - the array keeps the last call's contents; every byte a call reads is first rewritten by it;
+ *   - the first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current) and caches it; make that first call before any stream capture. */
+qgemm_status qgemm_mxfp8_noalloc(const qgemm_tensor *A, const qgemm_tensor *B, void *C,
+                                 int64_t ldc, void *stream);
+
 /* fp16 GEMM: C[M, N] = fp16_rn(A[M, K] @ B[K, N]), fp32 accumulation, all row-major fp16.
  * Passage: "TensorOps: quantized matmul ...", "VALIDATED ON M4 MAX" (kernel M0, half x half ->
  * half) and "TileLang Metal Backend Internals", section 1 (fp16 input, fp32 accumulation, fp16
