@@ -42,7 +42,12 @@ constexpr int BM = 128;                     // rows per CTA (256 per pair)
 constexpr int BN = 256;                     // columns per pair tile (128 of B per CTA)
 constexpr int BK = 128;                     // E4M3 bytes of K per stage
 constexpr int STAGES = 6;
-constexpr int THREADS = 320;                // producer, MMA, 4 epilogue, 4 scale warps
+// Warps: 0 producer, 1 MMA issuer, 2..9 epilogue (two per TMEM lane quarter, one per half of
+// the 256 accumulator columns, so the accumulator is drained -- and released to the next tile's
+// MMAs -- twice as fast as with four), 10..13 scale warps.
+constexpr int EPI_WARPS = 8;
+constexpr int SCALE_WARP0 = 2 + EPI_WARPS;
+constexpr int THREADS = 32 * (SCALE_WARP0 + 4);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;           // scale slots after the 256-column accumulator
 constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA 4 + SFB 8 (+4 spare)
@@ -58,7 +63,7 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr uint32_t OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t OFF_BAR = OFF_EPI + 4 * 2048;
+constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * 2048;
 // full[S] (leader), empty[S], sf_full[S], tmem_full, tmem_empty (leader), drain, then the slot
 constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
@@ -151,7 +156,7 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(sf_full(s), 1);    // this CTA's scale TMA
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 8);        // one lane of each epilogue warp of both CTAs
+        mbar_init(tmem_empty, 2 * EPI_WARPS);   // one lane of each epilogue warp of both CTAs
         mbar_init(drain_bar, 1);
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -259,7 +264,7 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         __syncwarp();
         // both CTAs: every pair MMA writing this CTA's TMEM has completed before it is freed
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
-    } else if (warp >= 6) {
+    } else if (warp >= SCALE_WARP0) {
         // ------------------------------------------------------------- scale warps
         // Lane i of the warp for lane quarter q writes TMEM lane 32 q + i of the stage's slot:
         // columns 0..3 the A scales of rows i + 32 c, columns 4..11 the B scales of rows i + 32 c.
@@ -289,7 +294,8 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const uint32_t q = warp & 3;
+        const uint32_t q = warp & 3;                     // TMEM lane quarter of this warp
+        const uint32_t half = (warp - 2) >> 2;            // accumulator columns [128 h, 128 h + 128)
         const uint32_t lead_empty = map_to_cta(tmem_empty, 0);
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs) {
@@ -300,9 +306,10 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN, 2>(tmem_base, q, lane, C, ldc,
-                                 mb * 2 * BM + static_cast<int>(rank) * BM, nb * BN, M, N,
-                                 c_vec != 0, lead_empty, sb + OFF_EPI + (warp - 2) * 2048);
+            epilogue_tile<BN / 2, 2>(tmem_base + half * (BN / 2), q, lane, C, ldc,
+                                     mb * 2 * BM + static_cast<int>(rank) * BM,
+                                     nb * BN + static_cast<int>(half) * (BN / 2), M, N,
+                                     c_vec != 0, lead_empty, sb + OFF_EPI + (warp - 2) * 2048);
             acc_phase ^= 1;
         }
     }
