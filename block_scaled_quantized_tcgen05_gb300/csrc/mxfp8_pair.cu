@@ -306,7 +306,7 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN / 2, 2>(tmem_base + half * (BN / 2), q, lane, C, ldc,
+            epilogue_tile<BN / 2, 3>(tmem_base + half * (BN / 2), q, lane, C, ldc,
                                      mb * 2 * BM + static_cast<int>(rank) * BM,
                                      nb * BN + static_cast<int>(half) * (BN / 2), M, N,
                                      c_vec != 0, lead_empty, sb + OFF_EPI + (warp - 2) * 2048);

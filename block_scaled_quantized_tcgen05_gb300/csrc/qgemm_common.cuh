@@ -61,7 +61,10 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
 // (arrival on `tmem_empty`) after its last column has been read.
 // RELEASE selects how the accumulator is released: 0 = every lane arrives on this CTA's barrier;
 // 2 = one lane per warp arrives on `tmem_empty` given as a shared::cluster address (a CTA pair
-// releases its accumulators on the MMA-issuing CTA's barrier).
+// releases its accumulators on the MMA-issuing CTA's barrier) with cluster-scope release
+// semantics; 3 = the same arrival relaxed (the TMEM reads it covers are complete at
+// tcgen05.wait::ld, so no memory ordering is needed, and a cluster-scope release costs about a
+// microsecond).
 template <int BN, int RELEASE = 0>
 __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, uint32_t lane,
                                               __half *C, int64_t ldc, int m0, int n0, int M,
@@ -78,6 +81,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
             if constexpr (RELEASE == 2) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tmem_empty);
+            } else if constexpr (RELEASE == 3) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed_cluster(tmem_empty);
             } else {
                 mbar_arrive(tmem_empty);
             }
@@ -127,6 +133,84 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
             }
         }
         __syncwarp();
+    }
+}
+
+// Stage one 32 x 32 fp16 chunk (16 packed pairs per lane, lane = row) through this warp's 2 KB of
+// shared memory and store it with whole-sector 16-byte stores (rows >= M and columns >= N masked).
+__device__ __forceinline__ void store_chunk_staged(const uint32_t (&p)[16], uint32_t lane,
+                                                   uint32_t stage, __half *C, int64_t ldc,
+                                                   int row0, int col0, int M, int N) {
+    const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t a = stage + lane * 64 + ((j ^ sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(p[4 * j]),
+                     "r"(p[4 * j + 1]), "r"(p[4 * j + 2]), "r"(p[4 * j + 3])
+                     : "memory");
+    }
+    __syncwarp();
+    const uint32_t c16 = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t r = (lane >> 2) + 8 * i;
+        uint4 w;
+        const uint32_t a = stage + r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4);
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(a)
+                     : "memory");
+        const int grow = row0 + static_cast<int>(r);
+        const int gcol = col0 + static_cast<int>(8 * c16);
+        if (grow < M) {
+            __half *dst = C + static_cast<int64_t>(grow) * ldc + gcol;
+            if (gcol + 8 <= N) {
+                st_global_stream(dst, w);
+            } else {
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (gcol + e < N)
+                        reinterpret_cast<uint16_t *>(dst)[e] =
+                            static_cast<uint16_t>((ww[e >> 1] >> ((e & 1) * 16)) & 0xFFFF);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// As epilogue_tile (staged form; `vec` must hold), software-pipelined: the TMEM read of chunk c + 1
+// is issued before chunk c is stored, so TMEM latency overlaps the stores and the accumulator is
+// released as soon as the last chunk has been read.
+template <int BN, int RELEASE = 0>
+__device__ __forceinline__ void epilogue_tile_pipelined(uint32_t tmem_base, uint32_t q,
+                                                        uint32_t lane, __half *C, int64_t ldc,
+                                                        int m0, int n0, int M, int N,
+                                                        uint32_t tmem_empty, uint32_t stage) {
+    constexpr int NCH = BN / 32;
+    const uint32_t taddr = tmem_base + ((q * 32) << 16);
+    const int row0 = m0 + static_cast<int>(q * 32);
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr, v);
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ++ch) {
+        tmem_wait_ld();
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            p[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (ch + 1 < NCH) {
+            tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, v);
+        } else {
+            tc_fence_before();
+            if constexpr (RELEASE == 2) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tmem_empty);
+            } else {
+                mbar_arrive(tmem_empty);
+            }
+        }
+        store_chunk_staged(p, lane, stage, C, ldc, row0, n0 + ch * 32, M, N);
     }
 }
 
