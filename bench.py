@@ -15,6 +15,7 @@ GPU (independent problems, no collective: weak scaling); rank 0 prints one JSON 
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -54,7 +55,7 @@ def _dist():
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms during the timed region."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -73,7 +74,9 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin: float | None = None, t_end: float | None = None):
+        """Summarise the samples taken between t_begin and t_end (host wall-clock seconds, the
+        timed region); all samples when no window is given or none falls inside it."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -82,25 +85,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), parts[4:8]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+        inside = [r for r in rows if t_begin is not None and t_begin <= r[0] <= t_end]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[4]):
                 if v.lower() == "active":
                     reasons.add(n)
+        sm = [r[1] for r in use]
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_median": statistics.median(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "power_w_median": statistics.median(r[3] for r in use) if use else None,
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------------------ our arm
@@ -195,12 +204,14 @@ def run_ours(args, ws, rank, local):
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
+    wall0 = time.time()
     t0.record(stream)
     for i in range(args.steps):
         step(i, evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop() if rank == 0 else None
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1) if rank == 0 else None
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

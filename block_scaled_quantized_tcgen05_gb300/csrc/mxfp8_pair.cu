@@ -20,16 +20,22 @@
 //     stream would sit in the tensor pipe's in-order queue in front of the MMAs; written from
 //     registers, the scales never enter that queue.
 //
-// Hand-off: only the leader (rank 0) issues MMAs, from one thread whose loop is the kernel's
-// critical path (a pair MMA takes about as long to issue as the tensor cores take to run it), so
-// that loop does one CTA-scope barrier wait per stage and nothing else but the four MMAs and a
-// commit.  Each stage's full barrier lives in the leader and collects everything the stage needs:
-// the leader's arrival with both CTAs' data bytes, both CTAs' data loads, and one arrival from
-// each scale warp of both CTAs once its tcgen05.st have completed (tcgen05.wait::st; the arrival
-// itself is relaxed -- a release at cluster scope costs about a microsecond per stage).  Commits
-// are multicast to the empty, accumulator-full and drain barriers of both CTAs; each epilogue
-// warp of both CTAs releases the accumulator with one arrival on the leader's barrier.  Every
-// wait is bounded.
+// Hand-off: only the leader (rank 0) issues MMAs, from one thread.  The tensor pipe's queue of
+// issued MMAs is shallow (a back-to-back stream of pair MMAs is accepted at exactly the rate they
+// execute, 128 cycles each), so that thread's loop does one CTA-scope barrier wait per stage and
+// nothing else but the four MMAs and a commit.  Each stage's full barrier lives in the leader and
+// collects everything the stage needs: the leader's arrival with both CTAs' data bytes, both
+// CTAs' data loads, and one arrival from each scale warp of both CTAs once its tcgen05.st have
+// completed (tcgen05.wait::st; the arrival itself is relaxed -- a release at cluster scope costs
+// about a microsecond per stage).  Commits are multicast to the empty, accumulator-full and drain
+// barriers of both CTAs.  Each epilogue warp of both CTAs reads its whole accumulator slice into
+// registers first and releases the accumulator with one relaxed arrival on the leader's barrier
+// (its TMEM reads are complete at tcgen05.wait::ld), then stores.  Every wait is bounded.
+//
+// Measured alternatives that lost: the scales copied by tcgen05.cp from the MMA thread (in this
+// kernel the copies serialise with the MMAs once TMA traffic competes for shared memory: +13%);
+// scale warps loading the repacked scales from global memory instead of shared memory (+2%);
+// direct 16-byte row stores from the epilogue instead of the staged, sector-wide ones (+4%).
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -306,10 +312,11 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN / 2, 3>(tmem_base + half * (BN / 2), q, lane, C, ldc,
-                                     mb * 2 * BM + static_cast<int>(rank) * BM,
-                                     nb * BN + static_cast<int>(half) * (BN / 2), M, N,
-                                     c_vec != 0, lead_empty, sb + OFF_EPI + (warp - 2) * 2048);
+            epilogue_tile_early<BN / 2>(tmem_base + half * (BN / 2), q, lane, C, ldc,
+                                        mb * 2 * BM + static_cast<int>(rank) * BM,
+                                        nb * BN + static_cast<int>(half) * (BN / 2), M, N,
+                                        c_vec != 0, lead_empty,
+                                        sb + OFF_EPI + (warp - 2) * 2048);
             acc_phase ^= 1;
         }
     }

@@ -214,4 +214,95 @@ __device__ __forceinline__ void epilogue_tile_pipelined(uint32_t tmem_base, uint
     }
 }
 
+// Store 16 packed fp16 pairs (32 columns of one output row) to crow[col0 .. col0 + 31], masking
+// columns >= N; 16-byte streaming stores when `vec` (see store_row_chunk32).
+__device__ __forceinline__ void store_row_packed16(__half *crow, int col0, int N, bool vec,
+                                                   const uint32_t (&p)[16]) {
+    if (vec && col0 + 32 <= N) {
+        uint4 *dst = reinterpret_cast<uint4 *>(crow + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_global_stream(dst + i, make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]));
+    } else {
+        uint16_t *dst = reinterpret_cast<uint16_t *>(crow + col0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < N) dst[i] = static_cast<uint16_t>((p[i >> 1] >> ((i & 1) * 16)) & 0xFFFF);
+    }
+}
+
+// As epilogue_tile, but the warp's whole 32 x BN slice is read from TMEM (16 columns at a time)
+// and packed to fp16 in registers (BN / 32 x 16 of them) before anything is stored, and the accumulator is released
+// right after the reads: the next tile's MMAs wait for the TMEM reads only, while the stores run
+// under them.  Release as RELEASE = 3 of epilogue_tile (one relaxed arrival per warp on
+// `tmem_empty`, a shared::cluster address).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile_early(uint32_t tmem_base, uint32_t q, uint32_t lane,
+                                                    __half *C, int64_t ldc, int m0, int n0, int M,
+                                                    int N, bool vec, uint32_t tmem_empty,
+                                                    uint32_t stage) {
+    constexpr int NCH = BN / 32;
+    uint32_t p[NCH][16];
+#pragma unroll
+    for (int h = 0; h < 2 * NCH; ++h) {     // 16 columns per read keeps the raw values few
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem_base + ((q * 32) << 16) + h * 16, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p[h >> 1][(h & 1) * 8 + i] = pack_f16x2(__uint_as_float(v[2 * i]),
+                                                    __uint_as_float(v[2 * i + 1]));
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_relaxed_cluster(tmem_empty);
+    const int row = m0 + static_cast<int>(q * 32 + lane);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int col0 = n0 + ch * 32;
+        if (stage == 0u || !vec) {
+            if (row < M) store_row_packed16(C + static_cast<int64_t>(row) * ldc, col0, N, vec, p[ch]);
+            continue;
+        }
+        // 32 x 32 chunk through this warp's 2 KB of shared memory (16-byte chunks swizzled by row
+        // pair), then 8 rows x 64 contiguous bytes per store instruction
+        const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t a = stage + lane * 64 + ((j ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(p[ch][4 * j]),
+                         "r"(p[ch][4 * j + 1]), "r"(p[ch][4 * j + 2]), "r"(p[ch][4 * j + 3])
+                         : "memory");
+        }
+        __syncwarp();
+        const uint32_t c16 = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t r = (lane >> 2) + 8 * i;
+            uint4 w;
+            const uint32_t a = stage + r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                         : "r"(a)
+                         : "memory");
+            const int grow = m0 + static_cast<int>(q * 32 + r);
+            const int gcol = col0 + static_cast<int>(8 * c16);
+            if (grow < M) {
+                __half *dst = C + static_cast<int64_t>(grow) * ldc + gcol;
+                if (gcol + 8 <= N) {
+                    st_global_stream(dst, w);
+                } else {
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (gcol + e < N)
+                            reinterpret_cast<uint16_t *>(dst)[e] =
+                                static_cast<uint16_t>((ww[e >> 1] >> ((e & 1) * 16)) & 0xFFFF);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace qg
