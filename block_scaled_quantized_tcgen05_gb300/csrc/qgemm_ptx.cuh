@@ -179,6 +179,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory, completion counted on an mbarrier (bytes).
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // L2 cache policy for TMA loads whose data is reused across many CTAs (keep resident).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
