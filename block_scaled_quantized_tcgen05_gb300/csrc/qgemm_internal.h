@@ -61,6 +61,10 @@ cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64
                             bool *encode_ok);
 cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
                          int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
+// CTA-pair W4A16 with the dequantised weights in TMEM (w4a16_pair.cu).
+bool w4a16_pair_eligible(int M, const qgemm_tensor *W);
+cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
+                              __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
                            __half *Y, int64_t ldy, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);

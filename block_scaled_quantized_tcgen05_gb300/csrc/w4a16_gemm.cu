@@ -20,6 +20,7 @@
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
+#include "w4a16_convert.cuh"
 
 namespace {
 
@@ -64,82 +65,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// fp16 bits of 2^(e-127) for e in [103, 142] (subnormals below 2^-14); outside that range the
-// nearest representable behaviour: 0 below, +inf above.
-__device__ __forceinline__ uint32_t ue8m0_to_f16x2(uint32_t e) {
-    const int x = static_cast<int>(e) - 127;
-    uint32_t h;
-    if (x > 15) h = 0x7C00u;
-    else if (x >= -14) h = static_cast<uint32_t>(x + 15) << 10;
-    else if (x >= -24) h = 1u << (x + 24);
-    else h = 0u;
-    return h | (h << 16);
-}
-
-// Fused path, exact for scale exponents x = e - 127 in [-10, 5]: byte j of the biased word is
-// spread to both halves, the low nibble as 1024 + u and the high nibble as 1024 + 16 u, and one
-// fp16x2 FMA with per-half constants (s, s/16) and (-1032 s, -72 s) gives (q_lo s, q_hi s).
-__device__ __forceinline__ bool fused_ok(uint32_t e) { return e >= 117u && e <= 132u; }
-
-__device__ __forceinline__ void fused_consts(uint32_t e, uint32_t &s2, uint32_t &c2) {
-    const uint32_t x15 = e - 112u;                          // x + 15
-    const uint32_t s = x15 << 10, s16 = (x15 - 4u) << 10;   // 2^x, 2^(x-4)
-    const uint32_t c1032 = 0x8000u | ((x15 + 10u) << 10) | 8u;    // -1032 * 2^x
-    const uint32_t c72 = 0x8000u | ((x15 + 6u) << 10) | 128u;     // -72 * 2^x
-    s2 = s | (s16 << 16);
-    c2 = c1032 | (c72 << 16);
-}
-
-__device__ __forceinline__ void i4x8_to_f16_fused(uint32_t v, uint32_t s2, uint32_t c2,
-                                                  uint32_t (&o)[4]) {
-    const uint32_t u = v ^ 0x88888888u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t b = __byte_perm(u, 0u, 0x4040u | (j << 8) | j);   // byte j in both halves
-        uint32_t tv;
-        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(tv) : "r"(b), "r"(0x00F0000Fu), "r"(0x64006400u));
-        o[j] = h2_fma(tv, s2, c2);
-    }
-}
-
-// 8 int4 (one 32-bit word, k = 8w .. 8w+7, even k in low nibbles) times the fp16x2 scale ->
-// four fp16x2 words in k order.
-__device__ __forceinline__ void i4x8_to_f16(uint32_t v, uint32_t s2, uint32_t (&o)[4]) {
-    const uint32_t u = v ^ 0x88888888u;  // q + 8 in every nibble
-    const uint32_t MAGIC = 0x64006400u;   // fp16 1024.0 in both halves
-    const uint32_t t0 = (u & 0x000F000Fu) | MAGIC;         // 1024 + u(k0), 1024 + u(k4)
-    const uint32_t t1 = (u & 0x00F000F0u) | MAGIC;         // 1024 + 16 u(k1), ... (k5)
-    const uint32_t t2 = ((u >> 8) & 0x000F000Fu) | MAGIC;  // k2, k6
-    const uint32_t t3 = ((u >> 8) & 0x00F000F0u) | MAGIC;  // k3, k7
-    const uint32_t B1032 = 0x64086408u;   // 1032.0
-    const uint32_t R16 = 0x2C002C00u;     // 1/16
-    const uint32_t N72 = 0xD480D480u;     // -72.0
-    const uint32_t h0 = h2_mul(h2_sub(t0, B1032), s2);         // (q0, q4) * s
-    const uint32_t h1 = h2_mul(h2_fma(t1, R16, N72), s2);      // (q1, q5) * s
-    const uint32_t h2 = h2_mul(h2_sub(t2, B1032), s2);         // (q2, q6) * s
-    const uint32_t h3 = h2_mul(h2_fma(t3, R16, N72), s2);      // (q3, q7) * s
-    o[0] = __byte_perm(h0, h1, 0x5410);  // (q0, q1)
-    o[1] = __byte_perm(h2, h3, 0x5410);  // (q2, q3)
-    o[2] = __byte_perm(h0, h1, 0x7632);  // (q4, q5)
-    o[3] = __byte_perm(h2, h3, 0x7632);  // (q6, q7)
 }
 
 template <bool SF_VEC>
@@ -640,6 +565,8 @@ namespace qgi {
 
 cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
                          int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
+    // CTA pairs with the weights dequantised into TMEM when the shape allows (w4a16_pair.cu)
+    if (w4a16_pair_eligible(M, W)) return launch_w4a16_pair(A, lda, M, W, C, ldc, ctx, encode_ok);
     const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
     CUtensorMap tmA;
     *encode_ok = encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM,

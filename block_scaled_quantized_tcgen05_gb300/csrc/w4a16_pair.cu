@@ -1,0 +1,377 @@
+// w4a16_pair.cu -- weight-only int4 GEMM on CTA pairs with the dequantised weights in TMEM.
+//
+// C[M, N] = fp16_rn( sum_k A[m, k] * q(W[n, k]) * 2^(SW[n, k/32] - 127) ),  fp32 accumulation.
+//
+// "TensorOps: quantized matmul ..." (sections "Revised kernel strategy" and "M2 = block-32 fp16
+// scaling") dequantises each 32-block of int4 weights into on-chip memory and runs the half x
+// half product there; its escape-hatch note asks for the dequantised weights to go straight into
+// the operand the matrix unit reads.  On GB300 the tensor core can read its A operand from TMEM,
+// so this kernel computes the transposed product D[n, m] = sum_k W[n, k] A[m, k] with the weights
+// as the A operand in TMEM and the activations as the B operand in shared memory:
+//
+//   * a cluster of two CTAs computes a 256 (weight rows) x 256 (tokens) tile with
+//     tcgen05.mma.cta_group::2.kind::f16; each CTA holds 128 weight rows in its TMEM and 128
+//     token rows of A in its shared memory;
+//   * converter warps -- two per TMEM lane quarter, taking alternate k-tiles -- read the packed
+//     int4 bytes of their 32 weight rows (one row per lane, landed by TMA), turn each 32-block
+//     into fp16 with its scale in registers and write the 64-element k-tile into the stage's TMEM
+//     slot with one tcgen05.st (32 columns, two fp16 per column, even k in the low half);
+//   * the dequantised weights never touch shared memory, whose bandwidth (TMA writes plus tensor
+//     reads) is what bounds a weight-in-shared-memory design;
+//   * the epilogue reads D (lane = weight row n, column = token m) and stores C[m, n]: each lane
+//     owns one output column, so a warp writes 64 contiguous bytes of a token row per store.
+//
+// Hand-off as in mxfp8_pair.cu: the leader issues every MMA from one thread and waits once per
+// stage on its full barrier, which collects both CTAs' activation bytes and one relaxed arrival
+// from each converter warp of both CTAs after its tcgen05.st completed; commits are multicast;
+// every wait is bounded.  Used for K % 512 == 0 with 16-byte aligned scale rows (scales are read
+// 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.
+#include "qgemm_common.cuh"
+#include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
+#include "w4a16_convert.cuh"
+
+namespace {
+
+using namespace qg;
+
+constexpr int BW = 128;                 // weight rows per CTA (256 per pair: the MMA's M)
+constexpr int BT = 256;                 // tokens per pair tile (the MMA's N), 128 per CTA
+constexpr int BK = 64;                  // k per stage
+constexpr int STAGES = 8;
+constexpr int EPI_WARPS = 8;            // two per lane quarter, one per half of the 256 tokens
+constexpr int CONV_WARP0 = 2 + EPI_WARPS;
+constexpr int CONV_WARPS = 8;           // two per lane quarter, alternate k-tiles
+constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COL0 = 256;        // weight slots after the 256-column accumulator
+constexpr uint32_t A_COLS = BK / 2;     // 32 columns per stage
+
+constexpr uint32_t X_BYTES = (BT / 2) * BK * 2;   // 16 KB: this CTA's 128 token rows
+constexpr uint32_t RAW_BYTES = BW * (BK / 2);     // 4 KB: packed int4 of this CTA's weight rows
+constexpr uint32_t STAGE_TX = 2 * X_BYTES;        // both CTAs' activations, on the leader
+constexpr uint32_t OFF_X = 0;
+constexpr uint32_t OFF_RAW = OFF_X + STAGES * X_BYTES;
+constexpr uint32_t OFF_BAR = OFF_RAW + STAGES * RAW_BYTES;
+// full[S] (leader), empty[S], raw_full[S], tmem_full, tmem_empty (leader), drain, then the slot
+constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
+constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(A_COL0 + STAGES * A_COLS <= TMEM_COLS, "TMEM budget");
+
+// kind::f16: D fp32, A and B fp16, K-major, N = 256 tokens, M = 256 weight rows (pair).
+constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BT >> 3) << 17) |
+                           (static_cast<uint32_t>(256 >> 4) << 24);
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ void st_global_cs_u16(__half *p, uint16_t v) {
+    asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  const uint8_t *__restrict__ scales, int64_t lds, __half *__restrict__ C,
+                  int64_t ldc, int M, int N, int K, unsigned *err, uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();      // 0 = leader
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    auto raw_full = [&](int s) { return sb + OFF_BAR + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (3 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t drain_bar = tmem_full + 16;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
+
+    // tiles: weight-row blocks of 256 (the "m" of tile_coords) x token blocks of 256
+    const int tiles_w = (N + 2 * BW - 1) / (2 * BW);
+    const int tiles_t = (M + BT - 1) / BT;
+    const int num_tiles = tiles_w * tiles_t;
+    const int KT = K / BK;
+    const int my_tiles = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
+    const int total = my_tiles * KT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1 + 2 * (CONV_WARPS / 2));   // expect_tx + converters of a stage
+            mbar_init(empty_bar(s), 1);                          // leader's multicast commit
+            mbar_init(raw_full(s), 1);                           // this CTA's packed-int4 TMA
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 2 * EPI_WARPS);   // one lane of each epilogue warp of both CTAs
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                   // barriers of both CTAs initialised before remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                int wb, tb;
+                tile_coords(tile, tiles_w, tiles_t, wb, tb);
+                const int w0 = wb * 2 * BW + static_cast<int>(rank) * BW;     // this CTA's weights
+                const int t0 = tb * BT + static_cast<int>(rank) * (BT / 2);   // this CTA's tokens
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+                    tma_load_2d_pair(sb + OFF_X + stage * X_BYTES, &tmX, lead_full, kt * BK, t0);
+                    mbar_arrive_expect_tx(raw_full(stage), RAW_BYTES);
+                    tma_load_2d(sb + OFF_RAW + stage * RAW_BYTES, &tmW, raw_full(stage),
+                                kt * (BK / 2), w0);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) atomicOr(err, ERR_PRODUCER);
+            for (int i = max(0, issued - STAGES); i < issued; ++i) {
+                if (!mbar_wait(raw_full(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
+                    atomicOr(err, ERR_DRAIN);
+                    break;
+                }
+                if (rank == 0 &&
+                    !mbar_wait_cluster(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
+                    atomicOr(err, ERR_DRAIN);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (rank == 0 && lane == 0) {
+            // --------------------------------------------------------- MMA issuer
+            const uint64_t bdesc0 = smem_desc(sb + OFF_X, 16, 1024, SWZ_128B);
+            uint32_t acc_phase = 0, stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_col = tmem_base + A_COL0 + stage * A_COLS;
+                    const uint64_t bdesc = bdesc0 + stage * (X_BYTES >> 4);
+                    mma_f16_pair_ta(tmem_base, a_col, bdesc, IDESC, kt > 0 ? 1u : 0u);
+#pragma unroll
+                    for (uint32_t j = 1; j < BK / 16; ++j)
+                        mma_f16_pair_ta(tmem_base, a_col + 8 * j, bdesc + 2 * j, IDESC, 1u);
+                    tc_commit_pair(empty_bar(stage), 3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(tmem_full, 3);
+                acc_phase ^= 1;
+            }
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit_pair(drain_bar, 3);
+        }
+        __syncwarp();
+        // both CTAs: every pair MMA writing this CTA's TMEM has completed before it is freed
+        if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
+    } else if (warp >= CONV_WARP0) {
+        // ----------------------------------------------------------------- converters
+        // Lane i of a warp of lane quarter q dequantises weight row 32 q + i of this CTA's 128;
+        // the two warps of a quarter take the even and the odd stages of the sequence.
+        const uint32_t q = warp & 3;
+        const int parity = static_cast<int>(warp - CONV_WARP0) >> 2;
+        const uint32_t lead_full = map_to_cta(full_bar(0), 0);
+        const int r = static_cast<int>(q * 32 + lane);
+        const int KG = KT / 8;                   // 16-byte scale groups per weight row
+        // scale group cache: the group of (tile index ti, group g), and the next one prefetched
+        auto group_ptr = [&](int ti, int g) -> const uint8_t * {
+            const int tile = pair + ti * npairs;
+            if (tile >= num_tiles) return nullptr;
+            int wb, tb;
+            tile_coords(tile, tiles_w, tiles_t, wb, tb);
+            const int n = wb * 2 * BW + static_cast<int>(rank) * BW + r;
+            return n < N ? scales + static_cast<int64_t>(n) * lds + 16 * g : nullptr;
+        };
+        const uint4 unit = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        int cur_ti = 0, cur_g = 0;
+        const uint8_t *p0 = total > 0 ? group_ptr(0, 0) : nullptr;
+        uint4 cur = p0 ? ld_nc_v4(p0) : unit;
+        int nxt_ti = KG > 1 ? 0 : 1, nxt_g = KG > 1 ? 1 : 0;
+        const uint8_t *p1 = total > 0 ? group_ptr(nxt_ti, nxt_g) : nullptr;
+        uint4 nxt = p1 ? ld_nc_v4(p1) : unit;
+        uint32_t stage = 0, phase = 0;
+        for (int it = 0; it < total; ++it) {
+            const int ti = it / KT, kt = it - ti * KT;
+            const int g = kt >> 3;
+            if (ti != cur_ti || g != cur_g) {    // move to the next scale group, prefetch one more
+                cur = nxt;
+                cur_ti = nxt_ti;
+                cur_g = nxt_g;
+                if (++nxt_g == KG) {
+                    nxt_g = 0;
+                    ++nxt_ti;
+                }
+                const uint8_t *pn = group_ptr(nxt_ti, nxt_g);
+                nxt = pn ? ld_nc_v4(pn) : unit;
+            }
+            if ((it & 1) == parity) {
+                if (!mbar_wait(raw_full(stage), phase, timeout_ns)) {
+                    if (lane == 0) atomicOr(err, ERR_PRODUCER);
+                    break;
+                }
+                tc_fence_after();   // the MMAs that last read this TMEM slot have completed
+                const uint8_t *raw = smem + OFF_RAW + stage * RAW_BYTES + r * (BK / 2);
+                const uint4 lo = *reinterpret_cast<const uint4 *>(raw);        // k  0..31
+                const uint4 hi = *reinterpret_cast<const uint4 *>(raw + 16);   // k 32..63
+                const int sbyte = (kt & 7) * 2;       // this stage's two scale bytes in the group
+                const int wsel = sbyte >> 2;
+                const uint32_t word = wsel == 0 ? cur.x : wsel == 1 ? cur.y : wsel == 2 ? cur.z : cur.w;
+                uint32_t out[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t e = (word >> (8 * ((sbyte & 3) + h))) & 0xFFu;
+                    const uint4 d = h ? hi : lo;
+                    const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+                    if (fused_ok(e)) {
+                        uint32_t s2, c2;
+                        fused_consts(e, s2, c2);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t o[4];
+                            i4x8_to_f16_fused(words[w], s2, c2, o);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
+                        }
+                    } else {
+                        const uint32_t s2 = ue8m0_to_f16x2(e);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t o[4];
+                            i4x8_to_f16(words[w], s2, o);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
+                        }
+                    }
+                }
+                tmem_st_32x32b_x32(tmem_base + ((q * 32) << 16) + A_COL0 + stage * A_COLS, out);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * stage);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        // Lane i of a warp of lane quarter q holds output column n = weight row 32 q + i; the
+        // warp covers 128 of the tile's 256 tokens, 32 per TMEM read.
+        const uint32_t q = warp & 3;
+        const uint32_t half = (warp - 2) >> 2;
+        const uint32_t lead_empty = map_to_cta(tmem_empty, 0);
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs) {
+            int wb, tb;
+            tile_coords(tile, tiles_w, tiles_t, wb, tb);
+            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int n = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32 + lane);
+            const int m0 = tb * BT + static_cast<int>(half) * (BT / 2);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + half * (BT / 2) + ch * 32, v);
+                tmem_wait_ld();
+                if (ch == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_relaxed_cluster(lead_empty);
+                }
+                if (n < N) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int m = m0 + ch * 32 + c;
+                        if (m < M)
+                            st_global_cs_u16(C + static_cast<int64_t>(m) * ldc + n,
+                                             __half_as_ushort(__float2half_rn(__uint_as_float(v[c]))));
+                    }
+                }
+            }
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                   // no remote arrival or multicast targets an exited CTA
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+}  // namespace
+
+namespace qgi {
+
+bool w4a16_pair_eligible(int M, const qgemm_tensor *W) {
+    return M > BT / 2 && W->rows > BW && W->k % 512 == 0 &&
+           reinterpret_cast<uintptr_t>(W->scales) % 16 == 0 && W->lds % 16 == 0;
+}
+
+cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
+                              __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
+    const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
+    CUtensorMap tmX, tmW;
+    *encode_ok = encode_tma_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
+                               BT / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K / 2, N, W->ld,
+                               BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(w4a16_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((N + 2 * BW - 1) / (2 * BW)) * ((M + BT - 1) / BT);
+    int pairs = ctx.num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    w4a16_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
+        tmX, tmW, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace qgi

@@ -248,6 +248,33 @@ def test_w4a16_matches_oracle(dev, orc, M, N, K):
     _check(C, res, orc, what=f"w4a16 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 640, 1536), (1000, 1000, 512), (129, 136, 512)])
+def test_w4a16_pair_path_ragged(dev, orc, M, N, K):
+    """Shapes of the CTA-pair route (M > 128, N > 128, K % 512 == 0, aligned scale rows) with
+    ragged token and weight tiles and several scale groups."""
+    d = synth.w4a16_inputs(M, N, K, seed=7 * M + N)
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(d["a"].to(dev), W, C)
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    _check(C, res, orc, what=f"w4a16 pair {M}x{N}x{K}")
+
+
+def test_w4a16_scales_outside_fused_window(dev, orc):
+    """Scale exponents on both sides of the fused conversion's window (117..132) take the exact
+    general path; every block gets one of 104, 110, 116, 117, 132, 133, 139."""
+    M, N, K = 256, 384, 1024
+    d = synth.w4a16_inputs(M, N, K, seed=99)
+    exps = torch.tensor([104, 110, 116, 117, 132, 133, 139], dtype=torch.uint8)
+    sw = exps[torch.randint(0, 7, d["sw"].shape, generator=synth.generator(5))].contiguous()
+    a = (d["a"].float() * 2.0 ** -6).to(torch.float16)      # keep products inside fp16 range
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), sw.to(dev))
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(a.to(dev), W, C)
+    res = orc.w4a16(a.numpy(), d["w"].numpy(), sw.numpy())
+    _check(C, res, orc, what="w4a16 extreme scales")
+
+
 def test_w4a16_full_size_sampled(dev, orc):
     d = synth.workload("w4a16_prefill")
     W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
