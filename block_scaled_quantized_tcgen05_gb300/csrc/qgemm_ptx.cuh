@@ -221,6 +221,23 @@ __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, in
                  : "memory");
 }
 
+// 2-D tiled bulk tensor store shared -> global (bulk-group completion); out-of-range parts of the
+// box are not written.  Wait with bulk_wait_read before the shared memory is reused.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's bulk stores have finished reading shared memory (all but the newest N groups).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// This thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 16-byte global store marked streaming (evict-first), for outputs that are not re-read.
 __device__ __forceinline__ void st_global_stream(void *p, uint4 v) {
     asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),

@@ -18,8 +18,13 @@
 //     slot with one tcgen05.st (32 columns, two fp16 per column, even k in the low half);
 //   * the dequantised weights never touch shared memory, whose bandwidth (TMA writes plus tensor
 //     reads) is what bounds a weight-in-shared-memory design;
-//   * the epilogue reads D (lane = weight row n, column = token m) and stores C[m, n]: each lane
-//     owns one output column, so a warp writes 64 contiguous bytes of a token row per store.
+//   * the epilogue reads D (lane = weight row n, column = token m); each lane owns one output
+//     column, so it writes its 32 tokens of a chunk as 2-byte stores into the warp's shared
+//     staging, laid out [token][32 columns] (one 64-byte row per store instruction, no bank
+//     conflicts); the accumulator is released right after the last TMEM read and the staged
+//     32 x 32 blocks go out as TMA tensor stores, so no tile waits for the output traffic (all pairs
+//     reach their epilogue together and the stores come in bursts).  C not 16-byte aligned, or
+//     its row stride not a multiple of 8, takes direct 2-byte global stores instead.
 //
 // Hand-off as in mxfp8_pair.cu: the leader issues every MMA from one thread and waits once per
 // stage on its full barrier, which collects both CTAs' activation bytes and one relaxed arrival
@@ -52,7 +57,9 @@ constexpr uint32_t RAW_BYTES = BW * (BK / 2);     // 4 KB: packed int4 of this C
 constexpr uint32_t STAGE_TX = 2 * X_BYTES;        // both CTAs' activations, on the leader
 constexpr uint32_t OFF_X = 0;
 constexpr uint32_t OFF_RAW = OFF_X + STAGES * X_BYTES;
-constexpr uint32_t OFF_BAR = OFF_RAW + STAGES * RAW_BYTES;
+constexpr uint32_t EPI_BYTES = 4 * 32 * 32 * 2;     // per epilogue warp: 4 chunks of 32 x 32 fp16
+constexpr uint32_t OFF_EPI = OFF_RAW + STAGES * RAW_BYTES;
+constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BYTES;
 // full[S] (leader), empty[S], raw_full[S], tmem_full, tmem_empty (leader), drain, then the slot
 constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
@@ -71,8 +78,13 @@ __device__ __forceinline__ void st_global_cs_u16(__half *p, uint16_t v) {
     asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  const __grid_constant__ CUtensorMap tmC, int c_tma,
                   const uint8_t *__restrict__ scales, int64_t lds, __half *__restrict__ C,
                   int64_t ldc, int M, int N, int K, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -112,6 +124,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         fence_barrier_init();
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmW);
+        if (c_tma) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
@@ -312,8 +325,14 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 break;
             }
             tc_fence_after();
-            const int n = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32 + lane);
+            const int n0 = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32);
+            const int n = n0 + static_cast<int>(lane);
             const int m0 = tb * BT + static_cast<int>(half) * (BT / 2);
+            const uint32_t stg = sb + OFF_EPI + (warp - 2) * EPI_BYTES;
+            if (c_tma) {   // the previous tile's stores have finished reading the staging
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+            }
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t v[32];
@@ -324,7 +343,13 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive_relaxed_cluster(lead_empty);
                 }
-                if (n < N) {
+                if (c_tma) {
+                    // row c of the chunk: tokens m0 + 32 ch + c, columns n0 .. n0 + 31
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        st_shared_u16(stg + ch * 2048 + c * 64 + lane * 2,
+                                      __half_as_ushort(__float2half_rn(__uint_as_float(v[c]))));
+                } else if (n < N) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int m = m0 + ch * 32 + c;
@@ -334,8 +359,20 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     }
                 }
             }
+            if (c_tma) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)   // blocks wholly past M or N are not stored
+                        if (n0 < N && m0 + ch * 32 < M)
+                            tma_store_2d(&tmC, stg + ch * 2048, n0, m0 + ch * 32);
+                    bulk_commit();
+                }
+            }
             acc_phase ^= 1;
         }
+        if (c_tma && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -357,12 +394,21 @@ bool w4a16_pair_eligible(int M, const qgemm_tensor *W) {
 cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
                               __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
     const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
-    CUtensorMap tmX, tmW;
+    CUtensorMap tmX, tmW, tmC;
     *encode_ok = encode_tma_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
                                BT / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
                  encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K / 2, N, W->ld,
                                BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!*encode_ok) return cudaErrorInvalidValue;
+    // output through TMA stores when C and its row stride allow a tensor map
+    const int c_tma = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    if (c_tma) {
+        *encode_ok = encode_tma_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2, 32, 32,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!*encode_ok) return cudaErrorInvalidValue;
+    } else {
+        tmC = tmX;   // unused
+    }
     cudaError_t e = cudaFuncSetAttribute(w4a16_pair_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -370,7 +416,7 @@ cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_t
     int pairs = ctx.num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     w4a16_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmX, tmW, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
+        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 
