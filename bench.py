@@ -36,6 +36,28 @@ METRIC = "MXFP8 GEMM TFLOP/s at 8192^3 (% of GB300 FP8 peak); W8 GEMV GB/s (% of
 WORKLOAD = "mxfp8_8192 + f16_4096 + w4a16_prefill + w8_decode(M=1,8,16)"
 
 
+def _mxfp8_traffic():
+    """DRAM bytes of one qgemm_mxfp8 call at 8192^3 from the committed ncu figures, or None when
+    the kernel sources have changed since those counters were taken (their sha1 no longer match)."""
+    import hashlib
+    import re
+    root = os.path.dirname(os.path.abspath(__file__))
+    try:
+        text = open(os.path.join(root, "profiles", "mxfp8_pair_8192_traffic.txt")).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_call: (\d+) sha1\(mxfp8_pair.cu\): ([0-9a-f]+) "
+                  r"sha1\(qgemm_common.cuh\): ([0-9a-f]+)", text)
+    if not m:
+        return None
+    csrc = os.path.join(root, "block_scaled_quantized_tcgen05_gb300", "csrc")
+    for name, want in (("mxfp8_pair.cu", m.group(2)), ("qgemm_common.cuh", m.group(3))):
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != want:
+                return None
+    return int(m.group(1))
+
+
 def _peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -279,7 +301,8 @@ def run_ours(args, ws, rank, local):
             "unit": "TFLOP/s", "frac": round(mx_tflops / fp8_peak_sust, 4),
             "peak_source": f"{peak_kind} bf16 sustained x 2 (nominal fp8/bf16 ratio)",
             "frac_of_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4),
-            "traffic": None},
+            "traffic": _mxfp8_traffic(), "traffic_unit": "bytes per call (ncu, dram read + write)",
+            "algorithmic_bytes": 2 * 8192 * 8192 + 2 * 8192 * 256 + 2 * 8192 * 8192},
         "kernels": secondary,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -391,7 +414,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
