@@ -58,6 +58,23 @@ def _mxfp8_traffic():
     return int(m.group(1))
 
 
+def max_over_ranks(values, ws: int, device):
+    """Element-wise maximum of a list of floats over all ranks of the default process group
+    (the identity at world size 1): every rank's timings become the slowest rank's."""
+    if ws <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(ws: int, work_per_rank: float, ms: float) -> float:
+    """Throughput of the whole job: the work all ranks did over the (max-over-ranks) time."""
+    return ws * work_per_rank / (ms * 1e-3)
+
+
 def _peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -244,12 +261,9 @@ def run_ours(args, ws, rank, local):
     per = {k: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
            for j, k in enumerate(kernels)}
     mean = {k: sum(v) / len(v) for k, v in per.items()}
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms] + [mean[k] for k in kernels], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
-        mean = {k: float(t[1 + j]) for j, k in enumerate(kernels)}
+    agg = max_over_ranks([total_ms] + [mean[k] for k in kernels], ws, dev)
+    total_ms = agg[0]
+    mean = {k: agg[1 + j] for j, k in enumerate(kernels)}
 
     # ----------------------------------------------------------- e2e through host buffers
     e2e = None
@@ -281,7 +295,8 @@ def run_ours(args, ws, rank, local):
         mx_tflops = flops["mxfp8"] / (mean["mxfp8"] * 1e-3) / 1e12
         secondary["mxfp8"] = {"us": round(mean["mxfp8"] * 1e3, 2), "tflops": round(mx_tflops, 1),
                               "frac_of_fp8_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4)}
-    value = ws * mx_tflops if mx_tflops is not None else None
+    value = (whole_job_rate(ws, flops["mxfp8"], mean["mxfp8"]) / 1e12
+             if mx_tflops is not None else None)
     # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM)
     launches = sum(2 if k == "mxfp8" else 1 for k in kernels) * args.steps
     line = {
