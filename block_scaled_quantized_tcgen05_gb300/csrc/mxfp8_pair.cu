@@ -38,7 +38,11 @@
 // scale warps loading the repacked scales from global memory instead of shared memory (+2%);
 // direct 16-byte row stores from the epilogue instead of the staged, sector-wide ones (+4%);
 // the scale blocks as 2-D tensor boxes 16 bytes wide (+0.6%); raster groups of 8 or 32 pair rows
-// instead of 16 (+1%, +5%); L2 prefetch of A and B eight k-tiles ahead (+10%).
+// instead of 16 (+1%, +5%); L2 prefetch of A and B eight k-tiles ahead (+10%); clusters of four
+// (two pairs sharing the N tile, each B half loaded once and multicast to both pairs: +8%; only
+// 36 such clusters fit on the GPU's 152 SMs, and multicast halves L2 reads but not the shared
+// memory each SM writes and its tensor core reads, which is what bounds this kernel -- loading
+// half of B, with wrong results, is 9% faster, half of A 6%).
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
