@@ -197,7 +197,9 @@ def run_ours(args, ws, rank, local):
         Ys = {m: torch.empty(m, 28672, dtype=torch.float16, device=dev) for m in (1, 8, 16)}
         del gv
 
-    all_kernels = ["mxfp8", "f16", "w4a16", "gemv_m1", "gemv_m8", "gemv_m16"]
+    # the decode GEMVs run after the fp16 GEMM (33 MB of output) rather than after W4A16, whose
+    # 117 MB of output is still being written back from L2 when the next kernel starts
+    all_kernels = ["mxfp8", "w4a16", "f16", "gemv_m1", "gemv_m8", "gemv_m16"]
     kernels = [k for k in all_kernels if want(k.split("_")[0])]
     stream = torch.cuda.current_stream()
 
@@ -261,9 +263,12 @@ def run_ours(args, ws, rank, local):
     per = {k: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
            for j, k in enumerate(kernels)}
     mean = {k: sum(v) / len(v) for k, v in per.items()}
-    agg = max_over_ranks([total_ms] + [mean[k] for k in kernels], ws, dev)
+    median = {k: statistics.median(v) for k, v in per.items()}
+    agg = max_over_ranks([total_ms] + [mean[k] for k in kernels] + [median[k] for k in kernels],
+                         ws, dev)
     total_ms = agg[0]
     mean = {k: agg[1 + j] for j, k in enumerate(kernels)}
+    median = {k: agg[1 + len(kernels) + j] for j, k in enumerate(kernels)}
 
     # ----------------------------------------------------------- e2e through host buffers
     e2e = None
@@ -280,20 +285,24 @@ def run_ours(args, ws, rank, local):
     for k in kernels:
         if k in ("f16", "w4a16"):
             tf = flops[k] / (mean[k] * 1e-3) / 1e12
-            secondary[k] = {"us": round(mean[k] * 1e3, 2), "tflops": round(tf, 1),
+            secondary[k] = {"us": round(mean[k] * 1e3, 2), "us_median": round(median[k] * 1e3, 2),
+                            "tflops": round(tf, 1),
                             "frac_of_f16_spec_2250": round(tf / SPEC_F16_TFLOPS, 4),
                             "frac_of_measured_bf16_sustained": round(
                                 tf / peaks.get("bf16_tflops_sustained", 1700.0), 4)}
         elif k.startswith("gemv"):
             m = int(k[6:])
             gbs = gemv_bytes[m] / (mean[k] * 1e-3) / 1e9
-            secondary[k] = {"us": round(mean[k] * 1e3, 2), "gbs": round(gbs, 1),
+            secondary[k] = {"us": round(mean[k] * 1e3, 2), "us_median": round(median[k] * 1e3, 2),
+                            "gbs": round(gbs, 1),
                             "frac_of_measured_hbm": round(gbs / hbm, 4),
                             "frac_of_spec_hbm_8000": round(gbs / SPEC_HBM_GBS, 4)}
     mx_tflops = None
     if "mxfp8" in mean:
         mx_tflops = flops["mxfp8"] / (mean["mxfp8"] * 1e-3) / 1e12
-        secondary["mxfp8"] = {"us": round(mean["mxfp8"] * 1e3, 2), "tflops": round(mx_tflops, 1),
+        secondary["mxfp8"] = {"us": round(mean["mxfp8"] * 1e3, 2),
+                              "us_median": round(median["mxfp8"] * 1e3, 2),
+                              "tflops": round(mx_tflops, 1),
                               "frac_of_fp8_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4)}
     value = (whole_job_rate(ws, flops["mxfp8"], mean["mxfp8"]) / 1e12
              if mx_tflops is not None else None)
