@@ -243,6 +243,28 @@ def w8_gemv(x, w, sw) -> Result:
     return Result(C, D, None)
 
 
+def epilogue(res: Result, c_old=None, relu: bool = False) -> Result:
+    """The fused output epilogue on an exact product.
+
+    "TensorOps: quantized matmul ..." (section "The real matmul2d API"): mode multiply_accumulate
+    computes C = A*B + C.  "Running inline ML operations in a shader with Metal 4" (section
+    "Combine an element-wise function"): ReLU, max(x, 0), on each product element before the
+    store.  Here C' = relu?(C + C_old) in fp64, rounded once to fp16 by Result; C_old (fp16, the
+    shape of res.C) is exact in fp64 and adds |C_old| to the magnitude D of the tolerance.
+    ReLU of x <= 0 is +0."""
+    C = np.array(res.C, np.float64, copy=True)
+    D = np.array(res.D, np.float64, copy=True)
+    if c_old is not None:
+        old = np.asarray(c_old, np.float16).astype(np.float64)
+        if old.shape != C.shape:
+            raise ValueError(f"c_old shape {old.shape} != result shape {C.shape}")
+        C = C + old
+        D = D + np.abs(old)
+    if relu:
+        C = np.where(C > 0.0, C, 0.0)
+    return Result(C, D, res.rows)
+
+
 def dequant_plane(dtype: int, data, scales, k: int) -> np.ndarray:
     """What the dequantise-only debug kernel must reproduce: decoded fp64 values."""
     return dequant(dtype, data, scales, None, k)

@@ -238,3 +238,45 @@ def test_tolerance_check_catches_planted_error(orc):
     bad[3, 7] += 0.01 * res.D[3, 7] + 1e-3
     ok, _, info = orc.within_tolerance(bad, res)
     assert not ok and info["n_bad"] == 1
+
+
+def test_epilogue_hand_worked_example(orc):
+    """Fused epilogue on a product worked out by hand: A = [[1, 2], [3, 4]] (E4M3 codes 0x38,
+    0x40, 0x44, 0x48, scale 2^0, K padded to 32 with zeros), B = [[1, -1], [2, 0.5]].
+    A B^T = [[1 - 2, 2 + 1], [3 - 4, 6 + 2]] = [[-1, 3], [-1, 8]]."""
+    a = np.zeros((2, 32), np.uint8)
+    a[0, :2] = [0x38, 0x40]          # 1, 2
+    a[1, :2] = [0x44, 0x48]          # 3, 4
+    b = np.zeros((2, 32), np.uint8)
+    b[0, :2] = [0x38, 0xB8]          # 1, -1
+    b[1, :2] = [0x40, 0x30]          # 2, 0.5
+    s = np.full((2, 1), 127, np.uint8)
+    res = orc.mxfp8(a, s, b, s)
+    assert res.C.tolist() == [[-1.0, 3.0], [-1.0, 8.0]]
+    # multiply_accumulate with C_old = [[0.5, -4], [1, -8]]: [[-0.5, -1], [0, 0]]
+    old = np.array([[0.5, -4.0], [1.0, -8.0]], np.float16)
+    acc = orc.epilogue(res, old)
+    assert acc.C.tolist() == [[-0.5, -1.0], [0.0, 0.0]]
+    assert acc.D.tolist() == [[3.5, 7.0], [8.0, 16.0]]    # sum |a b| (3, 3, 7, 8) + |C_old|
+    # ReLU alone, then both
+    assert orc.epilogue(res, relu=True).C.tolist() == [[0.0, 3.0], [0.0, 8.0]]
+    both = orc.epilogue(res, old, relu=True)
+    assert both.C.tolist() == [[0.0, 0.0], [0.0, 0.0]]
+    assert not np.signbit(both.C).any()                    # ReLU of x <= 0 is +0
+    assert both.f16_bits.tolist() == [[0, 0], [0, 0]]
+
+
+def test_epilogue_invariants(orc):
+    """Accumulating zeros is the plain product; accumulating -C (exact for integer products)
+    then ReLU gives +0 everywhere; ReLU leaves positive entries unchanged."""
+    g = np.random.default_rng(3)
+    a = g.integers(-4, 5, (6, 64)).astype(np.float64)
+    b = g.integers(-4, 5, (5, 64)).astype(np.float64)
+    C, D = orc.dot_rows(a, b)
+    res = orc.Result(C, D, None)
+    z = orc.epilogue(res, np.zeros(C.shape, np.float16))
+    assert np.array_equal(z.C, res.C) and np.array_equal(z.f16_bits, res.f16_bits)
+    neg = orc.epilogue(res, (-C).astype(np.float16), relu=True)
+    assert np.array_equal(neg.C, np.zeros_like(C))
+    r = orc.epilogue(res, relu=True)
+    assert np.array_equal(r.C[C > 0], C[C > 0]) and (r.C[C <= 0] == 0).all()
