@@ -30,6 +30,11 @@ STATUS_NAMES = {0: "QGEMM_OK", 1: "QGEMM_ERR_INVALID_ARG", 2: "QGEMM_ERR_UNSUPPO
 _lib = None
 
 
+class Epilogue(ctypes.Structure):
+    """qgemm_epilogue: C = relu?(A*B [+ C_old]), one fp16 rounding."""
+    _fields_ = [("accumulate", ctypes.c_int32), ("relu", ctypes.c_int32)]
+
+
 class QGemmError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         self.status = status
@@ -63,6 +68,10 @@ def load_library():
                                   ctypes.POINTER(P), ctypes.POINTER(I64)]),
         "qgemm_mxfp8": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
+        "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
+        "gemm_f16_ex": (S, [P, I64, P, I64, P, I64, I64, I64, I64, ctypes.POINTER(Epilogue), P]),
+        "qgemm_w4a16_ex": (S, [P, I64, I64, P, P, I64, ctypes.POINTER(Epilogue), P]),
+        "qgemm_w8_gemv_ex": (S, [P, I64, I64, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "gemm_f16": (S, [P, I64, P, I64, P, I64, I64, I64, I64, P]),
         "qgemm_w4a16": (S, [P, I64, I64, P, P, I64, P]),
         "qgemm_w8_gemv": (S, [P, I64, I64, P, P, I64, P]),
@@ -205,6 +214,38 @@ def qgemm_w4a16(A, W: QTensor, C, stream=None):
 def qgemm_w8_gemv(X, W: QTensor, Y, stream=None):
     _check(load_library().qgemm_w8_gemv(_ptr(X), _ld(X), X.shape[0], W.handle, _ptr(Y), _ld(Y),
                                         _stream(stream)), "qgemm_w8_gemv")
+    return Y
+
+
+def _epi(accumulate: bool, relu: bool):
+    return ctypes.byref(Epilogue(int(bool(accumulate)), int(bool(relu))))
+
+
+def qgemm_mxfp8_ex(A: QTensor, B: QTensor, C, accumulate=False, relu=False, stream=None):
+    """C = relu?(A B^T [+ C]) with the MXFP8 operands of qgemm_mxfp8."""
+    _check(load_library().qgemm_mxfp8_ex(A.handle, B.handle, _ptr(C), _ld(C),
+                                         _epi(accumulate, relu), _stream(stream)), "qgemm_mxfp8_ex")
+    return C
+
+
+def gemm_f16_ex(A, B, C, accumulate=False, relu=False, stream=None):
+    M, K = A.shape
+    N = B.shape[1]
+    _check(load_library().gemm_f16_ex(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), M, N, K,
+                                      _epi(accumulate, relu), _stream(stream)), "gemm_f16_ex")
+    return C
+
+
+def qgemm_w4a16_ex(A, W: QTensor, C, accumulate=False, relu=False, stream=None):
+    _check(load_library().qgemm_w4a16_ex(_ptr(A), _ld(A), A.shape[0], W.handle, _ptr(C), _ld(C),
+                                         _epi(accumulate, relu), _stream(stream)), "qgemm_w4a16_ex")
+    return C
+
+
+def qgemm_w8_gemv_ex(X, W: QTensor, Y, accumulate=False, relu=False, stream=None):
+    _check(load_library().qgemm_w8_gemv_ex(_ptr(X), _ld(X), X.shape[0], W.handle, _ptr(Y), _ld(Y),
+                                           _epi(accumulate, relu), _stream(stream)),
+           "qgemm_w8_gemv_ex")
     return Y
 
 

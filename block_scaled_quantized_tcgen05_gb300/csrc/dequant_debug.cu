@@ -58,6 +58,17 @@ __global__ void fill_zero_f16_kernel(__half *C, int64_t ldc, int64_t M, int64_t 
     }
 }
 
+// Epilogue of an empty reduction (K = 0) in accumulate mode: C = relu(C_old) in place.
+__global__ void relu_inplace_f16_kernel(__half *C, int64_t ldc, int64_t M, int64_t N) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        __half *p = C + r * ldc + c;
+        *p = __float2half_rn(fmaxf(__half2float(*p), 0.0f));
+    }
+}
+
 // Waits on an mbarrier that nothing ever completes; the bounded wait must give up, record
 // ERR_SELFTEST and let the kernel return normally.
 __global__ void selftest_wait_kernel(unsigned *err, uint64_t timeout_ns) {
@@ -95,6 +106,14 @@ cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
                                  const LaunchCtx &ctx) {
     if (M * N == 0) return cudaSuccess;
     fill_zero_f16_kernel<<<grid_for(M * N, ctx.num_sms), 256, 0, ctx.stream>>>(C, ldc, M, N);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_empty_sum_epilogue(__half *C, int64_t ldc, int64_t M, int64_t N,
+                                      const LaunchCtx &ctx) {
+    if (!(ctx.epi & EPI_ACCUMULATE)) return launch_fill_zero_f16(C, ldc, M, N, ctx);   // relu(0) = 0
+    if (!(ctx.epi & EPI_RELU) || M * N == 0) return cudaSuccess;                        // C unchanged
+    relu_inplace_f16_kernel<<<grid_for(M * N, ctx.num_sms), 256, 0, ctx.stream>>>(C, ldc, M, N);
     return cudaGetLastError();
 }
 

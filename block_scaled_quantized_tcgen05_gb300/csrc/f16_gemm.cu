@@ -49,8 +49,8 @@ __host__ __device__ constexpr uint32_t f16_idesc(int n) {
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, unsigned *err,
-                uint64_t timeout_ns) {
+                __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, int epi,
+                unsigned *err, uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -192,7 +192,7 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             tc_fence_after();
             epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048);
+                              tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048, epi);
             ++acc_it;
         }
     }
@@ -221,8 +221,8 @@ cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
-    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, c_vec, M, N, K, ctx.err,
-                                                        ctx.timeout_ns);
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, c_vec, M, N, K, ctx.epi,
+                                                        ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 
@@ -257,7 +257,7 @@ constexpr uint32_t P_IDESC = (1u << 4) | (1u << 16) | (static_cast<uint32_t>(P_B
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
-                     unsigned *err, uint64_t timeout_ns) {
+                     int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -399,7 +399,7 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             epilogue_tile<P_BN, 2>(tmem_base + ab * P_BN, q, lane, C, ldc,
                                  mb * 2 * P_BM + static_cast<int>(rank) * P_BM, nb * P_BN, M, N,
                                  c_vec != 0, map_to_cta(tmem_empty(ab), 0),
-                                 sb + P_OFF_EPI + (warp - 2) * 2048);
+                                 sb + P_OFF_EPI + (warp - 2) * 2048, epi);
             ++acc_it;
         }
     }
@@ -432,7 +432,7 @@ static cudaError_t launch_gemm_f16_pair(const __half *A, int64_t lda, const __ha
     if (pairs > tiles) pairs = tiles;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     gemm_f16_pair_kernel<<<2 * pairs, P_THREADS, P_SMEM_BYTES, ctx.stream>>>(
-        tmA, tmB, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+        tmA, tmB, C, ldc, c_vec, M, N, K, ctx.epi, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -112,7 +112,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                   const uint8_t *__restrict__ sfa, int64_t lds_a, const uint8_t *__restrict__ sfb,
                   int64_t lds_b, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
-                  unsigned *err, uint64_t timeout_ns) {
+                  int epi, unsigned *err, uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -398,7 +398,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_fence_after();
             epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
                               tmem_empty(ab),
-                              sb + G::OFF_EPI + (warp - 2) * 2048);
+                              sb + G::OFF_EPI + (warp - 2) * 2048, epi);
             ++acc_it;
         }
     }
@@ -437,7 +437,7 @@ cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, i
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, tmSA, tmSB, A->scales, A->lds,
                                                         B->scales, B->lds, C, ldc, c_vec, M, N, K,
-                                                        ctx.err, ctx.timeout_ns);
+                                                        ctx.epi, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 

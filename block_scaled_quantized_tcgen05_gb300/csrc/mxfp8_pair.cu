@@ -139,7 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const uint8_t *__restrict__ packA, const uint8_t *__restrict__ packB,
                   int rbpA, int rbpB, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N,
-                  int K, unsigned *err, uint64_t timeout_ns) {
+                  int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -319,11 +319,17 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            epilogue_tile_early<BN / 2>(tmem_base + half * (BN / 2), q, lane, C, ldc,
-                                        mb * 2 * BM + static_cast<int>(rank) * BM,
-                                        nb * BN + static_cast<int>(half) * (BN / 2), M, N,
-                                        c_vec != 0, lead_empty,
-                                        sb + OFF_EPI + (warp - 2) * 2048);
+            const int em0 = mb * 2 * BM + static_cast<int>(rank) * BM;
+            const int en0 = nb * BN + static_cast<int>(half) * (BN / 2);
+            if (epi & EPI_ACC_BIT)   // reads the old C: chunk by chunk
+                epilogue_tile<BN / 2, 3>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0, en0, M,
+                                         N, c_vec != 0, lead_empty,
+                                         sb + OFF_EPI + (warp - 2) * 2048, epi);
+            else
+                epilogue_tile_early<BN / 2>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0, en0,
+                                            M, N, c_vec != 0, lead_empty,
+                                            sb + OFF_EPI + (warp - 2) * 2048,
+                                            (epi & EPI_RELU_BIT) != 0);
             acc_phase ^= 1;
         }
     }
@@ -382,7 +388,8 @@ cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __ha
     if (pairs > tiles) pairs = tiles;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     mxfp8_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+        tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, K, ctx.epi, ctx.err,
+        ctx.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -273,8 +273,8 @@ static qgemm_status check_out_f16(const void *C, int64_t ldc, int64_t M, int64_t
     return QGEMM_OK;
 }
 
-qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
-                         void *stream) {
+static qgemm_status mxfp8_impl(const qgemm_tensor *A, const qgemm_tensor *B, void *C,
+                               int64_t ldc, int epi, void *stream) {
     if (!A || !B) return fail(QGEMM_ERR_INVALID_ARG, "A or B is NULL");
     if (A->dtype != QGEMM_E4M3 || B->dtype != QGEMM_E4M3)
         return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "qgemm_mxfp8 takes E4M3 views");
@@ -292,10 +292,11 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
     qgi::LaunchCtx ctx;
     st = get_ctx(stream, &ctx);
     if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
     cudaError_t e;
     if (K == 0) {
-        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C), ldc, M, N, ctx);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(C), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
     }
     bool enc = true;
     e = qgi::launch_mxfp8(A, B, static_cast<__half *>(C), ldc, ctx, &enc);
@@ -303,8 +304,9 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_mxfp8 launch");
 }
 
-qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
-                      int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream) {
+static qgemm_status gemm_f16_impl(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                                  int64_t ldc, int64_t M, int64_t N, int64_t K, int epi,
+                                  void *stream) {
     if (M < 0 || N < 0 || K < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative shape");
     if (M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
         return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
@@ -320,10 +322,11 @@ qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, vo
     qgi::LaunchCtx ctx;
     st = get_ctx(stream, &ctx);
     if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
     cudaError_t e;
     if (K == 0) {
-        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C), ldc, M, N, ctx);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(C), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
     }
     bool enc = true;
     e = qgi::launch_gemm_f16(static_cast<const __half *>(A), lda, static_cast<const __half *>(B),
@@ -332,8 +335,8 @@ qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, vo
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "gemm_f16 launch");
 }
 
-qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
-                         void *C_f16, int64_t ldc, void *stream) {
+static qgemm_status w4a16_impl(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                               void *C_f16, int64_t ldc, int epi, void *stream) {
     if (!W) return fail(QGEMM_ERR_INVALID_ARG, "W is NULL");
     if (W->dtype != QGEMM_INT4) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "W must be an INT4 view");
     if (M < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative M");
@@ -354,10 +357,11 @@ qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_
     qgi::LaunchCtx ctx;
     st = get_ctx(stream, &ctx);
     if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
     cudaError_t e;
     if (K == 0) {
-        e = qgi::launch_fill_zero_f16(static_cast<__half *>(C_f16), ldc, M, N, ctx);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(C_f16), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
     }
     bool enc = true;
     e = qgi::launch_w4a16(static_cast<const __half *>(A_f16), lda, (int)M, W,
@@ -366,8 +370,8 @@ qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16 launch");
 }
 
-qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
-                           void *Y_f16, int64_t ldy, void *stream) {
+static qgemm_status w8_gemv_impl(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                                 void *Y_f16, int64_t ldy, int epi, void *stream) {
     if (!W) return fail(QGEMM_ERR_INVALID_ARG, "W is NULL");
     if (W->dtype != QGEMM_INT8) return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "W must be an INT8 view");
     if (M < 1 || M > 16) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "M must be in 1..16 (got %lld)",
@@ -389,16 +393,79 @@ qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgem
     qgi::LaunchCtx ctx;
     qgemm_status st = get_ctx(stream, &ctx);
     if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
     cudaError_t e;
     if (K == 0) {
-        e = qgi::launch_fill_zero_f16(static_cast<__half *>(Y_f16), ldy, M, N, ctx);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "zero fill");
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(Y_f16), ldy, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
     }
     bool enc = true;
     e = qgi::launch_w8_gemv(static_cast<const __half *>(X_f16), ldx, (int)M, W,
                             static_cast<__half *>(Y_f16), ldy, ctx, &enc);
     if (!enc) return QGEMM_ERR_CUDA;
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w8_gemv launch");
+}
+
+// Epilogue descriptor -> EPI_* flags (NULL: plain store).
+static qgemm_status epi_flags(const qgemm_epilogue *ep, int *flags) {
+    *flags = 0;
+    if (!ep) return QGEMM_OK;
+    if ((ep->accumulate != 0 && ep->accumulate != 1) || (ep->relu != 0 && ep->relu != 1))
+        return fail(QGEMM_ERR_INVALID_ARG, "epilogue fields must be 0 or 1 (accumulate %d, relu %d)",
+                    ep->accumulate, ep->relu);
+    *flags = (ep->accumulate ? qgi::EPI_ACCUMULATE : 0) | (ep->relu ? qgi::EPI_RELU : 0);
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                         void *stream) {
+    return mxfp8_impl(A, B, C, ldc, 0, stream);
+}
+
+qgemm_status qgemm_mxfp8_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                            const qgemm_epilogue *epilogue, void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st : mxfp8_impl(A, B, C, ldc, f, stream);
+}
+
+qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                      int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream) {
+    return gemm_f16_impl(A, lda, B, ldb, C, ldc, M, N, K, 0, stream);
+}
+
+qgemm_status gemm_f16_ex(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                         int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         const qgemm_epilogue *epilogue, void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st : gemm_f16_impl(A, lda, B, ldb, C, ldc, M, N, K, f, stream);
+}
+
+qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                         void *C_f16, int64_t ldc, void *stream) {
+    return w4a16_impl(A_f16, lda, M, W, C_f16, ldc, 0, stream);
+}
+
+qgemm_status qgemm_w4a16_ex(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                            void *C_f16, int64_t ldc, const qgemm_epilogue *epilogue,
+                            void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st : w4a16_impl(A_f16, lda, M, W, C_f16, ldc, f, stream);
+}
+
+qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                           void *Y_f16, int64_t ldy, void *stream) {
+    return w8_gemv_impl(X_f16, ldx, M, W, Y_f16, ldy, 0, stream);
+}
+
+qgemm_status qgemm_w8_gemv_ex(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                              void *Y_f16, int64_t ldy, const qgemm_epilogue *epilogue,
+                              void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st : w8_gemv_impl(X_f16, ldx, M, W, Y_f16, ldy, f, stream);
 }
 
 qgemm_status qgemm_dequant_debug(const qgemm_tensor *t, float *out, void *stream) {

@@ -52,6 +52,43 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
     }
 }
 
+// Epilogue flags, as EPI_* on the host: bit 0 adds the existing output, bit 1 applies ReLU.
+constexpr int EPI_ACC_BIT = 1;
+constexpr int EPI_RELU_BIT = 2;
+
+// The fused epilogue on 32 fp32 accumulators of one output row (columns col0 .. col0 + 31 of
+// crow): x = acc (+ fp32(C_old) when accumulating, C_old read before it is overwritten), then
+// max(x, +0) for ReLU.  Columns >= N are not read.
+__device__ __forceinline__ void epilogue_math32(uint32_t (&v)[32], const __half *crow, int col0,
+                                                int N, bool vec, int epi) {
+    if (epi & EPI_ACC_BIT) {
+        if (vec && col0 + 32 <= N) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(crow + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 w = src[i];
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 h = *reinterpret_cast<const __half2 *>(&ww[j]);
+                    v[8 * i + 2 * j] = __float_as_uint(__uint_as_float(v[8 * i + 2 * j]) + __low2float(h));
+                    v[8 * i + 2 * j + 1] =
+                        __float_as_uint(__uint_as_float(v[8 * i + 2 * j + 1]) + __high2float(h));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col0 + i < N)
+                    v[i] = __float_as_uint(__uint_as_float(v[i]) + __half2float(crow[col0 + i]));
+        }
+    }
+    if (epi & EPI_RELU_BIT) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.0f));
+    }
+}
+
 // Drain one 128 x BN fp32 accumulator tile to fp16 global memory.  The warp reads its TMEM lane
 // quarter q (rows 32 q .. 32 q + 31 of the tile, one row per lane) 32 columns at a time.
 // Direct form: each lane stores its own row (16-byte stores).  Staged form (`stage` = 2 KB of
@@ -59,6 +96,7 @@ __device__ __forceinline__ void store_row_chunk32(__half *crow, int col0, int N,
 // chunks swizzled by row pair, conflict-free both ways) so that each store instruction writes
 // 8 rows x 64 contiguous bytes, i.e. whole 32-byte sectors.  The accumulator is released
 // (arrival on `tmem_empty`) after its last column has been read.
+// `epi` (EPI_ACC_BIT | EPI_RELU_BIT) fuses C = relu?(acc [+ C_old]) before the fp16 rounding.
 // RELEASE selects how the accumulator is released: 0 = every lane arrives on this CTA's barrier;
 // 2 = one lane per warp arrives on `tmem_empty` given as a shared::cluster address (a CTA pair
 // releases its accumulators on the MMA-issuing CTA's barrier) with cluster-scope release
@@ -69,7 +107,7 @@ template <int BN, int RELEASE = 0>
 __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, uint32_t lane,
                                               __half *C, int64_t ldc, int m0, int n0, int M,
                                               int N, bool vec, uint32_t tmem_empty,
-                                              uint32_t stage) {
+                                              uint32_t stage, int epi = 0) {
     const int row = m0 + static_cast<int>(q * 32 + lane);
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -89,6 +127,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
             }
         }
         const int col0 = n0 + ch * 32;
+        if (epi != 0 && row < M) epilogue_math32(v, C + static_cast<int64_t>(row) * ldc, col0, N, vec, epi);
         if (stage == 0u || !vec) {
             if (row < M) store_row_chunk32(C + static_cast<int64_t>(row) * ldc, col0, N, vec, v);
             continue;
@@ -235,12 +274,13 @@ __device__ __forceinline__ void store_row_packed16(__half *crow, int col0, int N
 // and packed to fp16 in registers (BN / 32 x 16 of them) before anything is stored, and the accumulator is released
 // right after the reads: the next tile's MMAs wait for the TMEM reads only, while the stores run
 // under them.  Release as RELEASE = 3 of epilogue_tile (one relaxed arrival per warp on
-// `tmem_empty`, a shared::cluster address).
+// `tmem_empty`, a shared::cluster address).  `relu` applies max(x, +0) before the rounding; the
+// accumulate epilogue (which reads the old C) takes epilogue_tile.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile_early(uint32_t tmem_base, uint32_t q, uint32_t lane,
                                                     __half *C, int64_t ldc, int m0, int n0, int M,
                                                     int N, bool vec, uint32_t tmem_empty,
-                                                    uint32_t stage) {
+                                                    uint32_t stage, bool relu = false) {
     constexpr int NCH = BN / 32;
     uint32_t p[NCH][16];
 #pragma unroll
@@ -248,6 +288,10 @@ __device__ __forceinline__ void epilogue_tile_early(uint32_t tmem_base, uint32_t
         uint32_t v[16];
         tmem_ld_32x32b_x16(tmem_base + ((q * 32) << 16) + h * 16, v);
         tmem_wait_ld();
+        if (relu) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.0f));
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             p[h >> 1][(h & 1) * 8 + i] = pack_f16x2(__uint_as_float(v[2 * i]),

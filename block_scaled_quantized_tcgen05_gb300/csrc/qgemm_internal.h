@@ -22,12 +22,17 @@ struct qgemm_tensor {
 
 namespace qgi {
 
+// Epilogue flags (LaunchCtx::epi): C = relu?( acc [+ C_old] ), one fp16 rounding at the end.
+constexpr int EPI_ACCUMULATE = 1;   // add the existing C (fp16) to the fp32 accumulator
+constexpr int EPI_RELU = 2;         // max(x, +0) before rounding
+
 struct LaunchCtx {
     cudaStream_t stream;
     unsigned *err;        // device error word
     uint64_t timeout_ns;  // bound on every device-side wait
     int num_sms;
     int device;
+    int epi = 0;          // EPI_* flags of the output epilogue
 };
 
 // Records a formatted message for qgemm_last_error_message() and returns `s`.
@@ -70,6 +75,9 @@ cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tens
 cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);
 cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
                                  const LaunchCtx &ctx);
+// K = 0: C = relu?(0 [+ C_old]) under ctx.epi.
+cudaError_t launch_empty_sum_epilogue(__half *C, int64_t ldc, int64_t M, int64_t N,
+                                      const LaunchCtx &ctx);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, const LaunchCtx &ctx);
 
 }  // namespace qgi

@@ -71,7 +71,8 @@ template <bool SF_VEC>
 __global__ void __launch_bounds__(THREADS, 1)
 w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__restrict__ W,
                   int64_t ldw, const uint8_t *__restrict__ SW, int64_t ldsw,
-                  __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, unsigned *err,
+                  __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, int epi,
+                  unsigned *err,
                   uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
@@ -203,7 +204,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             }
             tc_fence_after();
             epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), 0u);
+                              tmem_empty(ab), 0u, epi);
             ++acc_it;
         }
     } else {
@@ -332,7 +333,7 @@ static_assert(T_SMEM_BYTES <= 232448, "shared memory budget");
 __global__ void __launch_bounds__(T_THREADS, 1)
 w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmS, __half *__restrict__ C, int64_t ldc,
-                 int c_vec, int M, int N, int K, unsigned *err, uint64_t timeout_ns) {
+                 int c_vec, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -478,7 +479,7 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             tc_fence_after();
             epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), sb + T_OFF_EPI + (warp - 2) * 2048);
+                              tmem_empty(ab), sb + T_OFF_EPI + (warp - 2) * 2048, epi);
             ++acc_it;
         }
     } else {
@@ -589,7 +590,7 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
                                              T_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         w4a16_tma_kernel<<<grid, T_THREADS, T_SMEM_BYTES, ctx.stream>>>(
-            tmA, tmW, tmS, C, ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+            tmA, tmW, tmS, C, ldc, c_vec, M, N, K, ctx.epi, ctx.err, ctx.timeout_ns);
         return cudaGetLastError();
     }
     const bool sf_vec = reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0;
@@ -598,7 +599,8 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(tmA, W->data, W->ld, W->scales, W->lds, C,
-                                                    ldc, c_vec, M, N, K, ctx.err, ctx.timeout_ns);
+                                                    ldc, c_vec, M, N, K, ctx.epi, ctx.err,
+                                                    ctx.timeout_ns);
     return cudaGetLastError();
 }
 

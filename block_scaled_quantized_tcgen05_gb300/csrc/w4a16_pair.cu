@@ -86,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ CUtensorMap tmC, int c_tma,
                   const uint8_t *__restrict__ scales, int64_t lds, __half *__restrict__ C,
-                  int64_t ldc, int M, int N, int K, unsigned *err, uint64_t timeout_ns) {
+                  int64_t ldc, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -343,6 +343,11 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive_relaxed_cluster(lead_empty);
                 }
+                if ((epi & EPI_RELU_BIT) && !(epi & EPI_ACC_BIT)) {   // (after the add otherwise)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[c] = __float_as_uint(fmaxf(__uint_as_float(v[c]), 0.0f));
+                }
                 if (c_tma) {
                     // row c of the chunk: tokens m0 + 32 ch + c, columns n0 .. n0 + 31
 #pragma unroll
@@ -353,9 +358,15 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int m = m0 + ch * 32 + c;
-                        if (m < M)
-                            st_global_cs_u16(C + static_cast<int64_t>(m) * ldc + n,
-                                             __half_as_ushort(__float2half_rn(__uint_as_float(v[c]))));
+                        if (m < M) {
+                            __half *dst = C + static_cast<int64_t>(m) * ldc + n;
+                            float x = __uint_as_float(v[c]);
+                            if (epi & EPI_ACC_BIT) {   // C = relu?(acc + C_old), one rounding
+                                x += __half2float(*dst);
+                                if (epi & EPI_RELU_BIT) x = fmaxf(x, 0.0f);
+                            }
+                            st_global_cs_u16(dst, __half_as_ushort(__float2half_rn(x)));
+                        }
                     }
                 }
             }
@@ -401,7 +412,9 @@ cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_t
                                BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!*encode_ok) return cudaErrorInvalidValue;
     // output through TMA stores when C and its row stride allow a tensor map
-    const int c_tma = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    // (the accumulate epilogue reads the old C element by element: direct stores)
+    const int c_tma = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0 &&
+                       !(ctx.epi & EPI_ACCUMULATE)) ? 1 : 0;
     if (c_tma) {
         *encode_ok = encode_tma_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2, 32, 32,
                                    CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -416,7 +429,8 @@ cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_t
     int pairs = ctx.num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     w4a16_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.err, ctx.timeout_ns);
+        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.epi, ctx.err,
+        ctx.timeout_ns);
     return cudaGetLastError();
 }
 

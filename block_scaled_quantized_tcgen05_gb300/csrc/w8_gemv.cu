@@ -20,6 +20,7 @@
 // every UE8M0 scale is handled exactly.  CTAs are persistent over 64-row blocks.
 #include <cuda_fp16.h>
 
+#include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -148,7 +149,7 @@ template <int NH>
 __global__ void __launch_bounds__(THREADS)
 w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                int M, const uint8_t *__restrict__ SW, int64_t ldsw, int sw_vec,
-               __half *__restrict__ Y, int64_t ldy, int N, int K, unsigned *err,
+               __half *__restrict__ Y, int64_t ldy, int N, int K, int epi, unsigned *err,
                uint64_t timeout_ns) {
     using G = GCfg<NH>;
     extern __shared__ uint8_t smem_raw[];
@@ -272,7 +273,13 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             for (int i = 0; i < 4; ++i) {
                 const int m = 8 * h + 2 * t + (i & 1);
                 const int n = n0 + ((i & 2) ? 8 : 0);
-                if (m < M && n < N) Y[static_cast<int64_t>(m) * ldy + n] = __float2half_rn(acc[h][i]);
+                if (m < M && n < N) {
+                    __half *dst = Y + static_cast<int64_t>(m) * ldy + n;
+                    float x = acc[h][i];
+                    if (epi & EPI_ACC_BIT) x += __half2float(*dst);   // Y = relu?(X W^T + Y_old)
+                    if (epi & EPI_RELU_BIT) x = fmaxf(x, 0.0f);
+                    *dst = __float2half_rn(x);
+                }
             }
         }
     }
@@ -300,7 +307,7 @@ cudaError_t launch_nh(const __half *X, int64_t ldx, int M, const qgemm_tensor *W
     if (grid > nrb) grid = nrb;
     const int sw_vec = (reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0) ? 1 : 0;
     kern<<<grid, THREADS, G::SMEM, ctx.stream>>>(tmW, tmX, M, W->scales, W->lds, sw_vec, Y, ldy, N,
-                                                 K, ctx.err, ctx.timeout_ns);
+                                                 K, ctx.epi, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -180,6 +180,34 @@ qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_
 qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
                            void *Y_f16, int64_t ldy, void *stream);
 
+/* ---------------------------------------------------------------- fused output epilogue
+ * C = relu?( A*B [+ C_old] ): the product's fp32 accumulator plus, when `accumulate` is set,
+ * the existing fp16 output (read before it is overwritten), then, when `relu` is set,
+ * max(x, +0); one fp16 round-to-nearest-even at the end.
+ * Passages: "TensorOps: quantized matmul ...", section "The real matmul2d API" (the op's mode is
+ * multiply or multiply_accumulate, the latter computing C = A*B + C); "Running inline ML
+ * operations in a shader with Metal 4", section "Combine an element-wise function" (a ReLU
+ * postfix applied to the product's elements before they are stored, in the same dispatch).
+ * Each _ex call takes the arguments of the call it extends plus `epilogue` (NULL = plain store);
+ * its fields must be 0 or 1 (QGEMM_ERR_INVALID_ARG otherwise).  With accumulate set the output
+ * must hold valid fp16 data; K == 0 then leaves relu?(C_old).  Errors as the plain calls. */
+typedef struct qgemm_epilogue {
+    int32_t accumulate;   /* 1: add the existing output (matmul2d multiply_accumulate) */
+    int32_t relu;         /* 1: max(x, +0) before the rounding */
+} qgemm_epilogue;
+
+qgemm_status qgemm_mxfp8_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                            const qgemm_epilogue *epilogue, void *stream);
+qgemm_status gemm_f16_ex(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                         int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         const qgemm_epilogue *epilogue, void *stream);
+qgemm_status qgemm_w4a16_ex(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
+                            void *C_f16, int64_t ldc, const qgemm_epilogue *epilogue,
+                            void *stream);
+qgemm_status qgemm_w8_gemv_ex(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
+                              void *Y_f16, int64_t ldy, const qgemm_epilogue *epilogue,
+                              void *stream);
+
 /* Dequantise-only debug kernel: out[r, k] = decode(t.data[r, k]) * 2^(t.scales[r, k/32] - 127)
  * as fp32 (fp16 views: the value itself), written densely as [rows, k] row-major.  Exists so
  * that the decoded operand values can be compared bit for bit with the CPU reference, as the

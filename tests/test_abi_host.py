@@ -127,3 +127,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         q.load_library()
+
+
+def test_epilogue_descriptor_validation(lib):
+    """The _ex calls check their epilogue descriptor (fields 0 or 1) and then every argument
+    the plain call checks, all before any device work."""
+    _, a = _create(lib, q.E4M3, 128, 256, FAKE, 256, FAKE + 65536, 8)
+    _, b = _create(lib, q.E4M3, 256, 256, FAKE, 256, FAKE + 65536, 8)
+    _, b2 = _create(lib, q.E4M3, 256, 128, FAKE, 128, FAKE + 65536, 4)
+    _, w4 = _create(lib, q.INT4, 256, 256, FAKE, 128, FAKE + 65536, 8)
+    _, e0 = _create(lib, q.E4M3, 0, 256, FAKE, 256, FAKE + 65536, 8)
+    C = ctypes.c_void_p(FAKE + (1 << 24))
+    ok = ctypes.byref(q.Epilogue(1, 1))
+    assert lib.qgemm_mxfp8_ex(a, b, C, 256, ctypes.byref(q.Epilogue(2, 0)), None) == 1
+    assert lib.gemm_f16_ex(C, 256, C, 256, C, 256, 16, 256, 256,
+                           ctypes.byref(q.Epilogue(0, -1)), None) == 1
+    assert lib.qgemm_w4a16_ex(C, 256, 16, w4, C, 256, ctypes.byref(q.Epilogue(3, 1)), None) == 1
+    assert lib.qgemm_w8_gemv_ex(C, 256, 4, w4, C, 256, ok, None) == 4         # not INT8
+    assert lib.qgemm_mxfp8_ex(a, b2, C, 256, ok, None) == 1                     # K mismatch
+    assert lib.gemm_f16_ex(C, 20, C, 256, C, 256, 16, 256, 20, ok, None) == 3   # lda % 8
+    assert lib.qgemm_mxfp8_ex(e0, b, C, 256, ok, None) == 0                     # empty output
+    for t in (a, b, b2, w4, e0):
+        lib.qgemm_destroy_tensor(t)
