@@ -11,6 +11,7 @@ Workloads (all operands row-major, K contiguous, one UE8M0 scale per 32 elements
 * ``mxfp8_8192``    -- MXFP8 M=N=K=8192; each row of A and of B gets variance 10^U(-2,2).
 * ``w4a16_prefill`` -- fp16 A [4096,4096] N(0,1); int4 W [14336,4096] from N(0, 0.02^2).
 * ``w8_decode``     -- fp16 X [M,8192] N(0,1), M in {1,8,16}; int8 W [28672,8192] from N(0, 0.02^2).
+* ``mxfp4_8192``    -- MXFP4 M=N=K=8192; each row of A and of B gets variance 10^U(-2,2).
 
 Encoding recipes (the pages only say "power-of-two block scales, 32 elements per block"; the
 per-format details below are the workload definitions):
@@ -21,6 +22,10 @@ per-format details below are the workload definitions):
 * intN (N = 4 or 8, qmax = 7 or 127): scale s = 2^ceil(log2(amax / qmax)), byte log2(s) + 127,
   q = round-half-even(w / s) clamped to [-qmax-1, qmax].  int4 is packed two per byte, the even
   k in the low nibble ("TensorOps: quantized matmul ...", section "VALIDATED ON M4 MAX", fact 5).
+
+* MXFP4: per block X = floor(log2(amax)) - 2 (E2M1's largest exponent is 2), scale byte X + 127,
+  element = the nearest E2M1 value to v / 2^X (ties to the even code, i.e. mantissa bit 0),
+  saturated to +-6; two per byte, even k in the low nibble (the int4 rule).
 
 The E4M3 rounding is done by PyTorch's float8_e4m3fn cast (round-to-nearest-even) after the
 saturating clamp; exponents come from ``torch.frexp`` so no ``log2`` rounding is involved.
@@ -71,6 +76,39 @@ def quantize_mxfp8(x: torch.Tensor):
     return q.contiguous(), scale_bytes.contiguous()
 
 
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7; 8..15 negative
+
+
+def e2m1_round(y: torch.Tensor) -> torch.Tensor:
+    """Codes 0..7 of the nearest E2M1 magnitude to |y| (fp64 y), ties to the even code, values
+    above 6 saturated.  The spacing is 0.5 below 2, 1 in [2, 4) and 2 in [4, 6]; within each range
+    an even multiple of the spacing is an even code, so half-to-even rounding of y / spacing is
+    the tie rule."""
+    y = y.abs().clamp(max=6.0)
+    lo = torch.round(y / 0.5) * 0.5
+    mid = torch.round(y)
+    hi = torch.round(y / 2.0) * 2.0
+    v = torch.where(y < 2.0, lo, torch.where(y < 4.0, mid, hi))
+    grid = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float64)
+    return torch.searchsorted(grid, v.contiguous()).to(torch.uint8)
+
+
+def quantize_mxfp4(x: torch.Tensor):
+    """fp32 [rows, K] -> (packed E2M1 bytes uint8 [rows, K/2], UE8M0 bytes uint8 [rows, K/32])."""
+    x = x.to(torch.float64)
+    rows, k = x.shape
+    amax = _block_amax(x)
+    _, e = torch.frexp(amax)                       # amax = f * 2^e, f in [0.5, 1)
+    X = (e - 1 - 2).to(torch.int32)                # floor(log2(amax)) - 2
+    X = torch.where(amax > 0, X, torch.zeros_like(X)).clamp(-127, 127)
+    scale_bytes = (X + 127).to(torch.uint8)
+    xs = x.reshape(rows, k // BLOCK, BLOCK)
+    scaled = torch.ldexp(xs, (-X).to(torch.float64).unsqueeze(2)).reshape(rows, k)
+    code = e2m1_round(scaled) | (torch.signbit(scaled).to(torch.uint8) << 3)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).to(torch.uint8)
+    return packed.contiguous(), scale_bytes.contiguous()
+
+
 def quantize_int_blocks(w: torch.Tensor, qmax: int):
     """fp32 [rows, K] -> (int8 values [rows, K] in [-qmax-1, qmax], UE8M0 bytes [rows, K/32])."""
     w = w.to(torch.float64)
@@ -103,7 +141,7 @@ def log_uniform_row_std(rows: int, g: torch.Generator, lo_exp=-2.0, hi_exp=2.0) 
 
 
 # ------------------------------------------------------------------------------ workloads
-WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode")
+WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode", "mxfp4_8192")
 
 
 def mxfp8_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
@@ -119,6 +157,22 @@ def mxfp8_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
         b = normal((N, K), g)
     qa, sa_b = quantize_mxfp8(a)
     qb, sb_b = quantize_mxfp8(b)
+    return {"a": qa, "sa": sa_b, "b": qb, "sb": sb_b, "M": M, "N": N, "K": K}
+
+
+def mxfp4_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
+    """MXFP4 operands: A [M,K/2], B [N,K/2] (packed E2M1 bytes) with UE8M0 scales [rows, K/32]."""
+    g = generator(seed)
+    if row_variance:
+        sa = log_uniform_row_std(M, g)
+        sb = log_uniform_row_std(N, g)
+        a = normal((M, K), g) * sa[:, None]
+        b = normal((N, K), g) * sb[:, None]
+    else:
+        a = normal((M, K), g)
+        b = normal((N, K), g)
+    qa, sa_b = quantize_mxfp4(a)
+    qb, sb_b = quantize_mxfp4(b)
     return {"a": qa, "sa": sa_b, "b": qb, "sb": sb_b, "M": M, "N": N, "K": K}
 
 
@@ -161,4 +215,6 @@ def workload(name: str, M: int | None = None):
         return w4a16_inputs(4096, 14336, 4096, seed)
     if name == "w8_decode":
         return w8_inputs(16 if M is None else M, 28672, 8192, seed)
+    if name == "mxfp4_8192":
+        return mxfp4_inputs(8192, 8192, 8192, seed, row_variance=True)
     raise KeyError(name)

@@ -36,7 +36,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 # dtype codes of qgemm_oracle.c
-F16, E4M3, INT8, INT4 = 0, 1, 2, 3
+F16, E4M3, INT8, INT4, E2M1 = 0, 1, 2, 3, 4
 
 _lib = None
 _lock = threading.Lock()
@@ -87,6 +87,10 @@ def _load():
         lib.orc_dot_quant.argtypes = [I64, I64, I64, P, I, P, I64, P, I64, P, P]
         lib.orc_f16_rn_array.restype = None
         lib.orc_f16_rn_array.argtypes = [I64, P, P]
+        lib.orc_e2m1.restype = ctypes.c_double
+        lib.orc_e2m1.argtypes = [ctypes.c_uint8]
+        lib.orc_e2m1_table.restype = None
+        lib.orc_e2m1_table.argtypes = [P]
         lib.orc_e4m3_table.restype = None
         lib.orc_e4m3_table.argtypes = [P]
         lib.orc_ue8m0_table.restype = None
@@ -110,6 +114,13 @@ def _u8(a) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- decoders
+def e2m1_table() -> np.ndarray:
+    """Values of the 16 E2M1 codes (low nibble), fp64."""
+    out = np.empty(16, np.float64)
+    _load().orc_e2m1_table(_ptr(out))
+    return out
+
+
 def e4m3_table() -> np.ndarray:
     out = np.empty(256, np.float64)
     _load().orc_e4m3_table(_ptr(out))
@@ -150,7 +161,8 @@ def dequant(dtype: int, data, scales, rows: np.ndarray | None = None, k: int | N
         raise ValueError("data must be 2-D")
     R = d.shape[0]
     if k is None:
-        k = {F16: d.shape[1] // 2, E4M3: d.shape[1], INT8: d.shape[1], INT4: d.shape[1] * 2}[dtype]
+        k = {F16: d.shape[1] // 2, E4M3: d.shape[1], INT8: d.shape[1], INT4: d.shape[1] * 2,
+             E2M1: d.shape[1] * 2}[dtype]
     s = _u8(scales) if scales is not None else np.zeros((R, 1), np.uint8)
     idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, np.int64))
     n = R if idx is None else idx.size
@@ -204,6 +216,18 @@ def mxfp8(a, sa, b, sb, rows=None) -> Result:
     K = _u8(a).shape[1]
     Ad = dequant(E4M3, a, sa, rows, K)
     Bd = dequant(E4M3, b, sb, None, K)
+    C, D = dot_rows(Ad, Bd)
+    return Result(C, D, rows)
+
+
+def mxfp4(a, sa, b, sb, k=None, rows=None) -> Result:
+    """C[m,n] = sum_k e2m1(A[m,k]) 2^(SA[m,k/32]-127) * e2m1(B[n,k]) 2^(SB[n,k/32]-127).
+
+    A is [M,K/2] and B [N,K/2] packed E2M1 bytes (even k in the low nibble), scales
+    [rows, K/32] UE8M0."""
+    K = k if k is not None else _u8(a).shape[1] * 2
+    Ad = dequant(E2M1, a, sa, rows, K)
+    Bd = dequant(E2M1, b, sb, None, K)
     C, D = dot_rows(Ad, Bd)
     return Result(C, D, rows)
 

@@ -18,7 +18,12 @@
  *     summary), section "Shader MXFP8 tensor types": the data plane type is FP8 E4M3.
  *   - "Running inline ML operations in a shader with Metal 4": the product is checked against
  *     a CPU reference implementation; matmul2d in multiply mode overwrites C with A*B.
+ *   - same summary, section on the quantized data types: OS 27 adds 4-bit and 8-bit floating-point
+ *     data planes ("fp4, fp8, int2 native" in the TensorOps page's table).
  * Readings where the pages are silent:
+ *   - fp4 is the OCP MX FP4 element E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit; no
+ *     infinity or NaN; largest magnitude 6), packed two per byte with the low nibble holding the
+ *     even index (the pages' int4 rule), with the same UE8M0 block-32 scale plane.
  *   - E4M3 is the OCP 8-bit E4M3 encoding (bias 7, no infinity, S.1111.111 is NaN).
  *   - UE8M0 byte e means 2^(e-127); e = 255 is NaN.
  *   - The exact product sum_k deq(A)[m,k]*deq(B)[n,k] is formed in fp64; the reported output is
@@ -32,7 +37,7 @@
 #include <string.h>
 
 /* dtype codes private to the oracle */
-enum { ORC_F16 = 0, ORC_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3 };
+enum { ORC_F16 = 0, ORC_E4M3 = 1, ORC_INT8 = 2, ORC_INT4 = 3, ORC_E2M1 = 4 };
 
 /* OCP FP8 E4M3: sign(1) exponent(4, bias 7) mantissa(3).  Exponent field 0 is subnormal
  * (m * 2^-9); exponent 15 with mantissa 7 is NaN; there is no infinity. */
@@ -44,6 +49,16 @@ double orc_e4m3(uint8_t b) {
     if (e == 15 && m == 7) return NAN;
     if (e == 0) v = ldexp((double)m, -9);
     else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* OCP FP4 E2M1 (low 4 bits of nib): sign(1) exponent(2, bias 1) mantissa(1).  Exponent field 0
+ * is subnormal (m * 2^-1); no infinity, no NaN. */
+double orc_e2m1(uint8_t nib) {
+    int s = (nib >> 3) & 1;
+    int e = (nib >> 1) & 3;
+    int m = nib & 1;
+    double v = (e == 0) ? ldexp((double)m, -1) : ldexp(1.0 + (double)m / 2.0, e - 1);
     return s ? -v : v;
 }
 
@@ -101,6 +116,12 @@ static int orc_int4_val(const uint8_t *row, int64_t k) {
 }
 
 int orc_int4_get(const uint8_t *row, int64_t k) { return orc_int4_val(row, k); }
+
+/* element k of a packed E2M1 row: byte k/2, low nibble for even k, high nibble for odd k */
+static double orc_e2m1_val(const uint8_t *row, int64_t k) {
+    int byte = row[k >> 1];
+    return orc_e2m1((uint8_t)((k & 1) ? (byte >> 4) & 15 : byte & 15));
+}
 int orc_int8_get(uint8_t b) { return orc_int8_val(b); }
 
 /* Decoded value of element (r, j) of a [rows, k] plane, scale included. */
@@ -116,6 +137,7 @@ static double orc_element(int dtype, const uint8_t *data, int64_t ld, const uint
     case ORC_E4M3: q = orc_e4m3(row[j]); break;
     case ORC_INT8: q = (double)orc_int8_val(row[j]); break;
     case ORC_INT4: q = (double)orc_int4_val(row, j); break;
+    case ORC_E2M1: q = orc_e2m1_val(row, j); break;
     default: return NAN;
     }
     s = orc_ue8m0(scales[r * lds + j / 32]);   /* block of 32 along k, one row per block row */
@@ -207,6 +229,11 @@ void orc_f16_rn_array(int64_t count, const double *x, uint16_t *bits) {
 void orc_e4m3_table(double *out) {
     int b;
     for (b = 0; b < 256; ++b) out[b] = orc_e4m3((uint8_t)b);
+}
+
+void orc_e2m1_table(double *out) {
+    int b;
+    for (b = 0; b < 16; ++b) out[b] = orc_e2m1((uint8_t)b);
 }
 
 void orc_ue8m0_table(double *out) {

@@ -280,3 +280,70 @@ def test_epilogue_invariants(orc):
     assert np.array_equal(neg.C, np.zeros_like(C))
     r = orc.epilogue(res, relu=True)
     assert np.array_equal(r.C[C > 0], C[C > 0]) and (r.C[C <= 0] == 0).all()
+
+
+# OCP MX FP4 E2M1 by its definition: magnitudes of the 8 codes 0..7 (exponent field 0 is
+# subnormal: 0, 0.5; then 1, 1.5, 2, 3, 4, 6), codes 8..15 the negatives.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_reference(code: int) -> float:
+    v = E2M1_MAGNITUDES[code & 7]
+    return -v if code & 8 else v
+
+
+def test_e2m1_all_codes_match_definition(orc):
+    t = orc.e2m1_table()
+    for c in range(16):
+        assert t[c] == _e2m1_reference(c) and np.signbit(t[c]) == bool(c & 8)
+
+
+def test_e2m1_packing_even_k_in_low_nibble(orc):
+    row = np.array([[0x71, 0xF8]], np.uint8)      # k0 = 0x1 (0.5), k1 = 0x7 (6), k2 = 0x8 (-0), k3 = 0xF (-6)
+    d = orc.dequant(orc.E2M1, row, np.full((1, 1), 127, np.uint8), k=4)
+    assert d.tolist() == [[0.5, 6.0, -0.0, -6.0]]
+    d2 = orc.dequant(orc.E2M1, row, np.full((1, 1), 129, np.uint8), k=4)   # scale 2^2
+    assert d2.tolist() == [[2.0, 24.0, -0.0, -24.0]]
+
+
+def test_mxfp4_brute_force_exact_rationals(orc):
+    rng = np.random.default_rng(7)
+    for (M, N, K) in [(1, 1, 32), (3, 2, 64), (2, 4, 96)]:
+        a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+        b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+        sa = rng.integers(115, 140, (M, K // 32), dtype=np.uint8)
+        sb = rng.integers(115, 140, (N, K // 32), dtype=np.uint8)
+        res = orc.mxfp4(a, sa, b, sb)
+
+        def val(plane, scales, r, k):
+            byte = int(plane[r, k // 2])
+            code = byte & 15 if k % 2 == 0 else byte >> 4
+            return Fraction(_e2m1_reference(code)) * Fraction(2) ** (int(scales[r, k // 32]) - 127)
+
+        for m in range(M):
+            for n in range(N):
+                exact = sum(val(a, sa, m, k) * val(b, sb, n, k) for k in range(K))
+                mag = sum(abs(val(a, sa, m, k) * val(b, sb, n, k)) for k in range(K))
+                assert abs(Fraction(res.C[m, n]) - exact) <= Fraction(2.0 ** -50) * mag
+                assert Fraction(res.D[m, n]) == pytest.approx(float(mag), rel=1e-14)
+
+
+def test_mxfp4_matches_library_matmul(orc):
+    """Decode with the literal table, multiply with numpy: the same product as the oracle."""
+    rng = np.random.default_rng(8)
+    M, N, K = 5, 7, 128
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(120, 135, (N, K // 32), dtype=np.uint8)
+    tab = np.array([_e2m1_reference(c) for c in range(16)])
+
+    def decode(p, s):
+        codes = np.stack([p & 15, p >> 4], axis=-1).reshape(p.shape[0], -1)
+        return tab[codes] * np.exp2(np.repeat(s.astype(np.float64) - 127, 32, axis=1))
+
+    want = decode(a, sa) @ decode(b, sb).T
+    res = orc.mxfp4(a, sa, b, sb)
+    assert np.allclose(res.C, want, rtol=1e-12, atol=1e-12)
+    sel = orc.mxfp4(a, sa, b, sb, rows=np.array([4, 1]))
+    assert np.array_equal(sel.C, res.C[[4, 1]])

@@ -92,3 +92,59 @@ def test_workload_shapes_small():
     assert d["sa"].shape == (128, 4) and d["sb"].shape == (256, 4)
     d2 = synth.workload("mxfp8_small")
     assert torch.equal(d["a"], d2["a"]) and torch.equal(d["sb"], d2["sb"])   # seeded
+
+
+def _nearest_e2m1_code(y: float, table: np.ndarray) -> int:
+    """Nearest E2M1 value to y over all 16 codes, saturating at +-6; ties go to the code whose
+    mantissa bit (bit 0) is clear; the sign follows y."""
+    y = max(-6.0, min(6.0, y))
+    best = None
+    for code in range(16):
+        if (code >> 3) != (1 if math.copysign(1.0, y) < 0 else 0):
+            continue
+        key = (abs(float(table[code]) - y), code & 1)
+        if best is None or key < best[0]:
+            best = (key, code)
+    return best[1]
+
+
+def test_mxfp4_quantizer_matches_plain_restatement(orc):
+    table = orc.e2m1_table()
+    g = synth.generator(321)
+    x = synth.normal((5, 64), g) * torch.tensor([[1e-3], [1.0], [50.0], [1e-30], [0.0]])
+    x[1, 3] = -x[1, :32].abs().max() * 1.0001                     # negative amax
+    x[2, 40:44] = torch.tensor([0.25, 0.75, 2.5, 5.0]) * 2.0 ** math.floor(
+        math.log2(float(x[2, 32:].abs().max())) - 2)             # exact ties on the grid
+    p, s = synth.quantize_mxfp4(x)
+    assert p.shape == (5, 32) and s.shape == (5, 2)
+    for r in range(x.shape[0]):
+        for b in range(2):
+            blk = x[r, 32 * b:32 * b + 32].double().numpy()
+            amax = float(np.abs(blk).max())
+            X = 0
+            if amax > 0:
+                X = math.floor(math.log2(amax)) - 2
+                while 2.0 ** (X + 2) > amax:
+                    X -= 1
+                while 2.0 ** (X + 3) <= amax:
+                    X += 1
+                X = max(-127, min(127, X))
+            assert int(s[r, b]) == X + 127
+            for j in range(32):
+                k = 32 * b + j
+                byte = int(p[r, k // 2])
+                got = (byte >> 4) if k % 2 else (byte & 15)
+                want = _nearest_e2m1_code(blk[j] / 2.0 ** X, table)
+                assert table[got] == table[want], (r, b, j, blk[j], got, want)
+
+
+def test_mxfp4_quantizer_properties(orc):
+    table = orc.e2m1_table()
+    d = synth.mxfp4_inputs(64, 32, 256, seed=8, row_variance=True)
+    p = d["a"].numpy()
+    codes = np.stack([p & 15, p >> 4], axis=2).reshape(64, 256)
+    vals = table[codes]
+    blk_max = np.abs(vals).reshape(64, 8, 32).max(axis=2)
+    assert np.all((blk_max >= 4) & (blk_max <= 6))               # amax lands in [4, 6]
+    s = d["sa"].numpy().astype(np.int64)
+    assert np.all((s >= 1) & (s <= 254))
