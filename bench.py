@@ -30,6 +30,7 @@ if ROOT not in sys.path:
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 SPEC_FP8_TFLOPS = 4500.0
 SPEC_F16_TFLOPS = 2250.0
+SPEC_FP4_TFLOPS = 13500.0
 SPEC_HBM_GBS = 8000.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "MXFP8 GEMM TFLOP/s at 8192^3 (% of GB300 FP8 peak); W8 GEMV GB/s (% of HBM)"
@@ -178,6 +179,12 @@ def run_ours(args, ws, rank, local):
         # fused-epilogue variants: C = relu(A B^T), and C = relu(A B^T + C) on its own buffer
         C8r = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
         C8a = torch.zeros(8192, 8192, dtype=torch.float16, device=dev)
+    if only == "mxfp4":      # the FP4 row, timed on its own: 8192^3 E2M1 with UE8M0 scales
+        m4 = synth.workload("mxfp4_8192")
+        A4 = q.qgemm_create_tensor(q.E2M1, m4["a"].to(dev), m4["sa"].to(dev))
+        B4 = q.qgemm_create_tensor(q.E2M1, m4["b"].to(dev), m4["sb"].to(dev))
+        C4 = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
+        del m4
     if want("f16"):
         f = synth.workload("f16_4096")
         fa, fb = f["a"].to(dev), f["b"].to(dev)
@@ -206,6 +213,8 @@ def run_ours(args, ws, rank, local):
     kernels = [k for k in all_kernels if want(k.split("_")[0])]
     if only == "epilogue":   # the fused output epilogues on the MXFP8 workload
         kernels = ["mxfp8", "mxfp8_relu", "mxfp8_accrelu"]
+    if only == "mxfp4":
+        kernels = ["mxfp4"]
     stream = torch.cuda.current_stream()
 
     def launch(k, i):
@@ -215,6 +224,8 @@ def run_ours(args, ws, rank, local):
             q.qgemm_mxfp8_ex(A8, B8, C8r, relu=True)
         elif k == "mxfp8_accrelu":
             q.qgemm_mxfp8_ex(A8, B8, C8a, accumulate=True, relu=True)
+        elif k == "mxfp4":
+            q.qgemm_mxfp4(A4, B4, C4)
         elif k == "f16":
             q.gemm_f16(fa, fb, fc)
         elif k == "w4a16":
@@ -313,6 +324,17 @@ def run_ours(args, ws, rank, local):
                             "tflops": round(tf, 1), "frac_of_fp8_spec_4500": round(tf / SPEC_FP8_TFLOPS, 4),
                             "epilogue": "C = relu(A B^T)" if k == "mxfp8_relu"
                             else "C = relu(A B^T + C): reads the old C (+134 MB)"}
+    if "mxfp4" in mean:
+        tf = 2.0 * 8192 ** 3 / (mean["mxfp4"] * 1e-3) / 1e12
+        fp4_peak_sust = 6.0 * peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+        secondary["mxfp4"] = {"us": round(mean["mxfp4"] * 1e3, 2),
+                              "us_median": round(median["mxfp4"] * 1e3, 2),
+                              "tflops": round(tf, 1),
+                              "frac_of_fp4_spec_13500": round(tf / SPEC_FP4_TFLOPS, 4),
+                              "frac_of_measured_bf16_sustained_x6": round(tf / fp4_peak_sust, 4),
+                              "kernel": "qgemm_mxfp4 = sf_pack_kernel<2> + mx_pair_kernel<E2M1>",
+                              "algorithmic_bytes": 2 * 8192 * 4096 + 2 * 8192 * 256
+                              + 2 * 8192 * 8192}
     mx_tflops = None
     if "mxfp8" in mean:
         mx_tflops = flops["mxfp8"] / (mean["mxfp8"] * 1e-3) / 1e12
@@ -323,7 +345,7 @@ def run_ours(args, ws, rank, local):
     value = (whole_job_rate(ws, flops["mxfp8"], mean["mxfp8"]) / 1e12
              if mx_tflops is not None else None)
     # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM)
-    launches = sum(2 if k.startswith("mxfp8") else 1 for k in kernels) * args.steps
+    launches = sum(2 if k.startswith("mxfp") else 1 for k in kernels) * args.steps
     line = {
         "metric": METRIC, "value": round(value, 2) if value is not None else None,
         "unit": "TFLOP/s", "n_gpus": ws,
@@ -458,9 +480,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", default=None, choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue"],
+    ap.add_argument("--only", default=None,
+                    choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue", "mxfp4"],
                     help="run one row of the hot path only (profiling); 'epilogue': MXFP8 8192^3 "
-                         "plain, with C = relu(A B^T) and with C = relu(A B^T + C)")
+                         "plain, with C = relu(A B^T) and with C = relu(A B^T + C); 'mxfp4': the "
+                         "FP4 (E2M1) GEMM at 8192^3")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

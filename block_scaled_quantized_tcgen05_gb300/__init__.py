@@ -14,14 +14,14 @@ import os
 from . import build as _build
 
 __all__ = [
-    "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "load_library", "library_path",
+    "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
     "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
-    "qgemm_mxfp8", "gemm_f16", "qgemm_w4a16", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout",
 ]
 
-F16, E4M3, INT8, INT4 = 0, 1, 2, 3
+F16, E4M3, INT8, INT4, E2M1 = 0, 1, 2, 3, 4
 OK = 0
 STATUS_NAMES = {0: "QGEMM_OK", 1: "QGEMM_ERR_INVALID_ARG", 2: "QGEMM_ERR_UNSUPPORTED_SHAPE",
                 3: "QGEMM_ERR_MISALIGNED", 4: "QGEMM_ERR_UNSUPPORTED_DTYPE", 5: "QGEMM_ERR_CUDA",
@@ -69,6 +69,8 @@ def load_library():
         "qgemm_mxfp8": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
+        "qgemm_mxfp4": (S, [P, P, P, I64, P]),
+        "qgemm_mxfp4_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "gemm_f16_ex": (S, [P, I64, P, I64, P, I64, I64, I64, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_w4a16_ex": (S, [P, I64, I64, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_w8_gemv_ex": (S, [P, I64, I64, P, P, I64, ctypes.POINTER(Epilogue), P]),
@@ -155,13 +157,13 @@ def qgemm_status_string(status: int) -> str:
 def qgemm_create_tensor(dtype: int, data, scales=None, rows: int | None = None,
                         k: int | None = None, block_k: int = 32) -> QTensor:
     """View of a [rows, k] quantized matrix.  ``data`` is a 2-D device tensor holding the data
-    plane row-major (uint8 for E4M3 / INT8 / packed INT4, fp16 for F16); ``scales`` is the
+    plane row-major (uint8 for E4M3 / INT8 / packed INT4 or E2M1, fp16 for F16); ``scales`` is the
     [rows, k/32] uint8 UE8M0 plane (None for F16)."""
     lib = load_library()
     rows = data.shape[0] if rows is None else rows
     if k is None:
         k = {F16: data.shape[1], E4M3: data.shape[1], INT8: data.shape[1],
-             INT4: 2 * data.shape[1]}[dtype]
+             INT4: 2 * data.shape[1], E2M1: 2 * data.shape[1]}[dtype]
     out = ctypes.c_void_p()
     st = lib.qgemm_create_tensor(ctypes.byref(out), dtype, rows, k, _ptr(data),
                                  _row_stride_bytes(data), _ptr(scales),
@@ -185,6 +187,13 @@ def qgemm_destroy_tensor(t: QTensor):
 def qgemm_mxfp8(A: QTensor, B: QTensor, C, stream=None):
     _check(load_library().qgemm_mxfp8(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
            "qgemm_mxfp8")
+    return C
+
+
+def qgemm_mxfp4(A: QTensor, B: QTensor, C, stream=None):
+    """C = A B^T with E2M1 operands (UE8M0 scale per 32 along K), fp32 accumulation, fp16 out."""
+    _check(load_library().qgemm_mxfp4(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
+           "qgemm_mxfp4")
     return C
 
 
@@ -225,6 +234,13 @@ def qgemm_mxfp8_ex(A: QTensor, B: QTensor, C, accumulate=False, relu=False, stre
     """C = relu?(A B^T [+ C]) with the MXFP8 operands of qgemm_mxfp8."""
     _check(load_library().qgemm_mxfp8_ex(A.handle, B.handle, _ptr(C), _ld(C),
                                          _epi(accumulate, relu), _stream(stream)), "qgemm_mxfp8_ex")
+    return C
+
+
+def qgemm_mxfp4_ex(A: QTensor, B: QTensor, C, accumulate=False, relu=False, stream=None):
+    """C = relu?(A B^T [+ C]) with the MXFP4 operands of qgemm_mxfp4."""
+    _check(load_library().qgemm_mxfp4_ex(A.handle, B.handle, _ptr(C), _ld(C),
+                                         _epi(accumulate, relu), _stream(stream)), "qgemm_mxfp4_ex")
     return C
 
 

@@ -4,7 +4,9 @@
 // The debug kernel writes out[r, k] = decode(data[r, k]) * 2^(scale[r, k/32] - 127) in fp32 so a
 // test can compare the decoded operands bit for bit with the CPU reference (the check the
 // "Running inline ML operations in a shader with Metal 4" sample makes against a CPU
-// implementation).  E4M3 is decoded by the hardware conversion instruction; integers by shifts.
+// implementation).  E4M3 and E2M1 are decoded by the hardware conversion instructions (so the
+// test also checks that the tensor cores' reading of the codes is the one the oracle spells out);
+// integers by shifts.
 #include <cuda_fp16.h>
 
 #include "qgemm_internal.h"
@@ -19,6 +21,18 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
     const uint16_t pair = static_cast<uint16_t>(byte & 0xFF);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF)));
+}
+
+// E2M1 nibble `hi` (0 = low, 1 = high) of `byte`.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t byte, int hi) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(h2)
+        : "r"(byte & 0xFFu));
+    const uint16_t h = static_cast<uint16_t>(hi ? (h2 >> 16) : (h2 & 0xFFFF));
+    return __half2float(__ushort_as_half(h));
 }
 
 __global__ void dequant_kernel(int dtype, int64_t rows, int64_t k, const uint8_t *__restrict__ data,
@@ -36,6 +50,8 @@ __global__ void dequant_kernel(int dtype, int64_t rows, int64_t k, const uint8_t
             float q;
             if (dtype == QGEMM_E4M3) {
                 q = e4m3_to_f32(row[j]);
+            } else if (dtype == QGEMM_E2M1) {   // nibble (j & 1) of byte j / 2
+                q = e2m1_to_f32(row[j >> 1], static_cast<int>(j & 1));
             } else if (dtype == QGEMM_INT8) {
                 q = static_cast<float>(static_cast<int>(static_cast<int8_t>(row[j])));
             } else {  // int4: nibble (j & 1) of byte j / 2, sign-extended

@@ -1,4 +1,4 @@
-// mxfp8_pair.cu -- block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2).
+// mxfp8_pair.cu -- block-scaled FP8 and FP4 GEMMs on CTA pairs (tcgen05 cta_group::2).
 //
 // Same product as mxfp8_gemm.cu (E4M3 data, UE8M0 scale per 32 along K, fp32 accumulation,
 // fp16 output), with one MMA spanning two SMs: a cluster of two CTAs computes a 256 x 256 output
@@ -33,6 +33,13 @@
 // registers first and releases the accumulator with one relaxed arrival on the leader's barrier
 // (its TMEM reads are complete at tcgen05.wait::ld), then stores.  Every wait is bounded.
 //
+// The same pipeline computes the MXFP4 product (E2M1 data packed two per byte, even k in the low
+// nibble; the same UE8M0 scale per 32 along K), as kind::mxf4.block_scale.scale_vec::2X MMAs.  A
+// stage still moves 128 bytes of each row, now 256 elements: four MMAs of K = 64, each reading two
+// scale bytes per row.  The repacked scale lines then come in pairs per stage (W = 2 words per
+// row: word w holds k-blocks 4 w .. 4 w + 3 of the stage), and a stage's TMEM slot holds two
+// A columns groups and two B column groups.  The kernel is a template over the two formats.
+//
 // Measured alternatives that lost (or won less): the scales copied by tcgen05.cp from the MMA thread (in this
 // kernel the copies serialise with the MMAs once TMA traffic competes for shared memory: +13%);
 // scale warps loading the repacked scales from global memory instead of shared memory (+2%);
@@ -53,8 +60,7 @@ using namespace qg;
 
 constexpr int BM = 128;                     // rows per CTA (256 per pair)
 constexpr int BN = 256;                     // columns per pair tile (128 of B per CTA)
-constexpr int BK = 128;                     // E4M3 bytes of K per stage
-constexpr int STAGES = 6;
+constexpr int BK = 128;                     // data bytes of K per stage (128 E4M3, 256 E2M1)
 // Warps: 0 producer, 1 MMA issuer, 2..9 epilogue (two per TMEM lane quarter, one per half of
 // the 256 accumulator columns, so the accumulator is drained -- and released to the next tile's
 // MMAs -- twice as fast as with four), 10..13 scale warps.
@@ -63,32 +69,64 @@ constexpr int SCALE_WARP0 = 2 + EPI_WARPS;
 constexpr int THREADS = 32 * (SCALE_WARP0 + 4);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;           // scale slots after the 256-column accumulator
-constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA 4 + SFB 8 (+4 spare)
-
 constexpr uint32_t A_BYTES = BM * BK;                 // 16 KB
 constexpr uint32_t B_BYTES = (BN / 2) * BK;           // 16 KB (this CTA's half)
-constexpr uint32_t SFA_BYTES = 512;                   // 128 rows x 4 bytes
-constexpr uint32_t SFB_BYTES = 1024;                  // 256 rows x 4 bytes
-constexpr uint32_t STAGE_TX = 2 * (A_BYTES + B_BYTES);   // both CTAs' data, on the leader
-constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;          // this CTA's scales, locally
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr uint32_t OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * 2048;
-// full[S] (leader), empty[S], sf_full[S], tmem_full, tmem_empty (leader), drain, then the slot
-constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
-constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 
-// kind::mxf8f6f4 block-scaled descriptor: E4M3 x E4M3, K-major, N = 256, UE8M0 scales, M = 256.
-constexpr uint32_t IDESC = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-                           (static_cast<uint32_t>(256 >> 7) << 27);
+// Element formats.  W = scale words (4 k-blocks each) per row per stage; one MMA covers W
+// k-blocks, so MMA j of a stage reads k-block j W: word (j W) / 4, byte (j W) % 4.
+struct FmtE4M3 {
+    static constexpr int W = 1;
+    static constexpr int ELEMS_PER_BYTE = 1;
+    static constexpr int STAGES = 6;
+    static constexpr uint32_t SF_COLS_PER_STAGE = 16;   // SFA 4 + SFB 8 (+4 spare)
+    // kind::mxf8f6f4 block-scaled descriptor: E4M3 x E4M3 (formats 0), K-major, N = 256,
+    // UE8M0 scales, M = 256.
+    static constexpr uint32_t IDESC = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+                                      (static_cast<uint32_t>(256 >> 7) << 27);
+    static __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t acc) {
+        mma_mxf8_pair(d, a, b, idesc, sfa, sfb, acc);
+    }
+};
+struct FmtE2M1 {
+    static constexpr int W = 2;
+    static constexpr int ELEMS_PER_BYTE = 2;
+    static constexpr int STAGES = 5;                    // six do not fit beside 3 KB of scales
+    static constexpr uint32_t SF_COLS_PER_STAGE = 24;   // SFA 2 x 4 + SFB 2 x 8
+    // kind::mxf4 block-scaled descriptor: E2M1 x E2M1 (format 1 in bits 7-9 and 10-12),
+    // K-major, N = 256, UE8M0 scales, M = 256, dense K = 64 (bit 31 clear).
+    static constexpr uint32_t IDESC = (1u << 7) | (1u << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+                                      (static_cast<uint32_t>(256 >> 7) << 27);
+    static __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t acc) {
+        mma_mxf4_pair(d, a, b, idesc, sfa, sfb, acc);
+    }
+};
+
+// Shared-memory map of one format.
+template <class F>
+struct Smem {
+    static constexpr int STAGES = F::STAGES;
+    static constexpr uint32_t SFA_BYTES = 512 * F::W;         // 128 rows x 4 W bytes
+    static constexpr uint32_t SFB_BYTES = 1024 * F::W;        // 256 rows x 4 W bytes
+    static constexpr uint32_t STAGE_TX = 2 * (A_BYTES + B_BYTES);   // both CTAs' data, on the leader
+    static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;        // this CTA's scales, locally
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * 2048;
+    // full[S] (leader), empty[S], sf_full[S], tmem_full, tmem_empty (leader), drain, then the slot
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + (3 * STAGES + 3) * 8;
+    static constexpr uint32_t BYTES = OFF_SLOT + 16 + 1024;
+    static_assert(BYTES <= 232448, "shared memory budget");
+    static_assert(SF_COL0 + STAGES * F::SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+};
 
 // ------------------------------------------------------------------------ scale repacking
-constexpr int PACK_KT = 8;                  // k-tiles per packing block
+constexpr int PACK_KT = 8;                  // scale words (4 k-blocks) per packing block
 constexpr int PACK_ROW = PACK_KT * 4 + 4;   // bytes per staged row (+4 keeps banks apart)
 
 struct SfPackOperand {
@@ -97,11 +135,13 @@ struct SfPackOperand {
     int rows;
     int kcols;               // K / 32
     int rbp;                 // padded count of 128-row blocks (even)
-    uint8_t *out;            // [KT][rbp][32 lines][16 bytes]
+    uint8_t *out;            // [KT][rbp][W][32 lines][16 bytes]
 };
 
-// grid (max rbp, ceil(KT / 8), 2 operands) x 256 threads.  Stage 128 rows x 32 scale bytes with
-// row-contiguous (coalesced) byte loads, then write 8 k-tiles x 32 lines of 16 bytes.
+// grid (max rbp, ceil(KT W / 8), 2 operands) x 256 threads.  Stage 128 rows x 32 scale bytes
+// with row-contiguous (coalesced) byte loads, then write 8 scale words x 32 lines of 16 bytes;
+// word kw is word kw % W of stage kw / W.
+template <int W>
 __global__ void __launch_bounds__(256)
 sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     __shared__ __align__(16) uint8_t tile[128 * PACK_ROW];
@@ -121,8 +161,8 @@ sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     }
     __syncthreads();
     const int ktl = t >> 5, i = t & 31;
-    const int kt = kt0 + ktl;
-    if (kt >= KT) return;
+    const int kw = kt0 + ktl;
+    if (kw >= KT * W) return;
     const uint32_t *w = reinterpret_cast<const uint32_t *>(tile);
     constexpr int WPR = PACK_ROW / 4;             // words per staged row
     uint4 v;
@@ -130,16 +170,27 @@ sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     v.y = w[(i + 32) * WPR + ktl];
     v.z = w[(i + 64) * WPR + ktl];
     v.w = w[(i + 96) * WPR + ktl];
-    uint8_t *dst = op.out + ((static_cast<int64_t>(kt) * op.rbp + rb) * 32 + i) * 16;
+    uint8_t *dst =
+        op.out + (((static_cast<int64_t>(kw / W) * op.rbp + rb) * W + kw % W) * 32 + i) * 16;
     *reinterpret_cast<uint4 *>(dst) = v;
 }
 
 // -------------------------------------------------------------------------------- the GEMM
+// K is in data bytes (K elements of E4M3, K / 2 of E2M1).
+template <class F>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const uint8_t *__restrict__ packA, const uint8_t *__restrict__ packB,
-                  int rbpA, int rbpB, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N,
-                  int K, int epi, unsigned *err, uint64_t timeout_ns) {
+mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const uint8_t *__restrict__ packA, const uint8_t *__restrict__ packB,
+               int rbpA, int rbpB, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N,
+               int K, int epi, unsigned *err, uint64_t timeout_ns) {
+    using L = Smem<F>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int W = F::W;
+    constexpr uint32_t SFA_BYTES = L::SFA_BYTES, SFB_BYTES = L::SFB_BYTES;
+    constexpr uint32_t OFF_A = L::OFF_A, OFF_B = L::OFF_B, OFF_SFA = L::OFF_SFA,
+                       OFF_SFB = L::OFF_SFB, OFF_EPI = L::OFF_EPI, OFF_BAR = L::OFF_BAR,
+                       OFF_SLOT = L::OFF_SLOT;
+    constexpr uint32_t SF_COLS_PER_STAGE = F::SF_COLS_PER_STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
@@ -205,17 +256,17 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), L::STAGE_TX);
                     tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
                     tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, &tmB, lead_full, kt * BK,
                                           nh, keep);
-                    mbar_arrive_expect_tx(sf_full(stage), SF_TX);
+                    mbar_arrive_expect_tx(sf_full(stage), L::SF_TX);
                     bulk_load(sb + OFF_SFA + stage * SFA_BYTES,
-                              packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16, SFA_BYTES,
-                              sf_full(stage));
+                              packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W,
+                              SFA_BYTES, sf_full(stage));
                     bulk_load(sb + OFF_SFB + stage * SFB_BYTES,
-                              packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16, SFB_BYTES,
-                              sf_full(stage));
+                              packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W,
+                              SFB_BYTES, sf_full(stage));
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -255,12 +306,15 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
                     const uint64_t adesc = adesc0 + stage * (A_BYTES >> 4);
                     const uint64_t bdesc = bdesc0 + stage * (B_BYTES >> 4);
-                    mma_mxf8_pair(tmem_base, adesc, bdesc, IDESC, sf_col, sf_col + 4,
-                                  kt > 0 ? 1u : 0u);
+                    // MMA j: 32 bytes of K at byte 32 j; its first k-block is j W, i.e. byte
+                    // (j W) % 4 of scale word (j W) / 4 (SFA word w at +4 w, SFB at +4 W + 8 w)
 #pragma unroll
-                    for (uint32_t j = 1; j < BK / 32; ++j)
-                        mma_mxf8_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j,
-                                      IDESC | (j << 4) | (j << 29), sf_col, sf_col + 4, 1u);
+                    for (uint32_t j = 0; j < BK / 32; ++j) {
+                        const uint32_t blk = j * W, w = blk >> 2, id = blk & 3;
+                        F::mma(tmem_base, adesc + 2 * j, bdesc + 2 * j,
+                               F::IDESC | (id << 4) | (id << 29), sf_col + 4 * w,
+                               sf_col + 4 * W + 8 * w, (kt > 0 || j > 0) ? 1u : 0u);
+                    }
                     tc_commit_pair(empty_bar(stage), 3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -280,7 +334,8 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp >= SCALE_WARP0) {
         // ------------------------------------------------------------- scale warps
         // Lane i of the warp for lane quarter q writes TMEM lane 32 q + i of the stage's slot:
-        // columns 0..3 the A scales of rows i + 32 c, columns 4..11 the B scales of rows i + 32 c.
+        // for scale word w, columns 4 w .. 4 w + 3 the A scales of rows i + 32 c and columns
+        // 4 W + 8 w .. 4 W + 8 w + 7 the B scales of rows i + 32 c.
         const uint32_t q = warp & 3;
         const uint32_t lead_full = map_to_cta(full_bar(0), 0);
         const int my_tiles = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
@@ -292,14 +347,18 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (lane == 0) atomicOr(err, ERR_PRODUCER);
                 break;
             }
+            // shared layout: A [W][32 lines][16], B [2 row blocks][W][32 lines][16]
             const uint8_t *sfa = smem + OFF_SFA + s * SFA_BYTES + lane * 16;
             const uint8_t *sfb = smem + OFF_SFB + s * SFB_BYTES + lane * 16;
-            const uint4 va = *reinterpret_cast<const uint4 *>(sfa);
-            const uint4 vb0 = *reinterpret_cast<const uint4 *>(sfb);
-            const uint4 vb1 = *reinterpret_cast<const uint4 *>(sfb + 512);
             const uint32_t col = tmem_base + ((q * 32) << 16) + SF_COL0 + s * SF_COLS_PER_STAGE;
-            tmem_st_32x32b_x4(col, va);
-            tmem_st_32x32b_x8(col + 4, vb0, vb1);
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const uint4 va = *reinterpret_cast<const uint4 *>(sfa + 512 * w);
+                const uint4 vb0 = *reinterpret_cast<const uint4 *>(sfb + 512 * w);
+                const uint4 vb1 = *reinterpret_cast<const uint4 *>(sfb + 512 * (W + w));
+                tmem_st_32x32b_x4(col + 4 * w, va);
+                tmem_st_32x32b_x8(col + 4 * W + 8 * w, vb0, vb1);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -343,6 +402,56 @@ mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
 int padded_blocks(int64_t rows) { return static_cast<int>(2 * ((rows + 255) / 256)); }
 
+// Data bytes of K for a view of format F (K elements).
+template <class F>
+int64_t k_bytes(const qgemm_tensor *t) { return t->k / F::ELEMS_PER_BYTE; }
+
+template <class F>
+size_t pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
+    const int64_t KT = (k_bytes<F>(A) + BK - 1) / BK;
+    return static_cast<size_t>(KT) * (padded_blocks(A->rows) + padded_blocks(B->rows)) * 512 *
+           F::W;
+}
+
+template <class F>
+cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                        void *scratch, const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
+              K = static_cast<int>(A->k);
+    const int Kb = static_cast<int>(k_bytes<F>(A));
+    const int KT = (Kb + BK - 1) / BK;
+    const int rbpA = padded_blocks(M), rbpB = padded_blocks(N);
+    uint8_t *packA = static_cast<uint8_t *>(scratch);
+    uint8_t *packB = packA + static_cast<size_t>(KT) * rbpA * 512 * F::W;
+    CUtensorMap tmA, tmB;
+    *encode_ok =
+        qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, Kb, M, A->ld, BK, BM,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+        qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, Kb, N, B->ld, BK, BN / 2,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+
+    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA};
+    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB};
+    const dim3 pgrid(static_cast<unsigned>(rbpA > rbpB ? rbpA : rbpB),
+                     static_cast<unsigned>((KT * F::W + PACK_KT - 1) / PACK_KT), 2);
+    sf_pack_kernel<F::W><<<pgrid, 256, 0, ctx.stream>>>(pa, pb, KT);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    e = cudaFuncSetAttribute(mx_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<F>::BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+    int pairs = ctx.num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
+    mx_pair_kernel<F><<<2 * pairs, THREADS, Smem<F>::BYTES, ctx.stream>>>(
+        tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err,
+        ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace qgi {
@@ -352,45 +461,21 @@ bool mxfp8_pair_eligible(const qgemm_tensor *A, const qgemm_tensor *B) {
 }
 
 size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
-    const int64_t KT = (A->k + BK - 1) / BK;
-    return static_cast<size_t>(KT) * (padded_blocks(A->rows) + padded_blocks(B->rows)) * 512;
+    return pair_scratch_bytes<FmtE4M3>(A, B);
 }
 
 cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
                               int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok) {
-    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
-              K = static_cast<int>(A->k);
-    const int KT = (K + BK - 1) / BK;
-    const int rbpA = padded_blocks(M), rbpB = padded_blocks(N);
-    uint8_t *packA = static_cast<uint8_t *>(scratch);
-    uint8_t *packB = packA + static_cast<size_t>(KT) * rbpA * 512;
-    CUtensorMap tmA, tmB;
-    *encode_ok =
-        encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, K, M, A->ld, BK, BM,
-                      CU_TENSOR_MAP_SWIZZLE_128B) &&
-        encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, K, N, B->ld, BK, BN / 2,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!*encode_ok) return cudaErrorInvalidValue;
+    return launch_pair<FmtE4M3>(A, B, C, ldc, scratch, ctx, encode_ok);
+}
 
-    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA};
-    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB};
-    const dim3 pgrid(static_cast<unsigned>(rbpA > rbpB ? rbpA : rbpB),
-                     static_cast<unsigned>((KT + PACK_KT - 1) / PACK_KT), 2);
-    sf_pack_kernel<<<pgrid, 256, 0, ctx.stream>>>(pa, pb, KT);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+size_t mxfp4_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
+    return pair_scratch_bytes<FmtE2M1>(A, B);
+}
 
-    e = cudaFuncSetAttribute(mxfp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
-    int pairs = ctx.num_sms / 2;
-    if (pairs > tiles) pairs = tiles;
-    const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
-    mxfp8_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, K, ctx.epi, ctx.err,
-        ctx.timeout_ns);
-    return cudaGetLastError();
+cudaError_t launch_mxfp4_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                              int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok) {
+    return launch_pair<FmtE2M1>(A, B, C, ldc, scratch, ctx, encode_ok);
 }
 
 }  // namespace qgi

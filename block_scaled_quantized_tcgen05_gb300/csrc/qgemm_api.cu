@@ -114,7 +114,8 @@ int64_t elem_bits(int32_t dt) {
     case QGEMM_F16: return 16;
     case QGEMM_E4M3:
     case QGEMM_INT8: return 8;
-    case QGEMM_INT4: return 4;
+    case QGEMM_INT4:
+    case QGEMM_E2M1: return 4;
     default: return 0;
     }
 }
@@ -304,6 +305,42 @@ static qgemm_status mxfp8_impl(const qgemm_tensor *A, const qgemm_tensor *B, voi
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_mxfp8 launch");
 }
 
+static qgemm_status mxfp4_impl(const qgemm_tensor *A, const qgemm_tensor *B, void *C,
+                               int64_t ldc, int epi, void *stream) {
+    if (!A || !B) return fail(QGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if (A->dtype != QGEMM_E2M1 || B->dtype != QGEMM_E2M1)
+        return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "qgemm_mxfp4 takes E2M1 views");
+    if (A->k != B->k) return fail(QGEMM_ERR_INVALID_ARG, "K mismatch (%lld vs %lld)",
+                                  (long long)A->k, (long long)B->k);
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    qgemm_status st = check_out_f16(C, ldc, M, N);
+    if (st != QGEMM_OK) return st;
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (K % 32) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "K %% 32 != 0");
+    for (const qgemm_tensor *t : {A, B}) {
+        if (K > 0 && (!aligned(t->data, 16) || t->ld % 16))
+            return fail(QGEMM_ERR_MISALIGNED, "E2M1 data must be 16-byte aligned, row stride %% 16 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(C), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
+    }
+    void *scratch = nullptr;
+    e = qgi::scratch_alloc(qgi::mxfp4_scratch_bytes(A, B), ctx, &scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "qgemm_mxfp4 scratch");
+    bool enc = true;
+    e = qgi::launch_mxfp4_pair(A, B, static_cast<__half *>(C), ldc, scratch, ctx, &enc);
+    const cudaError_t f = qgi::scratch_free(scratch, ctx);
+    if (!enc) return QGEMM_ERR_CUDA;
+    if (e == cudaSuccess) e = f;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_mxfp4 launch");
+}
+
 static qgemm_status gemm_f16_impl(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
                                   int64_t ldc, int64_t M, int64_t N, int64_t K, int epi,
                                   void *stream) {
@@ -427,6 +464,18 @@ qgemm_status qgemm_mxfp8_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *
     int f;
     const qgemm_status st = epi_flags(epilogue, &f);
     return st != QGEMM_OK ? st : mxfp8_impl(A, B, C, ldc, f, stream);
+}
+
+qgemm_status qgemm_mxfp4(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                         void *stream) {
+    return mxfp4_impl(A, B, C, ldc, 0, stream);
+}
+
+qgemm_status qgemm_mxfp4_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                            const qgemm_epilogue *epilogue, void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st : mxfp4_impl(A, B, C, ldc, f, stream);
 }
 
 qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,

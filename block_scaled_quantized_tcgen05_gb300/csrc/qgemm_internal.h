@@ -53,6 +53,11 @@ size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B);
 cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
                               int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok);
 
+// MXFP4 (E2M1) GEMM on CTA pairs, same pipeline and scratch contract as launch_mxfp8_pair.
+size_t mxfp4_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B);
+cudaError_t launch_mxfp4_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                              int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok);
+
 // Stream-ordered scratch from the library's per-device memory pool (memory is kept in the pool
 // between calls, so steady-state calls do not reach the driver's allocator).
 cudaError_t scratch_alloc(size_t bytes, const LaunchCtx &ctx, void **p);

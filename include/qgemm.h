@@ -48,7 +48,10 @@ typedef enum {
     QGEMM_F16 = 0,   /* IEEE binary16, no scale plane                                        */
     QGEMM_E4M3 = 1,  /* FP8 E4M3 (OCP, no infinity), one byte per element                    */
     QGEMM_INT8 = 2,  /* two's complement int8, one byte per element                          */
-    QGEMM_INT4 = 3   /* two's complement int4, two per byte, even k in the low nibble        */
+    QGEMM_INT4 = 3,  /* two's complement int4, two per byte, even k in the low nibble        */
+    QGEMM_E2M1 = 4   /* FP4 E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit; values
+                        0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives), two per byte, even k in
+                        the low nibble                                                        */
 } qgemm_dtype;
 
 /* Opaque, host-side, NON-owning view of one quantized matrix [rows, k]. */
@@ -68,13 +71,13 @@ int32_t qgemm_version(void);
  *   dt             element type of the data plane.
  *   rows, k        logical shape [rows, k]; k is the contiguous (reduction) dimension.
  *   data           device pointer to element (0, 0); row r starts at data + r * data_row_stride_bytes.
- *                  int4: element (r, k) is nibble (k & 1) of byte k / 2 of row r.
+ *                  int4, E2M1: element (r, k) is nibble (k & 1) of byte k / 2 of row r.
  *   scales_ue8m0   device pointer to the [rows, ceil(k / 32)] UE8M0 scale plane; scale (r, b) at
  *                  scales_ue8m0 + r * scale_row_stride_bytes + b.  Must be NULL for QGEMM_F16 and
  *                  non-NULL for the other types.
  *   block_k        must be 32 (QGEMM_ERR_UNSUPPORTED_DTYPE otherwise; ignored for QGEMM_F16).
  * Errors: QGEMM_ERR_INVALID_ARG (null out/data, negative sizes, strides shorter than a row),
- *         QGEMM_ERR_UNSUPPORTED_SHAPE (k % 32 != 0 for a scaled type; odd k for int4),
+ *         QGEMM_ERR_UNSUPPORTED_SHAPE (k % 32 != 0 for a scaled type),
  *         QGEMM_ERR_UNSUPPORTED_DTYPE (unknown dtype, block_k != 32, scales present for F16). */
 qgemm_status qgemm_create_tensor(qgemm_tensor **out, qgemm_dtype dt, int64_t rows, int64_t k,
                                  const void *data, int64_t data_row_stride_bytes,
@@ -140,6 +143,26 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
 qgemm_status qgemm_mxfp8_noalloc(const qgemm_tensor *A, const qgemm_tensor *B, void *C,
                                  int64_t ldc, void *stream);
 
+/* MXFP4 GEMM: C[M, N] = fp16_rn(sum_k deq(A)[m, k] * deq(B)[n, k]), fp32 accumulation, with
+ * deq(x)[r, k] = e2m1(x[r, k]) * 2^(scale[r, k / 32] - 127).
+ * Passage: "TensorOps: quantized matmul ...", section "Quantized dtype support matrix" (fp4 data
+ * fed natively to matmul2d, with the MX block scale factors in FP8 E8M0 as the scale plane) and
+ * "Optimize custom machine learning operations with Metal tensors", sections on native quantized
+ * types (4-bit floating point added beside FP8) and on multi-plane tensors (one E8M0 scale per
+ * block of the data plane); the right operand stored transposed, [N, K], as for qgemm_mxfp8.
+ *   A   QGEMM_E2M1 view [M, K];  B   QGEMM_E2M1 view [N, K] (same K), scales UE8M0 per 32.
+ *   C   device fp16 [M, N] with row stride ldc elements (ldc >= N).
+ * Requirements: K % 32 == 0; data pointers and byte strides 16-byte aligned; scale planes any
+ * alignment; C 2-byte aligned.  Any M, N >= 0 (every shape runs on CTA pairs, ragged tiles
+ * masked); M or N == 0 writes nothing; K == 0 writes zeros.
+ * Scratch: both scale planes are first rewritten into the order the tensor cores read them, in
+ * (2 ceil(M/256) + 2 ceil(N/256)) * ceil(K/256) * 1024 bytes of device scratch taken from the
+ * library's per-device pool on `stream` (as qgemm_mxfp8; two kernel launches).
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA
+ * (including a failed scratch allocation). */
+qgemm_status qgemm_mxfp4(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                         void *stream);
+
 /* fp16 GEMM: C[M, N] = fp16_rn(A[M, K] @ B[K, N]), fp32 accumulation, all row-major fp16.
  * Passage: "TensorOps: quantized matmul ...", "VALIDATED ON M4 MAX" (kernel M0, half x half ->
  * half) and "TileLang Metal Backend Internals", section 1 (fp16 input, fp32 accumulation, fp16
@@ -198,6 +221,8 @@ typedef struct qgemm_epilogue {
 
 qgemm_status qgemm_mxfp8_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                             const qgemm_epilogue *epilogue, void *stream);
+qgemm_status qgemm_mxfp4_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                            const qgemm_epilogue *epilogue, void *stream);
 qgemm_status gemm_f16_ex(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
                          int64_t ldc, int64_t M, int64_t N, int64_t K,
                          const qgemm_epilogue *epilogue, void *stream);
@@ -212,7 +237,7 @@ qgemm_status qgemm_w8_gemv_ex(const void *X_f16, int64_t ldx, int64_t M, const q
  * as fp32 (fp16 views: the value itself), written densely as [rows, k] row-major.  Exists so
  * that the decoded operand values can be compared bit for bit with the CPU reference, as the
  * "Running inline ML operations in a shader with Metal 4" sample checks its GPU result against a
- * CPU implementation.  E4M3 NaN codes and scale byte 255 give NaN.
+ * CPU implementation.  E4M3 NaN codes and scale byte 255 give NaN (E2M1 has no NaN code).
  * Errors: INVALID_ARG (null t or out); CUDA. */
 qgemm_status qgemm_dequant_debug(const qgemm_tensor *t, float *out, void *stream);
 

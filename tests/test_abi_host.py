@@ -149,3 +149,30 @@ def test_epilogue_descriptor_validation(lib):
     assert lib.qgemm_mxfp8_ex(e0, b, C, 256, ok, None) == 0                     # empty output
     for t in (a, b, b2, w4, e0):
         lib.qgemm_destroy_tensor(t)
+
+
+def test_mxfp4_rejects_before_launch(lib):
+    """qgemm_mxfp4 and its _ex form check dtype, K, output and alignment with no device work."""
+    _, a = _create(lib, q.E2M1, 128, 256, FAKE, 128, FAKE + 65536, 8)
+    _, b = _create(lib, q.E2M1, 256, 256, FAKE, 128, FAKE + 65536, 8)
+    _, b2 = _create(lib, q.E2M1, 256, 128, FAKE, 64, FAKE + 65536, 4)
+    _, f8 = _create(lib, q.E4M3, 256, 256, FAKE, 256, FAKE + 65536, 8)
+    _, misal = _create(lib, q.E2M1, 256, 256, FAKE + 8, 128, FAKE + 65536, 8)
+    _, odd = _create(lib, q.E2M1, 256, 256, FAKE, 136, FAKE + 65536, 8)
+    _, e0 = _create(lib, q.E2M1, 0, 256, FAKE, 128, FAKE + 65536, 8)
+    C = ctypes.c_void_p(FAKE + (1 << 24))
+    assert lib.qgemm_mxfp4(a, b2, C, 256, None) == 1            # K mismatch
+    assert lib.qgemm_mxfp4(a, f8, C, 256, None) == 4            # E4M3 operand
+    assert lib.qgemm_mxfp8(a, b, C, 256, None) == 4             # E2M1 views to the FP8 call
+    assert lib.qgemm_mxfp4(a, b, C, 128, None) == 1             # ldc < N
+    assert lib.qgemm_mxfp4(a, b, ctypes.c_void_p(FAKE + 1), 256, None) == 3   # C misaligned
+    assert lib.qgemm_mxfp4(a, misal, C, 256, None) == 3         # data misaligned
+    assert lib.qgemm_mxfp4(a, odd, C, 256, None) == 3           # row stride % 16
+    assert lib.qgemm_mxfp4(None, b, C, 256, None) == 1
+    assert lib.qgemm_mxfp4(e0, b, C, 256, None) == 0            # empty output: no-op
+    assert lib.qgemm_mxfp4_ex(a, b, C, 256, ctypes.byref(q.Epilogue(0, 2)), None) == 1
+    assert lib.qgemm_mxfp4_ex(a, f8, C, 256, ctypes.byref(q.Epilogue(1, 0)), None) == 4
+    # an E2M1 view is two elements per byte: k = 256 needs 128-byte rows
+    assert _create(lib, q.E2M1, 4, 256, FAKE, 100, FAKE, 8)[0] == 1
+    for t in (a, b, b2, f8, misal, odd, e0):
+        lib.qgemm_destroy_tensor(t)
