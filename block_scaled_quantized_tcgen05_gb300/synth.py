@@ -12,6 +12,7 @@ Workloads (all operands row-major, K contiguous, one UE8M0 scale per 32 elements
 * ``w4a16_prefill`` -- fp16 A [4096,4096] N(0,1); int4 W [14336,4096] from N(0, 0.02^2).
 * ``w8_decode``     -- fp16 X [M,8192] N(0,1), M in {1,8,16}; int8 W [28672,8192] from N(0, 0.02^2).
 * ``mxfp4_8192``    -- MXFP4 M=N=K=8192; each row of A and of B gets variance 10^U(-2,2).
+* ``w4a16_f16s_prefill`` -- as ``w4a16_prefill`` with fp16 block scales s = fp16(amax / 7).
 
 Encoding recipes (the pages only say "power-of-two block scales, 32 elements per block"; the
 per-format details below are the workload definitions):
@@ -125,6 +126,21 @@ def quantize_int_blocks(w: torch.Tensor, qmax: int):
     return q.contiguous(), scale_bytes.contiguous()
 
 
+def quantize_int4_f16_scales(w: torch.Tensor):
+    """fp32 [rows, K] -> (int8 values [rows, K] in [-8, 7], fp16 scales [rows, K/32]).
+
+    The custom (non-MX) format: each block's scale is the fp16 value nearest to amax / 7 (1.0 for
+    an all-zero block), not a power of two; q = round_half_even(w / s) clamped to [-8, 7]."""
+    w = w.to(torch.float64)
+    rows, k = w.shape
+    amax = _block_amax(w)
+    s16 = torch.where(amax > 0, amax / 7.0, torch.ones_like(amax)).to(torch.float16)
+    s64 = s16.to(torch.float64)
+    ws = w.reshape(rows, k // BLOCK, BLOCK)
+    q = torch.round(ws / s64.unsqueeze(2)).clamp(-8, 7).to(torch.int8).reshape(rows, k)
+    return q.contiguous(), s16.contiguous()
+
+
 def pack_int4(q: torch.Tensor) -> torch.Tensor:
     """int8 values in [-8, 7], [rows, K] -> packed uint8 [rows, K/2], even k in the low nibble."""
     rows, k = q.shape
@@ -141,7 +157,8 @@ def log_uniform_row_std(rows: int, g: torch.Generator, lo_exp=-2.0, hi_exp=2.0) 
 
 
 # ------------------------------------------------------------------------------ workloads
-WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode", "mxfp4_8192")
+WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode", "mxfp4_8192",
+             "w4a16_f16s_prefill")
 
 
 def mxfp8_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
@@ -193,6 +210,16 @@ def w4a16_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
             "M": M, "N": N, "K": K}
 
 
+def w4a16_f16s_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
+    """fp16 A [M,K] N(0,1); int4 W [N,K] (packed) with fp16 block scales [N,K/32]."""
+    g = generator(seed)
+    a = normal((M, K), g).to(torch.float16)
+    w = normal((N, K), g, std=w_std)
+    q, s = quantize_int4_f16_scales(w)
+    return {"a": a.contiguous(), "w": pack_int4(q), "w_values": q, "sw": s,
+            "M": M, "N": N, "K": K}
+
+
 def w8_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
     g = generator(seed)
     x = normal((M, K), g).to(torch.float16)
@@ -217,4 +244,6 @@ def workload(name: str, M: int | None = None):
         return w8_inputs(16 if M is None else M, 28672, 8192, seed)
     if name == "mxfp4_8192":
         return mxfp4_inputs(8192, 8192, 8192, seed, row_variance=True)
+    if name == "w4a16_f16s_prefill":
+        return w4a16_f16s_inputs(4096, 14336, 4096, seed)
     raise KeyError(name)

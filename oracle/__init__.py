@@ -14,6 +14,10 @@ Functions and the passages they follow:
 * ``dequant`` -- element times the scale of its 32-element block along K ("TensorOps: quantized
   matmul ...", section "Scale planes: one MTLTensor = data + scales"); int4 nibble order from the
   same page, section "VALIDATED ON M4 MAX", fact 5.
+* ``dequant_int4_f16s`` / ``w4a16_f16s`` -- the custom-format escape hatch: int4 weights with
+  arbitrary fp16 scales per block of 32 along K ("TensorOps: quantized matmul ...", sections
+  "Revised kernel strategy" and "M2 = block-32 fp16 scaling"), each weight dequantised to
+  fp16_rn(q * s) as that recipe's half multiply gives, then the product over those weights.
 * ``mxfp8`` / ``gemm_f16`` / ``w4a16`` / ``w8_gemv`` -- C = A * B^T over the decoded operands in
   fp64 (matmul2d, mode multiply: "TensorOps: quantized matmul ...", section "The real matmul2d
   API"), reported as IEEE binary16 round-to-nearest-even.
@@ -79,6 +83,8 @@ def _load():
         lib.orc_int8_get.argtypes = [ctypes.c_uint8]
         lib.orc_dequant.restype = None
         lib.orc_dequant.argtypes = [I, I64, I64, P, I64, P, I64, P, P]
+        lib.orc_dequant_int4_f16s.restype = None
+        lib.orc_dequant_int4_f16s.argtypes = [I64, I64, P, I64, P, I64, P, P]
         lib.orc_dequant_f16_kn.restype = None
         lib.orc_dequant_f16_kn.argtypes = [I64, I64, P, I64, P, P]
         lib.orc_dot_rows.restype = None
@@ -172,6 +178,22 @@ def dequant(dtype: int, data, scales, rows: np.ndarray | None = None, k: int | N
     return out
 
 
+def dequant_int4_f16s(w_packed, s_f16, rows: np.ndarray | None = None) -> np.ndarray:
+    """fp64 [len(rows), K] of int4 weights [R, K/2] with fp16 scales [R, K/32]: each element is
+    the fp16 value nearest (ties to even) to int4 * scale."""
+    d = _u8(w_packed)
+    sc = np.ascontiguousarray(np.asarray(s_f16).view(np.uint16))
+    R, k = d.shape[0], d.shape[1] * 2
+    if sc.shape != (R, k // 32):
+        raise ValueError("scales must be [rows, K/32] fp16")
+    idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, np.int64))
+    n = R if idx is None else idx.size
+    out = np.empty((n, k), np.float64)
+    _load().orc_dequant_int4_f16s(n, k, _ptr(d), d.shape[1], _ptr(sc), sc.shape[1], _ptr(idx),
+                                  _ptr(out))
+    return out
+
+
 def dequant_f16_kn(b, cols: np.ndarray | None = None) -> np.ndarray:
     """fp16 [K, N] row-major -> fp64 [len(cols), K] (the transposed right operand)."""
     b = np.ascontiguousarray(np.asarray(b).view(np.uint16))
@@ -248,6 +270,17 @@ def w4a16(a, w_packed, sw, rows=None) -> Result:
     K = a16.shape[1]
     Ad = dequant(F16, a16.view(np.uint8), None, rows, K)
     Wd = dequant(INT4, w_packed, sw, None, K)
+    C, D = dot_rows(Ad, Wd)
+    return Result(C, D, rows)
+
+
+def w4a16_f16s(a, w_packed, s_f16, rows=None) -> Result:
+    """C[m,n] = sum_k A[m,k] * fp16_rn(int4(W[n,k]) * S[n,k/32]); A fp16 [M,K], W packed int4
+    [N,K/2], S fp16 [N,K/32] (any finite or infinite fp16 values)."""
+    a16 = np.ascontiguousarray(np.asarray(a).view(np.uint16))
+    K = a16.shape[1]
+    Ad = dequant(F16, a16.view(np.uint8), None, rows, K)
+    Wd = dequant_int4_f16s(w_packed, s_f16)
     C, D = dot_rows(Ad, Wd)
     return Result(C, D, rows)
 

@@ -29,6 +29,13 @@
  *   - The exact product sum_k deq(A)[m,k]*deq(B)[n,k] is formed in fp64; the reported output is
  *     that value rounded to IEEE binary16 with round-to-nearest-even, overflow to +-inf.
  *
+ *   - "TensorOps: quantized matmul ...", sections "Revised kernel strategy" and "M2 = block-32
+ *     fp16 scaling" (the custom-format escape hatch: int4 weights with arbitrary fp16 scales per
+ *     block of 32 along K, which the native E8M0 scale plane cannot carry): each weight of a
+ *     block is dequantised into half precision as its int4 value times the block's fp16 scale,
+ *     and the half x half product is accumulated.  Reading: that dequantised weight is the fp16
+ *     round-to-nearest-even of the exact product q * s (one rounding, as a half multiply gives);
+ *     the product is then formed exactly from those weights.
  * Every function here follows the plain definition: decode each element, multiply by its
  * block's scale, sum the products in index order.  No blocking, no reordering.
  */
@@ -142,6 +149,25 @@ static double orc_element(int dtype, const uint8_t *data, int64_t ld, const uint
     }
     s = orc_ue8m0(scales[r * lds + j / 32]);   /* block of 32 along k, one row per block row */
     return q * s;
+}
+
+/* int4 weights with fp16 block scales (the M2 recipe): out[i*k + j] = value of
+ * fp16_rn(int4(W[r, j]) * fp16(S[r, j / 32])) for r = rows_idx[i]; S is [rows, k/32] fp16 bits
+ * with a row stride of lds elements. */
+void orc_dequant_int4_f16s(int64_t nrows, int64_t k, const uint8_t *data, int64_t ld,
+                           const uint16_t *scales, int64_t lds, const int64_t *rows_idx,
+                           double *out) {
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < nrows; ++i) {
+        int64_t r = rows_idx ? rows_idx[i] : i;
+        const uint8_t *row = data + r * ld;
+        int64_t j;
+        for (j = 0; j < k; ++j) {
+            double exact = (double)orc_int4_val(row, j) * orc_f16(scales[r * lds + j / 32]);
+            out[i * k + j] = orc_f16(orc_f16_rn(exact));
+        }
+    }
 }
 
 /* out[i*k + j] = decoded element (rows_idx[i], j).  rows_idx == NULL means rows 0..nrows-1. */

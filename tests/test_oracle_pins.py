@@ -347,3 +347,81 @@ def test_mxfp4_matches_library_matmul(orc):
     assert np.allclose(res.C, want, rtol=1e-12, atol=1e-12)
     sel = orc.mxfp4(a, sa, b, sb, rows=np.array([4, 1]))
     assert np.array_equal(sel.C, res.C[[4, 1]])
+
+
+# ------------------------------------------------- int4 with fp16 block scales (M2 recipe)
+def _f16_rne(x: Fraction) -> Fraction:
+    """Nearest binary16 value to an exact rational (ties to even), by Python's own half
+    packing (struct 'e'), which is independent of the oracle's rounding routine."""
+    import struct
+    return Fraction(struct.unpack("<e", struct.pack("<e", float(x)))[0]) \
+        if abs(x) < 65520 else None
+
+
+def test_w4a16_f16s_hand_worked_fold(orc):
+    """q = 7 with scale 1 + 2^-10: the exact product 7.0068359375 is not a half; the recipe's half
+    multiply gives 7.0078125 (spacing 2^-8 between 4 and 8; 1793.75 rounds to 1794).  With every
+    A element 1 over one block, C = 32 * 7.0078125 = 224.25 (the unrounded weights would give
+    224.21875)."""
+    w = np.full((1, 16), 0x77, np.uint8)
+    s = np.array([[1 + 2.0 ** -10]], np.float16)
+    assert np.all(orc.dequant_int4_f16s(w, s) == 7.0078125)
+    a = np.ones((1, 32), np.float16)
+    res = orc.w4a16_f16s(a, w, s)
+    assert res.C[0, 0] == 224.25
+    assert res.D[0, 0] == 224.25
+
+
+def test_w4a16_f16s_power_of_two_scales_reduce_to_ue8m0(orc):
+    """With every fp16 scale a power of two inside the exact range the product is the pinned
+    UE8M0 W4A16 product, bit for bit."""
+    M, N, K = 8, 40, 256
+    d = synth.w4a16_inputs(M, N, K, seed=31)
+    e = d["sw"].numpy().astype(np.int64)
+    s16 = (2.0 ** (e - 127)).astype(np.float16)
+    assert np.all(s16.astype(np.float64) == 2.0 ** (e - 127))
+    a = d["a"].numpy()
+    r1 = orc.w4a16_f16s(a, d["w"].numpy(), s16)
+    r2 = orc.w4a16(a, d["w"].numpy(), d["sw"].numpy())
+    assert np.array_equal(r1.C, r2.C) and np.array_equal(r1.D, r2.D)
+
+
+def test_w4a16_f16s_brute_force_exact_rationals(orc):
+    """Tiny random case: every weight rounded to half from the exact rational q * s, products
+    summed exactly; the oracle's fp64 sum agrees to fp64 accuracy."""
+    rng = np.random.default_rng(5)
+    M, N, K = 3, 4, 64
+    q = rng.integers(-8, 8, size=(N, K))
+    s = (rng.standard_normal((N, K // 32)) * 0.37).astype(np.float16)
+    s[0, 1] = np.float16(2.0 ** -14 * (1 + 2.0 ** -10))      # near the subnormal boundary
+    s[1, 0] = np.float16(6.1e4)                               # q * s can overflow to inf
+    q[1, :32] = np.clip(q[1, :32], -1, 1)                     # keep that block finite
+    a = (rng.standard_normal((M, K))).astype(np.float16)
+    packed = ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+    res = orc.w4a16_f16s(a, packed, s)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            mag = Fraction(0)
+            for k in range(K):
+                wk = _f16_rne(Fraction(int(q[n, k])) * Fraction(float(s[n, k // 32])))
+                p = Fraction(float(a[m, k])) * wk
+                exact += p
+                mag += abs(p)
+            assert abs(Fraction(res.C[m, n]) - exact) <= Fraction(1, 2 ** 40) * (mag + 1)
+            assert abs(Fraction(res.D[m, n]) - mag) <= Fraction(1, 2 ** 40) * (mag + 1)
+
+
+def test_w4a16_f16s_matches_library_matmul(orc):
+    """The oracle == numpy fp64 matmul over numpy's own half rounding of q * s, on the seeded
+    workload recipe at a small size."""
+    M, N, K = 16, 48, 256
+    d = synth.w4a16_f16s_inputs(M, N, K, seed=13)
+    q = d["w_values"].numpy().astype(np.float64)
+    s = np.repeat(d["sw"].numpy().astype(np.float64), 32, axis=1)
+    W = (q * s).astype(np.float16).astype(np.float64)
+    A = d["a"].numpy().astype(np.float64)
+    res = orc.w4a16_f16s(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    assert np.all(np.abs(res.C - A @ W.T) <= 1e-13 * (np.abs(A) @ np.abs(W).T))
+    assert not np.all(np.abs(d["sw"].numpy().astype(np.float64)) ==
+                      2.0 ** np.round(np.log2(np.abs(d["sw"].numpy().astype(np.float64)))))

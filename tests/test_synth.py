@@ -148,3 +148,19 @@ def test_mxfp4_quantizer_properties(orc):
     assert np.all((blk_max >= 4) & (blk_max <= 6))               # amax lands in [4, 6]
     s = d["sa"].numpy().astype(np.int64)
     assert np.all((s >= 1) & (s <= 254))
+
+
+def test_int4_f16_scale_encoder_matches_plain_restatement():
+    g = synth.generator(10)
+    w = synth.normal((3, 96), g, std=0.02)
+    w[1, 32:64] = 0.0
+    q, s = synth.quantize_int4_f16_scales(w)
+    assert q.dtype == torch.int8 and s.dtype == torch.float16 and s.shape == (3, 3)
+    for r in range(3):
+        for b in range(3):
+            blk = w[r, 32 * b:32 * b + 32].double().numpy()
+            amax = float(np.abs(blk).max())
+            want_s = np.float16(amax / 7.0) if amax > 0 else np.float16(1.0)
+            assert s[r, b].item() == float(want_s)
+            want_q = np.clip(np.round(blk / float(want_s)), -8, 7)       # half to even
+            assert np.array_equal(q[r, 32 * b:32 * b + 32].numpy(), want_q.astype(np.int8))
