@@ -185,6 +185,11 @@ def run_ours(args, ws, rank, local):
         B4 = q.qgemm_create_tensor(q.E2M1, m4["b"].to(dev), m4["sb"].to(dev))
         C4 = torch.empty(8192, 8192, dtype=torch.float16, device=dev)
         del m4
+    if only == "w4a16_f16s":   # int4 weights with fp16 block scales, the prefill shape
+        wf = synth.workload("w4a16_f16s_prefill")
+        wfa, wfw, wfs = wf["a"].to(dev), wf["w"].to(dev), wf["sw"].to(dev)
+        wfc = torch.empty(4096, 14336, dtype=torch.float16, device=dev)
+        del wf
     if want("f16"):
         f = synth.workload("f16_4096")
         fa, fb = f["a"].to(dev), f["b"].to(dev)
@@ -215,6 +220,8 @@ def run_ours(args, ws, rank, local):
         kernels = ["mxfp8", "mxfp8_relu", "mxfp8_accrelu"]
     if only == "mxfp4":
         kernels = ["mxfp4"]
+    if only == "w4a16_f16s":
+        kernels = ["w4a16_f16s"]
     stream = torch.cuda.current_stream()
 
     def launch(k, i):
@@ -226,6 +233,8 @@ def run_ours(args, ws, rank, local):
             q.qgemm_mxfp8_ex(A8, B8, C8a, accumulate=True, relu=True)
         elif k == "mxfp4":
             q.qgemm_mxfp4(A4, B4, C4)
+        elif k == "w4a16_f16s":
+            q.qgemm_w4a16_f16s(wfa, wfw, wfs, wfc)
         elif k == "f16":
             q.gemm_f16(fa, fb, fc)
         elif k == "w4a16":
@@ -296,14 +305,15 @@ def run_ours(args, ws, rank, local):
         e2e = e2e_mxfp8(q, torch, dev, a, sa, b, sb, reps=max(3, min(10, args.steps)))
 
     # ---------------------------------------------------------- derived numbers
-    flops = {"mxfp8": 2.0 * 8192 ** 3, "f16": 2.0 * 4096 ** 3, "w4a16": 2.0 * 4096 * 14336 * 4096}
+    flops = {"mxfp8": 2.0 * 8192 ** 3, "f16": 2.0 * 4096 ** 3, "w4a16": 2.0 * 4096 * 14336 * 4096,
+             "w4a16_f16s": 2.0 * 4096 * 14336 * 4096}
     gemv_bytes = {m: 28672 * 8192 + 28672 * 256 + m * 8192 * 2 + m * 28672 * 2 for m in (1, 8, 16)}
     peaks, peak_kind = _peaks()
     fp8_peak_sust = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     secondary = {}
     for k in kernels:
-        if k in ("f16", "w4a16"):
+        if k in ("f16", "w4a16", "w4a16_f16s"):
             tf = flops[k] / (mean[k] * 1e-3) / 1e12
             secondary[k] = {"us": round(mean[k] * 1e3, 2), "us_median": round(median[k] * 1e3, 2),
                             "tflops": round(tf, 1),
@@ -481,10 +491,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue", "mxfp4"],
+                    choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue", "mxfp4", "w4a16_f16s"],
                     help="run one row of the hot path only (profiling); 'epilogue': MXFP8 8192^3 "
                          "plain, with C = relu(A B^T) and with C = relu(A B^T + C); 'mxfp4': the "
-                         "FP4 (E2M1) GEMM at 8192^3")
+                         "FP4 (E2M1) GEMM at 8192^3; 'w4a16_f16s': int4 with fp16 block scales, "
+                         "4096 x 14336 x 4096")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

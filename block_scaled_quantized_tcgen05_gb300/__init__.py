@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
     "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
-    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout",
 ]
@@ -70,6 +70,9 @@ def load_library():
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_mxfp4": (S, [P, P, P, I64, P]),
+        "qgemm_w4a16_f16s": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64, P]),
+        "qgemm_w4a16_f16s_ex": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64,
+                                    ctypes.POINTER(Epilogue), P]),
         "qgemm_mxfp4_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "gemm_f16_ex": (S, [P, I64, P, I64, P, I64, I64, I64, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_w4a16_ex": (S, [P, I64, I64, P, P, I64, ctypes.POINTER(Epilogue), P]),
@@ -255,6 +258,27 @@ def gemm_f16_ex(A, B, C, accumulate=False, relu=False, stream=None):
 def qgemm_w4a16_ex(A, W: QTensor, C, accumulate=False, relu=False, stream=None):
     _check(load_library().qgemm_w4a16_ex(_ptr(A), _ld(A), A.shape[0], W.handle, _ptr(C), _ld(C),
                                          _epi(accumulate, relu), _stream(stream)), "qgemm_w4a16_ex")
+    return C
+
+
+def qgemm_w4a16_f16s(A, W, S, C, stream=None):
+    """C = A W^T with int4 W [N, K/2] (packed uint8) and fp16 block-32 scales S [N, K/32], each
+    weight dequantised to the half nearest q * s (the custom-format escape hatch)."""
+    M, K = A.shape
+    N = W.shape[0]
+    _check(load_library().qgemm_w4a16_f16s(_ptr(A), _ld(A), M, _ptr(W), _row_stride_bytes(W),
+                                           _ptr(S), _ld(S), N, K, _ptr(C), _ld(C),
+                                           _stream(stream)), "qgemm_w4a16_f16s")
+    return C
+
+
+def qgemm_w4a16_f16s_ex(A, W, S, C, accumulate=False, relu=False, stream=None):
+    M, K = A.shape
+    N = W.shape[0]
+    _check(load_library().qgemm_w4a16_f16s_ex(_ptr(A), _ld(A), M, _ptr(W), _row_stride_bytes(W),
+                                              _ptr(S), _ld(S), N, K, _ptr(C), _ld(C),
+                                              _epi(accumulate, relu), _stream(stream)),
+           "qgemm_w4a16_f16s_ex")
     return C
 
 

@@ -407,6 +407,46 @@ static qgemm_status w4a16_impl(const void *A_f16, int64_t lda, int64_t M, const 
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16 launch");
 }
 
+static qgemm_status w4a16_f16s_impl(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
+                                    int64_t ldw, const void *scales_f16, int64_t lds, int64_t N,
+                                    int64_t K, void *C_f16, int64_t ldc, int epi, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative shape");
+    if (M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "dimension >= 2^31");
+    qgemm_status st = check_out_f16(C_f16, ldc, M, N);
+    if (st != QGEMM_OK) return st;
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (K % 256) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "K %% 256 != 0 (K = %lld)", (long long)K);
+    if (K > 0) {
+        if (!A_f16 || !W_int4 || !scales_f16)
+            return fail(QGEMM_ERR_INVALID_ARG, "A, W or scales is NULL");
+        if (lda < K || ldw < K / 2 || lds < K / 32)
+            return fail(QGEMM_ERR_INVALID_ARG, "lda < K, ldw < K/2 bytes or lds < K/32");
+        if (!aligned(A_f16, 16) || lda % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "A must be 16-byte aligned, lda %% 8 == 0");
+        if (!aligned(W_int4, 16) || ldw % 16)
+            return fail(QGEMM_ERR_MISALIGNED, "int4 data must be 16-byte aligned, stride %% 16 == 0");
+        if (!aligned(scales_f16, 16) || lds % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "fp16 scales must be 16-byte aligned, lds %% 8 == 0");
+    }
+    qgi::LaunchCtx ctx;
+    st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    ctx.epi = epi;
+    cudaError_t e;
+    if (K == 0) {
+        e = qgi::launch_empty_sum_epilogue(static_cast<__half *>(C_f16), ldc, M, N, ctx);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "empty-sum epilogue");
+    }
+    bool enc = true;
+    e = qgi::launch_w4a16_f16s(static_cast<const __half *>(A_f16), lda, (int)M,
+                               static_cast<const uint8_t *>(W_int4), ldw,
+                               static_cast<const __half *>(scales_f16), lds, (int)N, (int)K,
+                               static_cast<__half *>(C_f16), ldc, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16_f16s launch");
+}
+
 static qgemm_status w8_gemv_impl(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
                                  void *Y_f16, int64_t ldy, int epi, void *stream) {
     if (!W) return fail(QGEMM_ERR_INVALID_ARG, "W is NULL");
@@ -502,6 +542,24 @@ qgemm_status qgemm_w4a16_ex(const void *A_f16, int64_t lda, int64_t M, const qge
     int f;
     const qgemm_status st = epi_flags(epilogue, &f);
     return st != QGEMM_OK ? st : w4a16_impl(A_f16, lda, M, W, C_f16, ldc, f, stream);
+}
+
+qgemm_status qgemm_w4a16_f16s(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
+                              int64_t ldw_bytes, const void *scales_f16, int64_t lds, int64_t N,
+                              int64_t K, void *C_f16, int64_t ldc, void *stream) {
+    return w4a16_f16s_impl(A_f16, lda, M, W_int4, ldw_bytes, scales_f16, lds, N, K, C_f16, ldc, 0,
+                           stream);
+}
+
+qgemm_status qgemm_w4a16_f16s_ex(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
+                                 int64_t ldw_bytes, const void *scales_f16, int64_t lds,
+                                 int64_t N, int64_t K, void *C_f16, int64_t ldc,
+                                 const qgemm_epilogue *epilogue, void *stream) {
+    int f;
+    const qgemm_status st = epi_flags(epilogue, &f);
+    return st != QGEMM_OK ? st
+                          : w4a16_f16s_impl(A_f16, lda, M, W_int4, ldw_bytes, scales_f16, lds, N,
+                                            K, C_f16, ldc, f, stream);
 }
 
 qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,

@@ -75,6 +75,11 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
 bool w4a16_pair_eligible(int M, const qgemm_tensor *W);
 cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
                               __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
+// int4 weights [N, K] (packed, row stride ldw bytes) with fp16 block-32 scales [N, K/32] (row
+// stride lds_elems), on the CTA-pair kernel: K % 256 == 0, W and scales 16-byte aligned rows.
+cudaError_t launch_w4a16_f16s(const __half *A, int64_t lda, int M, const uint8_t *W_int4,
+                              int64_t ldw, const __half *scales, int64_t lds_elems, int N, int K,
+                              __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
                            __half *Y, int64_t ldy, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);

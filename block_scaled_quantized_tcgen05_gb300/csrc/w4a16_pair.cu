@@ -31,6 +31,13 @@
 // from each converter warp of both CTAs after its tcgen05.st completed; commits are multicast;
 // every wait is bounded.  Used for K % 512 == 0 with 16-byte aligned scale rows (scales are read
 // 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.
+//
+// The same kernel, instantiated with SB = 2, runs the custom-format escape hatch: int4 weights
+// with arbitrary fp16 scales per 32-block ("TensorOps: quantized matmul ...", "M2 = block-32 fp16
+// scaling": each weight dequantised into half as q times its block's half scale).  The
+// converters then multiply the exact fp16 q by the fp16 scale with one rounding (mul.rn.f16x2),
+// which is that recipe's half multiply; scales are read 16 bytes = 4 k-tiles at a time, so that
+// instance needs K % 256 == 0 and 16-byte aligned scale rows, and takes every M and N.
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -82,6 +89,8 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// SB: bytes per block scale (1: UE8M0 byte, 2: fp16).  lds is in bytes.
+template <int SB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ CUtensorMap tmC, int c_tma,
@@ -227,7 +236,8 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         const int parity = static_cast<int>(warp - CONV_WARP0) >> 2;
         const uint32_t lead_full = map_to_cta(full_bar(0), 0);
         const int r = static_cast<int>(q * 32 + lane);
-        const int KG = KT / 8;                   // 16-byte scale groups per weight row
+        constexpr int SPG = 8 / SB;              // k-tiles per 16-byte scale group
+        const int KG = KT / SPG;                 // 16-byte scale groups per weight row
         // scale group cache: the group of (tile index ti, group g), and the next one prefetched
         auto group_ptr = [&](int ti, int g) -> const uint8_t * {
             const int tile = pair + ti * npairs;
@@ -237,7 +247,9 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             const int n = wb * 2 * BW + static_cast<int>(rank) * BW + r;
             return n < N ? scales + static_cast<int64_t>(n) * lds + 16 * g : nullptr;
         };
-        const uint4 unit = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        // rows past N: scale 1 (their weights are TMA zero fill, so any finite scale gives 0)
+        constexpr uint32_t ONE = SB == 1 ? 0x7F7F7F7Fu : 0x3C003C00u;
+        const uint4 unit = make_uint4(ONE, ONE, ONE, ONE);
         int cur_ti = 0, cur_g = 0;
         const uint8_t *p0 = total > 0 ? group_ptr(0, 0) : nullptr;
         uint4 cur = p0 ? ld_nc_v4(p0) : unit;
@@ -247,7 +259,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         uint32_t stage = 0, phase = 0;
         for (int it = 0; it < total; ++it) {
             const int ti = it / KT, kt = it - ti * KT;
-            const int g = kt >> 3;
+            const int g = kt / SPG;
             if (ti != cur_ti || g != cur_g) {    // move to the next scale group, prefetch one more
                 cur = nxt;
                 cur_ti = nxt_ti;
@@ -268,10 +280,27 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const uint8_t *raw = smem + OFF_RAW + stage * RAW_BYTES + r * (BK / 2);
                 const uint4 lo = *reinterpret_cast<const uint4 *>(raw);        // k  0..31
                 const uint4 hi = *reinterpret_cast<const uint4 *>(raw + 16);   // k 32..63
-                const int sbyte = (kt & 7) * 2;       // this stage's two scale bytes in the group
+                // this stage's two block scales: bytes 2 (kt % 8), + 1 of the group (UE8M0), or
+                // the fp16 pair in word kt % 4 (fp16 scales)
+                const int sbyte = SB == 1 ? (kt & 7) * 2 : (kt & 3) * 4;
                 const int wsel = sbyte >> 2;
                 const uint32_t word = wsel == 0 ? cur.x : wsel == 1 ? cur.y : wsel == 2 ? cur.z : cur.w;
                 uint32_t out[32];
+                if constexpr (SB == 2) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t s2 = __byte_perm(word, 0u, h ? 0x3232u : 0x1010u);
+                        const uint4 d = h ? hi : lo;
+                        const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t o[4];
+                            i4x8_to_f16(words[w], s2, o);   // exact q, then one rounding of q*s
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t e = (word >> (8 * ((sbyte & 3) + h))) & 0xFFu;
@@ -297,6 +326,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                             for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
                         }
                     }
+                }
                 }
                 tmem_st_32x32b_x32(tmem_base + ((q * 32) << 16) + A_COL0 + stage * A_COLS, out);
                 tmem_wait_st();
@@ -393,6 +423,39 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
+template <int SB>
+cudaError_t launch_pair_impl(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
+                             __half *C, int64_t ldc, const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
+    CUtensorMap tmX, tmW, tmC;
+    *encode_ok = qgi::encode_tma_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
+                               BT / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 qgi::encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K / 2, N, W->ld,
+                               BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!*encode_ok) return cudaErrorInvalidValue;
+    // output through TMA stores when C and its row stride allow a tensor map
+    // (the accumulate epilogue reads the old C element by element: direct stores)
+    const int c_tma = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0 &&
+                       !(ctx.epi & qgi::EPI_ACCUMULATE)) ? 1 : 0;
+    if (c_tma) {
+        *encode_ok = qgi::encode_tma_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2, 32, 32,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!*encode_ok) return cudaErrorInvalidValue;
+    } else {
+        tmC = tmX;   // unused
+    }
+    cudaError_t e = cudaFuncSetAttribute(w4a16_pair_kernel<SB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((N + 2 * BW - 1) / (2 * BW)) * ((M + BT - 1) / BT);
+    int pairs = ctx.num_sms / 2;
+    if (pairs > tiles) pairs = tiles;
+    w4a16_pair_kernel<SB><<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
+        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.epi, ctx.err,
+        ctx.timeout_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace qgi {
@@ -404,34 +467,15 @@ bool w4a16_pair_eligible(int M, const qgemm_tensor *W) {
 
 cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
                               __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
-    const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
-    CUtensorMap tmX, tmW, tmC;
-    *encode_ok = encode_tma_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
-                               BT / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
-                 encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K / 2, N, W->ld,
-                               BK / 2, BW, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!*encode_ok) return cudaErrorInvalidValue;
-    // output through TMA stores when C and its row stride allow a tensor map
-    // (the accumulate epilogue reads the old C element by element: direct stores)
-    const int c_tma = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0 &&
-                       !(ctx.epi & EPI_ACCUMULATE)) ? 1 : 0;
-    if (c_tma) {
-        *encode_ok = encode_tma_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, ldc * 2, 32, 32,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (!*encode_ok) return cudaErrorInvalidValue;
-    } else {
-        tmC = tmX;   // unused
-    }
-    cudaError_t e = cudaFuncSetAttribute(w4a16_pair_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int tiles = ((N + 2 * BW - 1) / (2 * BW)) * ((M + BT - 1) / BT);
-    int pairs = ctx.num_sms / 2;
-    if (pairs > tiles) pairs = tiles;
-    w4a16_pair_kernel<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.epi, ctx.err,
-        ctx.timeout_ns);
-    return cudaGetLastError();
+    return launch_pair_impl<1>(A, lda, M, W, C, ldc, ctx, encode_ok);
+}
+
+cudaError_t launch_w4a16_f16s(const __half *A, int64_t lda, int M, const uint8_t *W_int4,
+                              int64_t ldw, const __half *scales, int64_t lds_elems, int N, int K,
+                              __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok) {
+    qgemm_tensor w{QGEMM_INT4, N, K, W_int4, ldw, reinterpret_cast<const uint8_t *>(scales),
+                   lds_elems * 2};
+    return launch_pair_impl<2>(A, lda, M, &w, C, ldc, ctx, encode_ok);
 }
 
 }  // namespace qgi

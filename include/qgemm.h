@@ -189,6 +189,30 @@ qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, vo
 qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
                          void *C_f16, int64_t ldc, void *stream);
 
+/* Custom-format escape hatch: int4 weights with arbitrary fp16 scales per block of 32 along K.
+ * C[M, N] = fp16_rn(sum_k A[m, k] * w[n, k]),  w[n, k] = fp16_rn(q[n, k] * S[n, k / 32]),
+ * fp32 accumulation.
+ * Passage: "TensorOps: quantized matmul ...", sections "Two facts ..." (fact 2: the native scale
+ * plane takes only E8M0, so arbitrary fp16 block scales cannot ride on a tensor view), "Revised
+ * kernel strategy" and "M2 = block-32 fp16 scaling" (each weight of a 32-block dequantised into
+ * half as its int4 value times the block's fp16 scale, then the half x half matmul with fp32
+ * accumulation).  The dequantised weight is the half nearest to q * s (ties to even): exactly
+ * one rounding, as the recipe's half multiply gives.  Raw pointers, no view: the format is
+ * outside the native tensor type.
+ *   A        device fp16 [M, K], row stride lda elements.
+ *   W_int4   device int4 [N, K], two per byte (even k in the low nibble), row stride ldw_bytes.
+ *   scales   device fp16 [N, K / 32], row stride lds elements; any fp16 values (inf and NaN
+ *            propagate as the half multiply gives).
+ *   C        device fp16 [M, N], row stride ldc elements.
+ * Requirements: K % 256 == 0; A 16-byte aligned with lda % 8 == 0; W 16-byte aligned with
+ * ldw_bytes % 16 == 0; scales 16-byte aligned with lds % 8 == 0; C 2-byte aligned (16-byte
+ * aligned C with ldc % 8 == 0 takes TMA stores); any M, N >= 0 (ragged tiles masked; K == 0
+ * writes zeros).  Runs on CTA pairs for every shape.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+qgemm_status qgemm_w4a16_f16s(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
+                              int64_t ldw_bytes, const void *scales_f16, int64_t lds, int64_t N,
+                              int64_t K, void *C_f16, int64_t ldc, void *stream);
+
 /* Decode GEMV with int8 weights: Y[m, n] = fp16_rn(sum_k X[m, k] * deq(W)[n, k]), 1 <= M <= 16.
  * Passage: "TensorOps: quantized matmul ...", section "Why this matters here" (decode is bound
  * by memory bandwidth; int8 weights are read at int8 cost) and "VALIDATED ON M4 MAX" (kernel
@@ -229,6 +253,10 @@ qgemm_status gemm_f16_ex(const void *A, int64_t lda, const void *B, int64_t ldb,
 qgemm_status qgemm_w4a16_ex(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
                             void *C_f16, int64_t ldc, const qgemm_epilogue *epilogue,
                             void *stream);
+qgemm_status qgemm_w4a16_f16s_ex(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
+                                 int64_t ldw_bytes, const void *scales_f16, int64_t lds,
+                                 int64_t N, int64_t K, void *C_f16, int64_t ldc,
+                                 const qgemm_epilogue *epilogue, void *stream);
 qgemm_status qgemm_w8_gemv_ex(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
                               void *Y_f16, int64_t ldy, const qgemm_epilogue *epilogue,
                               void *stream);

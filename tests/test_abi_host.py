@@ -176,3 +176,30 @@ def test_mxfp4_rejects_before_launch(lib):
     assert _create(lib, q.E2M1, 4, 256, FAKE, 100, FAKE, 8)[0] == 1
     for t in (a, b, b2, f8, misal, odd, e0):
         lib.qgemm_destroy_tensor(t)
+
+
+def test_w4a16_f16s_rejects_before_launch(lib):
+    """The fp16-scale int4 GEMM validates shape, strides and alignment with no device work."""
+    P = ctypes.c_void_p
+    A, W, S, C = (P(FAKE + off) for off in (0, 1 << 20, 1 << 22, 1 << 24))
+    ok = dict(lda=256, M=16, ldw=128, lds=8, N=64, K=256, ldc=64)
+
+    def call(A=A, W=W, S=S, C=C, **kw):
+        a = dict(ok, **kw)
+        return lib.qgemm_w4a16_f16s(A, a["lda"], a["M"], W, a["ldw"], S, a["lds"], a["N"],
+                                    a["K"], C, a["ldc"], None)
+    assert call(K=288, lda=288, ldw=144, lds=16) == 2          # K % 256
+    assert call(lda=128) == 1                                  # lda < K
+    assert call(ldw=64) == 1                                   # ldw < K/2
+    assert call(lds=4) == 1                                    # lds < K/32
+    assert call(lda=260) == 3                                  # lda % 8
+    assert call(A=P(FAKE + 8)) == 3                            # A misaligned
+    assert call(W=P(FAKE + (1 << 20) + 8)) == 3                # W misaligned
+    assert call(ldw=136) == 3                                  # ldw % 16
+    assert call(S=P(FAKE + (1 << 22) + 2)) == 3                # scales misaligned
+    assert call(lds=12) == 3                                   # lds % 8
+    assert call(ldc=32) == 1                                   # ldc < N
+    assert call(M=-1) == 1
+    assert call(M=0) == 0 and call(N=0) == 0                   # empty output: no-op
+    assert lib.qgemm_w4a16_f16s_ex(A, 256, 16, W, 128, S, 8, 64, 256, C, 64,
+                                   ctypes.byref(q.Epilogue(0, 5)), None) == 1
