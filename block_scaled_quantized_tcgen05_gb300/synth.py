@@ -13,6 +13,8 @@ Workloads (all operands row-major, K contiguous, one UE8M0 scale per 32 elements
 * ``w8_decode``     -- fp16 X [M,8192] N(0,1), M in {1,8,16}; int8 W [28672,8192] from N(0, 0.02^2).
 * ``mxfp4_8192``    -- MXFP4 M=N=K=8192; each row of A and of B gets variance 10^U(-2,2).
 * ``w4a16_f16s_prefill`` -- as ``w4a16_prefill`` with fp16 block scales s = fp16(amax / 7).
+* ``attn_prefill``  -- fused attention: Q, K, V fp16 [32 heads, 4096, 128] N(0,1), scale
+  1/sqrt(128) (a bidirectional prefill of one sequence).
 
 Encoding recipes (the pages only say "power-of-two block scales, 32 elements per block"; the
 per-format details below are the workload definitions):
@@ -158,7 +160,7 @@ def log_uniform_row_std(rows: int, g: torch.Generator, lo_exp=-2.0, hi_exp=2.0) 
 
 # ------------------------------------------------------------------------------ workloads
 WORKLOADS = ("mxfp8_small", "f16_4096", "mxfp8_8192", "w4a16_prefill", "w8_decode", "mxfp4_8192",
-             "w4a16_f16s_prefill")
+             "w4a16_f16s_prefill", "attn_prefill")
 
 
 def mxfp8_inputs(M: int, N: int, K: int, seed: int, row_variance: bool = False):
@@ -220,6 +222,17 @@ def w4a16_f16s_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
             "M": M, "N": N, "K": K}
 
 
+def attention_inputs(BH: int, Lq: int, Lk: int, d: int, seed: int, q_std: float = 1.0):
+    """fp16 Q [BH, Lq, d], K and V [BH, Lk, d] from N(0, 1) (Q times q_std: a larger q_std makes
+    the softmax rows peakier); scale 1/sqrt(d)."""
+    g = generator(seed)
+    q = (normal((BH, Lq, d), g) * q_std).to(torch.float16)
+    k = normal((BH, Lk, d), g).to(torch.float16)
+    v = normal((BH, Lk, d), g).to(torch.float16)
+    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), "scale": d ** -0.5,
+            "BH": BH, "Lq": Lq, "Lk": Lk, "d": d}
+
+
 def w8_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
     g = generator(seed)
     x = normal((M, K), g).to(torch.float16)
@@ -246,4 +259,6 @@ def workload(name: str, M: int | None = None):
         return mxfp4_inputs(8192, 8192, 8192, seed, row_variance=True)
     if name == "w4a16_f16s_prefill":
         return w4a16_f16s_inputs(4096, 14336, 4096, seed)
+    if name == "attn_prefill":
+        return attention_inputs(32, 4096, 4096, 128, seed)
     raise KeyError(name)

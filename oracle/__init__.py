@@ -18,6 +18,10 @@ Functions and the passages they follow:
   arbitrary fp16 scales per block of 32 along K ("TensorOps: quantized matmul ...", sections
   "Revised kernel strategy" and "M2 = block-32 fp16 scaling"), each weight dequantised to
   fp16_rn(q * s) as that recipe's half multiply gives, then the product over those weights.
+* ``attention`` -- fused attention ("TensorOps: quantized matmul ...", section "FlashAttention on
+  TensorOps (the recipe)"; "Optimize custom machine learning operations with Metal tensors",
+  section on FlashAttention with cooperative tensors): Q K^T scaled, each row's maximum, exp of
+  the scores minus it, normalised by the row sum, times V, all in fp64.
 * ``mxfp8`` / ``gemm_f16`` / ``w4a16`` / ``w8_gemv`` -- C = A * B^T over the decoded operands in
   fp64 (matmul2d, mode multiply: "TensorOps: quantized matmul ...", section "The real matmul2d
   API"), reported as IEEE binary16 round-to-nearest-even.
@@ -85,6 +89,9 @@ def _load():
         lib.orc_dequant.argtypes = [I, I64, I64, P, I64, P, I64, P, P]
         lib.orc_dequant_int4_f16s.restype = None
         lib.orc_dequant_int4_f16s.argtypes = [I64, I64, P, I64, P, I64, P, P]
+        lib.orc_attention.restype = None
+        lib.orc_attention.argtypes = [I64, P, P, I64, I64, P, I64, I64, P, I64, I64, P, I64, I64,
+                                      ctypes.c_double, P, P]
         lib.orc_dequant_f16_kn.restype = None
         lib.orc_dequant_f16_kn.argtypes = [I64, I64, P, I64, P, P]
         lib.orc_dot_rows.restype = None
@@ -283,6 +290,28 @@ def w4a16_f16s(a, w_packed, s_f16, rows=None) -> Result:
     Wd = dequant_int4_f16s(w_packed, s_f16)
     C, D = dot_rows(Ad, Wd)
     return Result(C, D, rows)
+
+
+def attention(q, k, v, scale: float, heads=None, qrows=None) -> Result:
+    """O = softmax(scale * Q K^T) V per head, q [BH, Lq, d], k and v [BH, Lk, d] fp16 (numpy or
+    torch CPU).  ``heads`` / ``qrows`` select output rows (default: every (head, row) pair, in
+    order); the Result holds O and D as [n, d]."""
+    Q = np.ascontiguousarray(np.asarray(q).view(np.uint16))
+    K = np.ascontiguousarray(np.asarray(k).view(np.uint16))
+    V = np.ascontiguousarray(np.asarray(v).view(np.uint16))
+    BH, Lq, d = Q.shape
+    Lk = K.shape[1]
+    if heads is None:
+        heads = np.repeat(np.arange(BH, dtype=np.int64), Lq)
+        qrows = np.tile(np.arange(Lq, dtype=np.int64), BH)
+    heads = np.ascontiguousarray(np.asarray(heads, np.int64))
+    qrows = np.ascontiguousarray(np.asarray(qrows, np.int64))
+    n = heads.size
+    O = np.empty((n, d), np.float64)
+    D = np.empty((n, d), np.float64)
+    _load().orc_attention(n, _ptr(heads), _ptr(qrows), Lk, d, _ptr(Q), Lq * d, d, _ptr(K),
+                          Lk * d, d, _ptr(V), Lk * d, d, float(scale), _ptr(O), _ptr(D))
+    return Result(O, D, None)
 
 
 def w8_gemv(x, w, sw) -> Result:

@@ -36,11 +36,19 @@
  *     and the half x half product is accumulated.  Reading: that dequantised weight is the fp16
  *     round-to-nearest-even of the exact product q * s (one rounding, as a half multiply gives);
  *     the product is then formed exactly from those weights.
+ *   - "TensorOps: quantized matmul ...", section "FlashAttention on TensorOps (the recipe)", and
+ *     "Optimize custom machine learning operations with Metal tensors", section on FlashAttention
+ *     with cooperative tensors: fused attention multiplies Q by K^T, takes each row's maximum
+ *     (initial value -infinity), exponentiates each score minus its row maximum, and multiplies
+ *     the result by V.  Readings: the softmax is normalised (each row of exp(s - max) divided by
+ *     its sum, which is what softmax means in that text); the scores carry a caller-given scale
+ *     (1/sqrt(d) for scaled dot-product attention); no mask (the recipe shows none).
  * Every function here follows the plain definition: decode each element, multiply by its
  * block's scale, sum the products in index order.  No blocking, no reordering.
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* dtype codes private to the oracle */
@@ -249,6 +257,48 @@ void orc_f16_rn_array(int64_t count, const double *x, uint16_t *bits) {
     int64_t i;
 #pragma omp parallel for schedule(static)
     for (i = 0; i < count; ++i) bits[i] = orc_f16_rn(x[i]);
+}
+
+/* Fused attention, one output row per (head, query) pair listed in heads[i], qrows[i]:
+ *   s_j = scale * sum_c Q[h, r, c] K[h, j, c]        (j = 0 .. Lk-1)
+ *   m = max_j s_j;  p_j = exp(s_j - m);  l = sum_j p_j
+ *   O[i, c] = sum_j p_j V[h, j, c] / l;   Dm[i, c] = sum_j p_j |V[h, j, c]| / l
+ * Q, K, V are fp16 bits laid out [BH][L][d] with the given head and row strides (elements).
+ * Dm is the magnitude the tolerance is normalised by. */
+void orc_attention(int64_t n, const int64_t *heads, const int64_t *qrows, int64_t Lk, int64_t d,
+                   const uint16_t *Q, int64_t q_hs, int64_t q_rs, const uint16_t *K, int64_t k_hs,
+                   int64_t k_rs, const uint16_t *V, int64_t v_hs, int64_t v_rs, double scale,
+                   double *O, double *Dm) {
+    int64_t i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < n; ++i) {
+        const uint16_t *q = Q + heads[i] * q_hs + qrows[i] * q_rs;
+        double *s = (double *)malloc((size_t)Lk * sizeof(double));
+        double m = -INFINITY, l = 0.0;
+        int64_t j, c;
+        for (j = 0; j < Lk; ++j) {
+            const uint16_t *k = K + heads[i] * k_hs + j * k_rs;
+            double dot = 0.0;
+            for (c = 0; c < d; ++c) dot += orc_f16(q[c]) * orc_f16(k[c]);
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        for (j = 0; j < Lk; ++j) {
+            s[j] = exp(s[j] - m);
+            l += s[j];
+        }
+        for (c = 0; c < d; ++c) {
+            double o = 0.0, a = 0.0;
+            for (j = 0; j < Lk; ++j) {
+                double v = orc_f16(V[heads[i] * v_hs + j * v_rs + c]);
+                o += s[j] * v;
+                a += s[j] * fabs(v);
+            }
+            O[i * d + c] = o / l;
+            Dm[i * d + c] = a / l;
+        }
+        free(s);
+    }
 }
 
 /* tables for the pin tests: all 256 codes of each 8-bit format */

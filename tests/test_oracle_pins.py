@@ -425,3 +425,76 @@ def test_w4a16_f16s_matches_library_matmul(orc):
     assert np.all(np.abs(res.C - A @ W.T) <= 1e-13 * (np.abs(A) @ np.abs(W).T))
     assert not np.all(np.abs(d["sw"].numpy().astype(np.float64)) ==
                       2.0 ** np.round(np.log2(np.abs(d["sw"].numpy().astype(np.float64)))))
+
+
+# ----------------------------------------------------------------------- fused attention
+def _attn_arrays(BH, Lq, Lk, d, seed, q_std=1.0):
+    d_ = synth.attention_inputs(BH, Lq, Lk, d, seed, q_std=q_std)
+    return d_["q"].numpy(), d_["k"].numpy(), d_["v"].numpy(), d_["scale"]
+
+
+def test_attention_equal_keys_give_the_mean_of_v(orc):
+    """All keys equal: every score of a row is the same, the softmax is uniform and O is the
+    plain mean of the value rows."""
+    q, k, v, scale = _attn_arrays(2, 5, 7, 16, seed=51)
+    k[:] = k[:, :1, :]
+    res = orc.attention(q, k, v, scale)
+    want = np.repeat(v.astype(np.float64).mean(axis=1), 5, axis=0)
+    assert np.allclose(res.C, want, rtol=0, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value(orc):
+    """One score 1000 above the rest: exp(-1000) underflows to 0 in fp64, so O is that key's
+    value row exactly and D its magnitude."""
+    d = 8
+    q = np.zeros((1, 1, d), np.float16)
+    q[0, 0, 0] = 1.0
+    k = np.zeros((1, 4, d), np.float16)
+    k[0, 2, 0] = 1000.0
+    v = np.arange(32, dtype=np.float16).reshape(1, 4, d) - 10
+    res = orc.attention(q, k, v, 1.0)
+    assert np.array_equal(res.C[0], v[0, 2].astype(np.float64))
+    assert np.array_equal(res.D[0], np.abs(v[0, 2].astype(np.float64)))
+
+
+def test_attention_matches_library_sdpa(orc):
+    """torch's scaled_dot_product_attention in fp64 (a library routine) on decoded fp16 data."""
+    q, k, v, scale = _attn_arrays(3, 37, 53, 32, seed=52, q_std=3.0)
+    res = orc.attention(q, k, v, scale)
+    t = [torch.from_numpy(x.astype(np.float64)) for x in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(t[0], t[1], t[2], scale=scale)
+    assert np.allclose(res.C, ref.reshape(-1, 32).numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_invariants(orc):
+    """Permuting keys together with their values leaves O unchanged; a per-row shift of every
+    score (a key component shared by all keys) leaves O unchanged."""
+    q, k, v, scale = _attn_arrays(1, 6, 40, 16, seed=53, q_std=2.0)
+    base = orc.attention(q, k, v, scale).C
+    perm = np.random.default_rng(0).permutation(40)
+    assert np.allclose(orc.attention(q, k[:, perm], v[:, perm], scale).C, base, atol=1e-13)
+    k2 = k.copy()
+    k2[:, :, 15] = 1.0
+    q0 = q.copy()
+    q0[:, :, 15] = 0.0
+    q1 = q.copy()
+    q1[:, :, 15] = np.linspace(-4, 4, 6).astype(np.float16)
+    assert np.allclose(orc.attention(q0, k2, v, scale).C, orc.attention(q1, k2, v, scale).C,
+                       atol=1e-13)
+
+
+def test_attention_high_precision_tiny(orc):
+    """A tiny case against 50-digit arithmetic (mpmath) of the same definition."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    q, k, v, scale = _attn_arrays(1, 3, 5, 4, seed=54, q_std=2.0)
+    res = orc.attention(q, k, v, scale)
+    for i in range(3):
+        s = [mpmath.mpf(scale) * sum(mpmath.mpf(float(q[0, i, c])) * mpmath.mpf(float(k[0, j, c]))
+                                     for c in range(4)) for j in range(5)]
+        m = max(s)
+        p = [mpmath.e ** (x - m) for x in s]
+        l = sum(p)
+        for c in range(4):
+            o = sum(p[j] * mpmath.mpf(float(v[0, j, c])) for j in range(5)) / l
+            assert abs(float(o) - res.C[i, c]) <= 1e-14
