@@ -190,6 +190,12 @@ def run_ours(args, ws, rank, local):
         wfa, wfw, wfs = wf["a"].to(dev), wf["w"].to(dev), wf["sw"].to(dev)
         wfc = torch.empty(4096, 14336, dtype=torch.float16, device=dev)
         del wf
+    if only == "attention":   # fused attention, 32 heads x 4096 x 4096 x 128
+        at = synth.workload("attn_prefill")
+        atq, atk, atv = at["q"].to(dev), at["k"].to(dev), at["v"].to(dev)
+        ato = torch.empty_like(atq)
+        at_scale = at["scale"]
+        del at
     if want("f16"):
         f = synth.workload("f16_4096")
         fa, fb = f["a"].to(dev), f["b"].to(dev)
@@ -222,6 +228,8 @@ def run_ours(args, ws, rank, local):
         kernels = ["mxfp4"]
     if only == "w4a16_f16s":
         kernels = ["w4a16_f16s"]
+    if only == "attention":
+        kernels = ["attention"]
     stream = torch.cuda.current_stream()
 
     def launch(k, i):
@@ -235,6 +243,8 @@ def run_ours(args, ws, rank, local):
             q.qgemm_mxfp4(A4, B4, C4)
         elif k == "w4a16_f16s":
             q.qgemm_w4a16_f16s(wfa, wfw, wfs, wfc)
+        elif k == "attention":
+            q.qgemm_attention(atq, atk, atv, ato, scale=at_scale)
         elif k == "f16":
             q.gemm_f16(fa, fb, fc)
         elif k == "w4a16":
@@ -306,14 +316,14 @@ def run_ours(args, ws, rank, local):
 
     # ---------------------------------------------------------- derived numbers
     flops = {"mxfp8": 2.0 * 8192 ** 3, "f16": 2.0 * 4096 ** 3, "w4a16": 2.0 * 4096 * 14336 * 4096,
-             "w4a16_f16s": 2.0 * 4096 * 14336 * 4096}
+             "w4a16_f16s": 2.0 * 4096 * 14336 * 4096, "attention": 4.0 * 32 * 4096 * 4096 * 128}
     gemv_bytes = {m: 28672 * 8192 + 28672 * 256 + m * 8192 * 2 + m * 28672 * 2 for m in (1, 8, 16)}
     peaks, peak_kind = _peaks()
     fp8_peak_sust = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     secondary = {}
     for k in kernels:
-        if k in ("f16", "w4a16", "w4a16_f16s"):
+        if k in ("f16", "w4a16", "w4a16_f16s", "attention"):
             tf = flops[k] / (mean[k] * 1e-3) / 1e12
             secondary[k] = {"us": round(mean[k] * 1e3, 2), "us_median": round(median[k] * 1e3, 2),
                             "tflops": round(tf, 1),
@@ -491,11 +501,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue", "mxfp4", "w4a16_f16s"],
+                    choices=["mxfp8", "f16", "w4a16", "gemv", "epilogue", "mxfp4", "w4a16_f16s",
+                             "attention"],
                     help="run one row of the hot path only (profiling); 'epilogue': MXFP8 8192^3 "
                          "plain, with C = relu(A B^T) and with C = relu(A B^T + C); 'mxfp4': the "
                          "FP4 (E2M1) GEMM at 8192^3; 'w4a16_f16s': int4 with fp16 block scales, "
-                         "4096 x 14336 x 4096")
+                         "4096 x 14336 x 4096; 'attention': fused attention, 32 heads x 4096 x "
+                         "4096 x 128")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

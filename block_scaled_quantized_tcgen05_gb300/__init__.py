@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
     "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
-    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout",
 ]
@@ -70,6 +70,7 @@ def load_library():
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_mxfp4": (S, [P, P, P, I64, P]),
+        "qgemm_attention_f16": (S, [P, P, P, P] + [I64] * 12 + [ctypes.c_float, P]),
         "qgemm_w4a16_f16s": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64, P]),
         "qgemm_w4a16_f16s_ex": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64,
                                     ctypes.POINTER(Epilogue), P]),
@@ -259,6 +260,23 @@ def qgemm_w4a16_ex(A, W: QTensor, C, accumulate=False, relu=False, stream=None):
     _check(load_library().qgemm_w4a16_ex(_ptr(A), _ld(A), A.shape[0], W.handle, _ptr(C), _ld(C),
                                          _epi(accumulate, relu), _stream(stream)), "qgemm_w4a16_ex")
     return C
+
+
+def qgemm_attention(Q, K, V, O, scale=None, stream=None):
+    """O = softmax(scale Q K^T) V per head; Q, O [BH, Lq, 128], K, V [BH, Lk, 128] fp16 device
+    tensors with a contiguous last dimension; scale defaults to 1/sqrt(128)."""
+    for t in (Q, K, V, O):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("expected [BH, L, d] tensors with a contiguous last dimension")
+    BH, Lq, d = Q.shape
+    Lk = K.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    _check(load_library().qgemm_attention_f16(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), BH, Lq, Lk, d, Q.stride(0), Q.stride(1),
+        K.stride(0), K.stride(1), V.stride(0), V.stride(1), O.stride(0), O.stride(1),
+        float(scale), _stream(stream)), "qgemm_attention_f16")
+    return O
 
 
 def qgemm_w4a16_f16s(A, W, S, C, stream=None):

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -134,9 +135,8 @@ qgemm_status fail(qgemm_status s, const char *fmt, ...) {
     return s;
 }
 
-bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
-                   uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
-                   uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+// The driver's tensor-map encoder, looked up once; records an error and returns null if absent.
+static EncodeTiledFn get_encode() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -145,10 +145,14 @@ bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, u
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     });
-    if (!g_encode) {
-        fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-        return false;
-    }
+    if (!g_encode) fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return g_encode;
+}
+
+bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                   uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                   uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    if (!get_encode()) return false;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
@@ -160,6 +164,24 @@ bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, u
         fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu stride %llu",
              static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
              (unsigned long long)row_stride_bytes);
+        return false;
+    }
+    return true;
+}
+
+bool encode_tma_3d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t d0,
+                   uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                   uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle) {
+    if (!get_encode()) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        fail(QGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", static_cast<int>(r));
         return false;
     }
     return true;
@@ -542,6 +564,68 @@ qgemm_status qgemm_w4a16_ex(const void *A_f16, int64_t lda, int64_t M, const qge
     int f;
     const qgemm_status st = epi_flags(epilogue, &f);
     return st != QGEMM_OK ? st : w4a16_impl(A_f16, lda, M, W, C_f16, ldc, f, stream);
+}
+
+qgemm_status qgemm_attention_f16(const void *Q, const void *K, const void *V, void *O, int64_t BH,
+                                 int64_t Lq, int64_t Lk, int64_t d, int64_t q_head_stride,
+                                 int64_t q_row_stride, int64_t k_head_stride, int64_t k_row_stride,
+                                 int64_t v_head_stride, int64_t v_row_stride,
+                                 int64_t o_head_stride, int64_t o_row_stride, float scale,
+                                 void *stream) {
+    if (BH < 0 || Lq < 0 || Lk < 0 || d < 0) return fail(QGEMM_ERR_INVALID_ARG, "negative shape");
+    if (BH == 0 || Lq == 0) return QGEMM_OK;
+    if (d != 128) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "head dimension must be 128 (got %lld)",
+                              (long long)d);
+    if (Lk == 0) return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "Lk = 0: softmax over no keys");
+    if (BH > 65535 || Lq > MAX_DIM || Lk > MAX_DIM)
+        return fail(QGEMM_ERR_UNSUPPORTED_SHAPE, "BH > 65535 or a length >= 2^31");
+    if (!(scale > 0.0f) || !isfinite(scale))
+        return fail(QGEMM_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (!Q || !K || !V || !O) return fail(QGEMM_ERR_INVALID_ARG, "Q, K, V or O is NULL");
+    struct View { const void *p; int64_t hs, rs, L; const char *name; };
+    const View views[4] = {{Q, q_head_stride, q_row_stride, Lq, "Q"},
+                           {K, k_head_stride, k_row_stride, Lk, "K"},
+                           {V, v_head_stride, v_row_stride, Lk, "V"},
+                           {O, o_head_stride, o_row_stride, Lq, "O"}};
+    for (const View &v : views) {
+        if (v.rs < 0 || v.hs < 0) return fail(QGEMM_ERR_INVALID_ARG, "%s: negative stride", v.name);
+        if (!aligned(v.p, 16) || v.rs % 8 || v.hs % 8)
+            return fail(QGEMM_ERR_MISALIGNED, "%s must be 16-byte aligned with strides %% 8 == 0",
+                        v.name);
+    }
+    // O's rows must not overlap: heads outside rows ([BH, Lq, d]) or rows outside heads
+    // ([Lq, BH, d], e.g. a [batch, L, heads, d] buffer)
+    const bool heads_outer = (BH == 1 || o_head_stride >= Lq * o_row_stride) && o_row_stride >= d;
+    const bool rows_outer = (Lq == 1 || o_row_stride >= BH * o_head_stride) && o_head_stride >= d;
+    if (!heads_outer && !rows_outer)
+        return fail(QGEMM_ERR_INVALID_ARG, "O strides make output rows overlap");
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    qgi::AttnArgs a;
+    a.Q = static_cast<const __half *>(Q);
+    a.K = static_cast<const __half *>(K);
+    a.V = static_cast<const __half *>(V);
+    a.O = static_cast<__half *>(O);
+    // a stride that is never stepped (one head, one row) may be anything; the tensor maps need a
+    // positive multiple of 16 bytes there
+    auto eff = [](int64_t stride, int64_t extent) { return extent > 1 || stride > 0 ? stride : 8; };
+    a.q_hs = eff(q_head_stride, BH);
+    a.k_hs = eff(k_head_stride, BH);
+    a.v_hs = eff(v_head_stride, BH);
+    a.o_hs = eff(o_head_stride, BH);
+    a.q_rs = eff(q_row_stride, Lq);
+    a.k_rs = eff(k_row_stride, Lk);
+    a.v_rs = eff(v_row_stride, Lk);
+    a.o_rs = eff(o_row_stride, Lq);
+    a.BH = (int)BH;
+    a.Lq = (int)Lq;
+    a.Lk = (int)Lk;
+    a.scale = scale;
+    bool enc = true;
+    const cudaError_t e = qgi::launch_attention(a, ctx, &enc);
+    if (!enc) return QGEMM_ERR_CUDA;
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_attention_f16 launch");
 }
 
 qgemm_status qgemm_w4a16_f16s(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,

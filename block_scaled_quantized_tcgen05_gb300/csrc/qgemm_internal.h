@@ -43,6 +43,11 @@ bool encode_tma_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, u
                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                    uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// Encode a 3-D tiled TMA descriptor (dimension 0 innermost; strides of dimensions 1 and 2).
+bool encode_tma_3d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t d0,
+                   uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                   uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle);
+
 // Kernel launchers (one per translation unit).  Arguments are already validated.
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
                          const LaunchCtx &ctx, bool *encode_ok);
@@ -82,6 +87,15 @@ cudaError_t launch_w4a16_f16s(const __half *A, int64_t lda, int M, const uint8_t
                               __half *C, int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
                            __half *Y, int64_t ldy, const LaunchCtx &ctx, bool *encode_ok);
+// Fused attention, head dimension 128: O = softmax(scale Q K^T) V per head (attention.cu).
+struct AttnArgs {
+    const __half *Q, *K, *V;
+    __half *O;
+    int64_t q_hs, q_rs, k_hs, k_rs, v_hs, v_rs, o_hs, o_rs;   // strides in elements
+    int BH, Lq, Lk;
+    float scale;
+};
+cudaError_t launch_attention(const AttnArgs &a, const LaunchCtx &ctx, bool *encode_ok);
 cudaError_t launch_dequant(const qgemm_tensor *t, float *out, const LaunchCtx &ctx);
 cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
                                  const LaunchCtx &ctx);

@@ -227,6 +227,30 @@ qgemm_status qgemm_w4a16_f16s(const void *A_f16, int64_t lda, int64_t M, const v
 qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgemm_tensor *W,
                            void *Y_f16, int64_t ldy, void *stream);
 
+/* Fused attention forward: for every head h and query row i,
+ *   O[h, i, :] = sum_j softmax_j(scale * <Q[h, i, :], K[h, j, :]>) V[h, j, :],
+ * fp16 Q, K, V and O, scores and the softmax in fp32, P = exp(s - max) rounded to fp16 for the
+ * second product, fp32 accumulation, one fp16 rounding of O.  No mask.
+ * Passage: "TensorOps: quantized matmul ...", section "FlashAttention on TensorOps (the recipe)"
+ * and "Optimize custom machine learning operations with Metal tensors", section on FlashAttention
+ * with cooperative tensors (Q K^T, the row maximum with initial value -infinity, exp of each
+ * score minus it, times V, in one kernel with the intermediate never written to memory; the
+ * softmax is normalised by its row sum, the scale is the caller's, e.g. 1/sqrt(d)).
+ *   Q, O     device fp16 [BH, Lq, d];  K, V  device fp16 [BH, Lk, d]; element (h, i, c) of X at
+ *            X + h * x_head_stride + i * x_row_stride + c (strides in elements).
+ * Requirements: d == 128; Lk >= 1; BH <= 65535; scale finite and > 0; every base 16-byte aligned
+ * and every stride a multiple of 8 (and non-negative); O's rows must not overlap: heads outside
+ * rows (row stride >= d, head stride >= Lq * row stride) or rows outside heads (head stride >= d,
+ * row stride >= BH * head stride, as in a [batch, L, heads, d] buffer).  BH == 0 or Lq == 0 does
+ * nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+qgemm_status qgemm_attention_f16(const void *Q, const void *K, const void *V, void *O, int64_t BH,
+                                 int64_t Lq, int64_t Lk, int64_t d, int64_t q_head_stride,
+                                 int64_t q_row_stride, int64_t k_head_stride, int64_t k_row_stride,
+                                 int64_t v_head_stride, int64_t v_row_stride,
+                                 int64_t o_head_stride, int64_t o_row_stride, float scale,
+                                 void *stream);
+
 /* ---------------------------------------------------------------- fused output epilogue
  * C = relu?( A*B [+ C_old] ): the product's fp32 accumulator plus, when `accumulate` is set,
  * the existing fp16 output (read before it is overwritten), then, when `relu` is set,

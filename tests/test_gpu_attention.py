@@ -1,0 +1,120 @@
+"""GPU parity of the fused attention kernel (qgemm_attention_f16) against the oracle's fp64
+softmax attention, through the C ABI.
+
+Tolerance (element-wise): |O_gpu - O| <= 2e-3 * D + 2^-24 with D = sum_j p_j |v_j| / sum_j p_j,
+the magnitude the weighted average is formed from.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_quantized_tcgen05_gb300 as q
+from block_scaled_quantized_tcgen05_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+REL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from block_scaled_quantized_tcgen05_gb300 import build
+    build.build()
+    q.load_library()
+    q.qgemm_set_wait_timeout_ns(2_000_000_000)
+    return torch.device("cuda:0")
+
+
+def _check(got, res, orc, what):
+    code = q.qgemm_poll_device_error()
+    assert code == 0, f"{what}: a device wait timed out (error word {code:#x})"
+    g = got.float().cpu().numpy().reshape(res.C.shape)
+    ok, worst, info = orc.within_tolerance(g, res, REL)
+    assert ok, f"{what}: {info}"
+    return worst
+
+
+def _run(d, dev, layout="bhld"):
+    Q, K, V = d["q"].to(dev), d["k"].to(dev), d["v"].to(dev)
+    O = torch.full_like(Q, float("nan"))
+    q.qgemm_attention(Q, K, V, O, scale=d["scale"])
+    return O
+
+
+@pytest.mark.parametrize("BH,Lq,Lk,q_std", [(2, 128, 128, 1.0), (3, 200, 300, 1.0),
+                                            (1, 1, 1, 1.0), (2, 257, 1000, 2.0),
+                                            (4, 512, 640, 4.0), (1, 384, 2048, 8.0)])
+def test_attention_matches_oracle(dev, orc, BH, Lq, Lk, q_std):
+    d = synth.attention_inputs(BH, Lq, Lk, 128, seed=BH + Lq + Lk, q_std=q_std)
+    O = _run(d, dev)
+    res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"])
+    _check(O, res, orc, f"attention {BH}x{Lq}x{Lk} q_std={q_std}")
+
+
+def test_attention_rising_maximum_rescales(dev, orc):
+    """Keys whose norm grows along the sequence: every key tile raises the row maximum by more
+    than 2^8, so the output accumulator is rescaled on every tile."""
+    BH, Lq, Lk = 2, 256, 1024
+    d = synth.attention_inputs(BH, Lq, Lk, 128, seed=71)
+    growth = torch.linspace(0.2, 3.0, Lk).reshape(1, Lk, 1)
+    d["k"] = (d["k"].float() * growth).to(torch.float16)
+    d["q"] = (d["q"].float() * 2.0).to(torch.float16)
+    O = _run(d, dev)
+    res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"])
+    _check(O, res, orc, "attention rising maximum")
+
+
+def test_attention_single_key_is_exact(dev):
+    """One key: every softmax weight is exactly 1 and O is that value row, bit for bit."""
+    d = synth.attention_inputs(3, 130, 1, 128, seed=72)
+    O = _run(d, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(O.cpu(), d["v"].expand(3, 130, 128))
+
+
+def test_attention_interleaved_heads_layout(dev, orc):
+    """[L, heads, d] buffers (row stride = heads * d, head stride = d) for Q, K, V and O."""
+    H, Lq, Lk = 4, 192, 320
+    d = synth.attention_inputs(H, Lq, Lk, 128, seed=73, q_std=2.0)
+    Qi = d["q"].transpose(0, 1).contiguous().to(dev)     # [Lq, H, d]
+    Ki = d["k"].transpose(0, 1).contiguous().to(dev)
+    Vi = d["v"].transpose(0, 1).contiguous().to(dev)
+    Oi = torch.full((Lq, H, 128), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_attention(Qi.transpose(0, 1), Ki.transpose(0, 1), Vi.transpose(0, 1),
+                      Oi.transpose(0, 1), scale=d["scale"])
+    res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"])
+    _check(Oi.transpose(0, 1), res, orc, "attention interleaved heads")
+
+
+def test_attention_errors(dev):
+    x = torch.zeros(1, 16, 64, dtype=torch.float16, device=dev)
+    with pytest.raises(q.QGemmError) as ei:
+        q.qgemm_attention(x, x, x, x.clone())
+    assert ei.value.name == "QGEMM_ERR_UNSUPPORTED_SHAPE"          # d != 128
+    y = torch.zeros(1, 16, 128, dtype=torch.float16, device=dev)
+    k0 = torch.zeros(1, 0, 128, dtype=torch.float16, device=dev)
+    with pytest.raises(q.QGemmError) as ei:
+        q.qgemm_attention(y, k0, k0, y.clone())
+    assert ei.value.name == "QGEMM_ERR_UNSUPPORTED_SHAPE"          # Lk = 0
+    with pytest.raises(q.QGemmError) as ei:
+        q.qgemm_attention(y, y, y, y.clone(), scale=-1.0)
+    assert ei.value.name == "QGEMM_ERR_INVALID_ARG"
+    big = torch.zeros(1, 16, 136, dtype=torch.float16, device=dev)
+    with pytest.raises(q.QGemmError) as ei:
+        q.qgemm_attention(big[:, :, 4:132], y, y, y.clone())           # base not 16-byte aligned
+    assert ei.value.name == "QGEMM_ERR_MISALIGNED"
+
+
+def test_attention_full_size_sampled(dev, orc):
+    """32 heads x 4096 x 4096 x 128 (the prefill workload), oracle on sampled rows."""
+    d = synth.workload("attn_prefill")
+    O = _run(d, dev)
+    rng = np.random.default_rng(4)
+    heads = np.concatenate([[0, 31], rng.integers(0, 32, 30)])
+    rows = np.concatenate([[0, 4095], rng.integers(0, 4096, 30)])
+    res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"],
+                        heads=heads, qrows=rows)
+    got = O[torch.from_numpy(heads).to(dev), torch.from_numpy(rows).to(dev)]
+    _check(got, res, orc, "attention 32x4096x4096 sampled")
