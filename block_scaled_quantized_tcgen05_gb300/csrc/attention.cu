@@ -71,6 +71,67 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 2^x on the FMA pipe, for x <= 9 (larger x is never formed here): x = n + f with n the nearest
+// integer (added to a float's exponent field by the round-to-nearest of x + 1.5 * 2^23) and
+// f in [-1/2, 1/2]; 2^f by a cubic fitted here for least maximum relative error on that interval
+// (7.5e-5, below the half-ulp 2.4e-4 of the fp16 the result is rounded to).  Inputs below -126
+// give 2^-126 or less, where an exact value would be at most that.
+__device__ __forceinline__ float ex2_poly(float x) {
+    x = fmaxf(x, -126.0f);
+    const float t = x + 12582912.0f;                  // 1.5 * 2^23: rounds x to an integer
+    const int n = __float_as_int(t) - 0x4B400000;
+    const float f = x - (t - 12582912.0f);
+    float p = fmaf(0.0551715f, f, 0.24261096f);
+    p = fmaf(p, f, 0.69326099f);
+    p = fmaf(p, f, 0.99992808f);
+    return __int_as_float(__float_as_int(p) + (n << 23));
+}
+
+// One key tile of one query row: the running maximum m (log2 units) is given; writes
+// P = 2^(s c - m) as fp16 pairs into TMEM columns scol .. scol + 63 of this warp's lanes and
+// returns the row sum of P.  One pair in four is exponentiated on the FMA pipe, the rest by
+// ex2.approx, so that neither pipe alone sets the pace.  MASK: keys >= valid give P = 0.
+template <bool MASK>
+__device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int valid, float c,
+                                              float m, uint32_t scol) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {                      // 64 keys -> 32 packed columns
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int k0 = 64 * h + 2 * i;
+            const float x0 = fmaf(__uint_as_float(v[k0]), c, -m);
+            const float x1 = fmaf(__uint_as_float(v[k0 + 1]), c, -m);
+            float p0 = (i & 3) == 3 ? ex2_poly(x0) : ex2_approx(x0);
+            float p1 = (i & 3) == 3 ? ex2_poly(x1) : ex2_approx(x1);
+            if (MASK) {
+                p0 = k0 < valid ? p0 : 0.0f;
+                p1 = k0 + 1 < valid ? p1 : 0.0f;
+            }
+            acc[i & 3] += p0 + p1;
+            pk[i] = pack_f16x2(p0, p1);
+        }
+        tmem_st_32x32b_x32(scol + 32 * h, pk);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// Row maximum of the tile's raw scores; MASK: only keys < valid count.
+template <bool MASK>
+__device__ __forceinline__ float tile_max(const uint32_t (&v)[128], int valid) {
+    float mx[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+        const float x = __uint_as_float(v[i]);
+        mx[i & 7] = fmaxf(mx[i & 7], MASK ? (i < valid ? x : -INFINITY) : x);
+    }
+    return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, __half *__restrict__ O, int64_t o_hs,
@@ -239,11 +300,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 tmem_ld_32x32b_x32(scol + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
             tmem_wait_ld();
             const int valid = Lk - j * BKV;                   // keys of this tile inside Lk
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < BKV; ++i)
-                if (i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
-            const float mx2 = mx * c_log2;
+            const bool full = valid >= BKV;
+            const float mx2 = (full ? tile_max<false>(v, valid) : tile_max<true>(v, valid)) * c_log2;
             // raise the running maximum only when this tile exceeds it by more than 2^8
             const bool need = mx2 > m_used + 8.0f;
             if (__any_sync(0xFFFFFFFFu, need)) {
@@ -272,21 +330,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 }
                 m_used = m_new;
             }
-            float sum = 0.0f;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {                      // 64 keys -> 32 packed columns
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int k0 = 64 * h + 2 * i;
-                    const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(v[k0]), c_log2, -m_used)) : 0.0f;
-                    const float p1 = k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(v[k0 + 1]), c_log2, -m_used)) : 0.0f;
-                    sum += p0 + p1;
-                    pk[i] = pack_f16x2(p0, p1);
-                }
-                tmem_st_32x32b_x32(scol + 32 * h, pk);
-            }
-            l += sum;
+            l += full ? softmax_tile<false>(v, valid, c_log2, m_used, scol)
+                      : softmax_tile<true>(v, valid, c_log2, m_used, scol);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
