@@ -9,11 +9,12 @@
 //
 // The GB300 form of that recipe:
 //   * one CTA per (head, 128 query rows), head dimension 128; K and V tiles of 128 keys arrive
-//     by TMA (3-D maps: d, row, head) into three stages of shared memory each; a K stage is
-//     released when its scores are done, a V stage when its P V is done;
+//     by TMA (3-D maps: d, row, head) into three stages of shared memory each, from two
+//     producer threads (K runs ahead of V); a K stage is released when its scores are done, a
+//     V stage when its P V is done;
 //   * S = Q K^T for a key tile is one tcgen05.mma chain (M = 128 queries, N = 128 keys,
-//     K = 128) into one of two 128-column TMEM buffers, so the tensor core computes the next
-//     tile's scores while the current one is in softmax;
+//     K = 128) into one of three 128-column TMEM buffers: the scores of tile j + 3 are issued
+//     right after P V of tile j, so the softmax never waits for a P V -> S chain to drain;
 //   * a TMEM lane is a query row, so each softmax thread owns a whole row: it reads its 128
 //     scores into registers (tcgen05.ld), and the row maximum, the exponentials and the row sum
 //     are in-register loops -- no exchange at all;
@@ -26,7 +27,8 @@
 //     write back, after the previous P V has completed) is rare;
 //   * after the last tile each thread divides its row of O by its row sum and stores it.
 // Keys past Lk (TMA zero fill) are masked to -inf; query rows past Lq are computed and dropped.
-// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 2-5 softmax and epilogue.
+// Roles: warp 0 TMA producer of Q and K, warp 1 MMA issuer (one thread), warps 2-5 softmax and
+// epilogue, warp 6 TMA producer of V.
 // Every wait is bounded; on a timeout the kernel records the error bit, stops issuing work,
 // waits for its MMAs, frees TMEM and returns.
 #include "qgemm_common.cuh"
@@ -41,10 +43,11 @@ constexpr int BQ = 128;                 // query rows per CTA
 constexpr int BKV = 128;                // keys per tile
 constexpr int HD = 128;                 // head dimension
 constexpr int KV_STAGES = 3;
-constexpr int THREADS = 32 * 6;
+constexpr int THREADS = 32 * 7;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL0 = 0;          // two score buffers of 128 columns
-constexpr uint32_t O_COL = 256;         // output accumulator, 128 columns
+constexpr int NSB = 3;                  // score buffers of 128 columns from column 0
+constexpr uint32_t S_COL0 = 0;
+constexpr uint32_t O_COL = 128 * NSB;   // output accumulator, 128 columns
 
 constexpr uint32_t HALF_BYTES = 128 * 128;            // 128 rows x 64 halves (one swizzle span)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;       // 128 rows x 128 halves
@@ -52,9 +55,9 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE_BYTES;
-// q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done[2],
-// drain, then the TMEM slot
-constexpr int NBARS = 1 + 4 * KV_STAGES + 6 + 1;
+// q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NSB], p_full[NSB],
+// pv_done[NSB], drain, then the TMEM slot
+constexpr int NBARS = 1 + 4 * KV_STAGES + 3 * NSB + 1;
 constexpr uint32_t OFF_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -151,9 +154,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     auto k_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 2 * KV_STAGES + s); };
     auto v_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 3 * KV_STAGES + s); };
     auto s_full = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + b); };
-    auto p_full = [&](int b) { return sb + OFF_BAR + 8u * (3 + 4 * KV_STAGES + b); };
-    auto pv_done = [&](int b) { return sb + OFF_BAR + 8u * (5 + 4 * KV_STAGES + b); };
-    const uint32_t drain_bar = sb + OFF_BAR + 8u * (7 + 4 * KV_STAGES);
+    auto p_full = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + NSB + b); };
+    auto pv_done = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + 2 * NSB + b); };
+    const uint32_t drain_bar = sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + 3 * NSB);
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
 
     if (threadIdx.x == 0) {
@@ -164,7 +167,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             mbar_init(k_empty(s), 1);
             mbar_init(v_empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NSB; ++b) {
             mbar_init(s_full(b), 1);
             mbar_init(p_full(b), 4);     // one arrival per softmax warp
             mbar_init(pv_done(b), 1);
@@ -185,7 +188,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t tmem_base = *slot;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- producer
+        // ------------------------------------------------------ producer of Q and K
         if (lane == 0) {
             bool ok = true;
             mbar_arrive_expect_tx(q_full, TILE_BYTES);
@@ -194,36 +197,45 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             int issued = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int st = j % KV_STAGES;
-                const uint32_t free_par = ((j / KV_STAGES) & 1) ^ 1;
-                if (!mbar_wait(k_empty(st), free_par, timeout_ns)) {
+                if (!mbar_wait(k_empty(st), ((j / KV_STAGES) & 1) ^ 1, timeout_ns)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sk = sb + OFF_K + st * TILE_BYTES;
-                const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
                 mbar_arrive_expect_tx(k_full(st), TILE_BYTES);
                 tma_load_3d(sk, &tmK, k_full(st), 0, j * BKV, head);
                 tma_load_3d(sk + HALF_BYTES, &tmK, k_full(st), 64, j * BKV, head);
-                if (!mbar_wait(v_empty(st), free_par, timeout_ns)) {
+                ++issued;
+            }
+            if (!ok) atomicOr(err, ERR_PRODUCER);
+            // no copy may be in flight when the CTA exits
+            bool drained = mbar_wait(q_full, 0, timeout_ns);
+            for (int i = max(0, issued - KV_STAGES); i < issued && drained; ++i)
+                drained = mbar_wait(k_full(i % KV_STAGES), (i / KV_STAGES) & 1, timeout_ns);
+            if (!drained) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ----------------------------------------------------------- producer of V
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % KV_STAGES;
+                if (!mbar_wait(v_empty(st), ((j / KV_STAGES) & 1) ^ 1, timeout_ns)) {
                     ok = false;
-                    // the K copy just issued must land before the CTA exits
-                    if (!mbar_wait(k_full(st), (j / KV_STAGES) & 1, timeout_ns))
-                        atomicOr(err, ERR_DRAIN);
                     break;
                 }
+                const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
                 mbar_arrive_expect_tx(v_full(st), TILE_BYTES);
                 tma_load_3d(sv, &tmV, v_full(st), 0, j * BKV, head);
                 tma_load_3d(sv + HALF_BYTES, &tmV, v_full(st), 64, j * BKV, head);
                 ++issued;
             }
             if (!ok) atomicOr(err, ERR_PRODUCER);
-            // no copy may be in flight when the CTA exits
-            bool drained = mbar_wait(q_full, 0, timeout_ns);
-            for (int i = max(0, issued - KV_STAGES); i < issued && drained; ++i) {
-                const uint32_t par = (i / KV_STAGES) & 1;
-                drained = mbar_wait(k_full(i % KV_STAGES), par, timeout_ns) &&
-                          mbar_wait(v_full(i % KV_STAGES), par, timeout_ns);
-            }
+            bool drained = true;
+            for (int i = max(0, issued - KV_STAGES); i < issued && drained; ++i)
+                drained = mbar_wait(v_full(i % KV_STAGES), (i / KV_STAGES) & 1, timeout_ns);
             if (!drained) atomicOr(err, ERR_DRAIN);
         }
         __syncwarp();
@@ -233,7 +245,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const uint64_t qdesc = smem_desc(sb + OFF_Q, 16, 1024, SWZ_128B);
             bool ok = mbar_wait(q_full, 0, timeout_ns);
             auto issue_s = [&](int j) -> bool {
-                const int b = j & 1, st = j % KV_STAGES;
+                const int b = j % NSB, st = j % KV_STAGES;
                 if (!mbar_wait(k_full(st), (j / KV_STAGES) & 1, timeout_ns)) return false;
                 tc_fence_after();
                 const uint64_t kdesc = smem_desc(sb + OFF_K + st * TILE_BYTES, 16, 1024, SWZ_128B);
@@ -249,8 +261,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
-                const int b = j & 1, st = j % KV_STAGES;
-                if (!mbar_wait(p_full(b), (j >> 1) & 1, timeout_ns)) return false;
+                const int b = j % NSB, st = j % KV_STAGES;
+                if (!mbar_wait(p_full(b), (j / NSB) & 1, timeout_ns)) return false;
                 if (!mbar_wait(v_full(st), (j / KV_STAGES) & 1, timeout_ns)) return false;
                 tc_fence_after();
                 const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
@@ -267,13 +279,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 tc_commit(pv_done(b));
                 return true;
             };
-            if (ok && nkv > 0) ok = issue_s(0);
+            // scores run NSB tiles ahead: S(0 .. NSB-1), then P V(j) followed by S(j + NSB),
+            // which reuses the buffer P V(j) has just read (the tensor pipe keeps issue order)
+            for (int j = 0; j < NSB && j < nkv && ok; ++j) ok = issue_s(j);
             for (int j = 0; j < nkv && ok; ++j) {
-                if (j + 1 < nkv && !issue_s(j + 1)) {
+                if (!issue_pv(j)) {
                     ok = false;
                     break;
                 }
-                if (!issue_pv(j)) ok = false;
+                if (j + NSB < nkv && !issue_s(j + NSB)) ok = false;
             }
             if (!ok) atomicOr(err, ERR_MMA);
             tc_commit(drain_bar);
@@ -287,8 +301,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         float m_used = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1;
-            if (!mbar_wait(s_full(b), (j >> 1) & 1, timeout_ns)) {
+            const int b = j % NSB;
+            if (!mbar_wait(s_full(b), (j / NSB) & 1, timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -308,7 +322,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 const float m_new = fmaxf(m_used, mx2);
                 if (j > 0) {
                     // the previous P V must have completed before O is rescaled
-                    if (!mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, timeout_ns)) {
+                    if (!mbar_wait(pv_done((j - 1) % NSB), ((j - 1) / NSB) & 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -341,7 +355,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (lane == 0) atomicOr(err, ERR_EPILOGUE);
         } else if (nkv > 0) {
             const int last = nkv - 1;
-            if (!mbar_wait(pv_done(last & 1), (last >> 1) & 1, timeout_ns)) {
+            if (!mbar_wait(pv_done(last % NSB), (last / NSB) & 1, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
             } else {
                 tc_fence_after();
