@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
     "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
-    "qgemm_mxfp8", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_mxfp8", "qgemm_mxfp8_host", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout",
 ]
@@ -70,6 +70,7 @@ def load_library():
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_mxfp4": (S, [P, P, P, I64, P]),
+        "qgemm_mxfp8_host": (S, [P, P, P, I64, P]),
         "qgemm_attention_f16": (S, [P, P, P, P] + [I64] * 12 + [ctypes.c_float, P]),
         "qgemm_w4a16_f16s": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64, P]),
         "qgemm_w4a16_f16s_ex": (S, [P, I64, I64, P, I64, P, I64, I64, I64, P, I64,
@@ -198,6 +199,17 @@ def qgemm_mxfp4(A: QTensor, B: QTensor, C, stream=None):
     """C = A B^T with E2M1 operands (UE8M0 scale per 32 along K), fp32 accumulation, fp16 out."""
     _check(load_library().qgemm_mxfp4(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
            "qgemm_mxfp4")
+    return C
+
+
+def qgemm_mxfp8_host(A: QTensor, B: QTensor, C, stream=None):
+    """qgemm_mxfp8 with A, B (views of host tensors, preferably pinned) and C (a host fp16 tensor)
+    in host memory: uploads, computes and downloads with the three overlapped; asynchronous on
+    ``stream`` (synchronise it before reading C)."""
+    if C.is_cuda:
+        raise ValueError("C must be a host tensor")
+    _check(load_library().qgemm_mxfp8_host(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
+           "qgemm_mxfp8_host")
     return C
 
 

@@ -163,6 +163,24 @@ qgemm_status qgemm_mxfp8_noalloc(const qgemm_tensor *A, const qgemm_tensor *B, v
 qgemm_status qgemm_mxfp4(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                          void *stream);
 
+/* qgemm_mxfp8 on host memory: A and B are views whose data and scale planes are in host memory
+ * (page-locked memory lets the copies run asynchronously; pageable memory works but the copies
+ * then stage through the driver), C is host fp16 [M, N] with row stride ldc elements.  The pages
+ * have no counterpart: this is the end-to-end form of the product for a caller whose operands
+ * live on the host.  One call uploads both operands, runs the GEMM of qgemm_mxfp8 and downloads
+ * C, overlapping the three: B first, then A in row chunks; each chunk's product starts when that
+ * chunk has landed and each finished chunk of C is downloaded while the next one computes.
+ * Ordering: everything is ordered after the work already on `stream`, and `stream` completes
+ * only after C is on the host; calls on one stream therefore run one after another, while calls
+ * on different streams overlap (the uploads of one with the downloads of another).  The host
+ * planes must not be modified, nor C read, before `stream` has completed the call.
+ * Device memory: two buffer sets per device, grown to the largest shape seen, held until exit
+ * (A + B + scales + C: 272 MB each at M = N = K = 8192), plus the scratch of qgemm_mxfp8.
+ * Requirements and errors: as qgemm_mxfp8 (no alignment rule for the host planes); CUDA also for
+ * a failed copy or allocation. */
+qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
+                              void *stream);
+
 /* fp16 GEMM: C[M, N] = fp16_rn(A[M, K] @ B[K, N]), fp32 accumulation, all row-major fp16.
  * Passage: "TensorOps: quantized matmul ...", "VALIDATED ON M4 MAX" (kernel M0, half x half ->
  * half) and "TileLang Metal Backend Internals", section 1 (fp16 input, fp32 accumulation, fp16

@@ -203,3 +203,20 @@ def test_w4a16_f16s_rejects_before_launch(lib):
     assert call(M=0) == 0 and call(N=0) == 0                   # empty output: no-op
     assert lib.qgemm_w4a16_f16s_ex(A, 256, 16, W, 128, S, 8, 64, 256, C, 64,
                                    ctypes.byref(q.Epilogue(0, 5)), None) == 1
+
+
+def test_mxfp8_host_rejects_before_any_cuda_call(lib):
+    """qgemm_mxfp8_host validates its views and output before it touches CUDA (no GPU here)."""
+    _, a = _create(lib, q.E4M3, 128, 256, FAKE, 256, FAKE + 65536, 8)
+    _, b2 = _create(lib, q.E4M3, 256, 128, FAKE, 128, FAKE + 65536, 4)
+    _, b = _create(lib, q.E4M3, 256, 256, FAKE, 256, FAKE + 65536, 8)
+    _, w8 = _create(lib, q.INT8, 256, 256, FAKE, 256, FAKE + 65536, 8)
+    C = ctypes.c_void_p(FAKE + (1 << 24))
+    assert lib.qgemm_mxfp8_host(a, b2, C, 256, None) == 1      # K mismatch
+    assert lib.qgemm_mxfp8_host(a, w8, C, 256, None) == 4      # dtype
+    assert lib.qgemm_mxfp8_host(a, b, C, 128, None) == 1       # ldc < N
+    assert lib.qgemm_mxfp8_host(a, b, None, 256, None) == 1    # no output
+    _, e0 = _create(lib, q.E4M3, 0, 256, FAKE, 256, FAKE + 65536, 8)
+    assert lib.qgemm_mxfp8_host(e0, b, C, 256, None) == 0      # empty output: nothing to do
+    for t in (a, b2, b, w8, e0):
+        lib.qgemm_destroy_tensor(t)
