@@ -378,7 +378,7 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2: each kernel's inputs are evicted by the rest of "
                          "the step (>129 MB between reuses); GEMV weights rotate over 2 copies"},
         "roofline": None if mx_tflops is None else {
-            "kernel": "qgemm_mxfp8 = sf_pack_kernel + mxfp8_pair_kernel", "bound": "tensor",
+            "kernel": "qgemm_mxfp8 = sf_pack_kernel<1> + mx_pair_kernel<FmtE4M3>", "bound": "tensor",
             "achieved": round(mx_tflops, 1), "peak": round(fp8_peak_sust, 1),
             "unit": "TFLOP/s", "frac": round(mx_tflops / fp8_peak_sust, 4),
             "peak_source": f"{peak_kind} bf16 sustained x 2 (nominal fp8/bf16 ratio)",
