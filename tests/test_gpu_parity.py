@@ -218,8 +218,9 @@ def test_mxfp8_full_size_sampled(dev, orc):
 
 
 # ------------------------------------------------------------------------------- fp16
+# (1024, 4864, 128): exactly one wave of 256 x 256 pair tiles on 76 pairs
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 328, 200), (96, 64, 512),
-                                   (384, 512, 1024)])
+                                   (384, 512, 1024), (1024, 4864, 128)])
 def test_gemm_f16_matches_oracle(dev, orc, M, N, K):
     d = synth.f16_inputs(M, N, K, seed=M * 7 + N)
     C = torch.empty(M, N, dtype=torch.float16, device=dev)
