@@ -136,6 +136,7 @@ struct SfPackOperand {
     int kcols;               // K / 32
     int rbp;                 // padded count of 128-row blocks (even)
     uint8_t *out;            // [KT][rbp][W][32 lines][16 bytes]
+    int vec;                 // scales and lds 16-byte aligned: 16-byte loads
 };
 
 // grid (max rbp, ceil(KT W / 8), 2 operands) x 256 threads.  Stage 128 rows x 32 scale bytes
@@ -150,14 +151,29 @@ sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     if (rb >= op.rbp) return;
     const int kt0 = blockIdx.y * PACK_KT;
     const int t = threadIdx.x;
+    if (op.vec && kt0 * 4 + 32 <= op.kcols) {
+        // 128 rows x 32 bytes as 256 16-byte loads: thread t takes half t & 1 of row t / 2
+        const int row = t >> 1, half = t & 1;
+        const int r = rb * 128 + row;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < op.rows)
+            v = __ldg(reinterpret_cast<const uint4 *>(op.scales + static_cast<int64_t>(r) * op.lds +
+                                                      kt0 * 4 + 16 * half));
+        uint32_t *dst = reinterpret_cast<uint32_t *>(tile + row * PACK_ROW + 16 * half);
+        dst[0] = v.x;
+        dst[1] = v.y;
+        dst[2] = v.z;
+        dst[3] = v.w;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int idx = t + 256 * j;              // 128 rows x 32 bytes
-        const int row = idx >> 5, col = idx & 31;
-        const int r = rb * 128 + row, c = kt0 * 4 + col;
-        uint8_t v = 0;
-        if (r < op.rows && c < op.kcols) v = op.scales[static_cast<int64_t>(r) * op.lds + c];
-        tile[row * PACK_ROW + col] = v;
+        for (int j = 0; j < 16; ++j) {
+            const int idx = t + 256 * j;              // 128 rows x 32 bytes
+            const int row = idx >> 5, col = idx & 31;
+            const int r = rb * 128 + row, c = kt0 * 4 + col;
+            uint8_t v = 0;
+            if (r < op.rows && c < op.kcols) v = op.scales[static_cast<int64_t>(r) * op.lds + c];
+            tile[row * PACK_ROW + col] = v;
+        }
     }
     __syncthreads();
     const int ktl = t >> 5, i = t & 31;
@@ -431,8 +447,11 @@ cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
 
-    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA};
-    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB};
+    auto vec16 = [](const qgemm_tensor *t) {
+        return (reinterpret_cast<uintptr_t>(t->scales) % 16 == 0 && t->lds % 16 == 0) ? 1 : 0;
+    };
+    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA, vec16(A)};
+    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB, vec16(B)};
     const dim3 pgrid(static_cast<unsigned>(rbpA > rbpB ? rbpA : rbpB),
                      static_cast<unsigned>((KT * F::W + PACK_KT - 1) / PACK_KT), 2);
     sf_pack_kernel<F::W><<<pgrid, 256, 0, ctx.stream>>>(pa, pb, KT);
