@@ -11,13 +11,17 @@
 //
 // Streaming: a producer warp keeps S stages in flight, each one TMA box of 64 weight rows x 128
 // bytes of K plus the matching 128-wide slice of X, both with the 128-byte swizzle so that the
-// consumers' fragment reads from shared memory are free of bank conflicts.  Four consumer warps
-// own 16 weight rows each.  Per 32-element block a lane quad (t = 0..3) takes 8 consecutive
-// int8 of rows g and g+8, converts them exactly to fp16 with a byte-permute into the mantissa of
-// 1024 (a published integer-to-half technique), and feeds two k16 MMAs; the 32 k of a block are
-// permuted identically for weights and activations, so the dot product is unchanged.  The
-// block's fp32 partial sum is scaled by 2^(e-127) (exact) and added to the running fp32 sum, so
-// every UE8M0 scale is handled exactly.  CTAs are persistent over 64-row blocks.
+// consumers' fragment reads from shared memory are free of bank conflicts.  Work is split along K
+// inside a stage: consumer warp w takes 32-block w of every stage for all 64 rows, as four 16-row
+// MMA fragments that share one activation fragment (each activation byte is read from shared
+// memory once per stage instead of once per row fragment).  Per fragment a lane quad (t = 0..3)
+// takes 8 consecutive int8 of rows g and g+8, converts them exactly to fp16 with a byte-permute
+// into the mantissa of 1024 (a published integer-to-half technique), and feeds two k16 MMAs; the
+// 32 k of a block are permuted identically for weights and activations, so the dot product is
+// unchanged.  The block's fp32 partial sum is scaled by 2^(e-127) (exact) and added to the warp's
+// running fp32 sum, so every UE8M0 scale is handled exactly.  At the end of a row block the four
+// warps' sums are added in a fixed order (warp 0, 1, 2, 3) through shared memory, so results do
+// not depend on timing.  CTAs are persistent over 64-row blocks.
 #include <cuda_fp16.h>
 
 #include "qgemm_common.cuh"
@@ -30,19 +34,22 @@ using namespace qg;
 
 constexpr int CONSUMERS = 4;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
-constexpr int ROWS = CONSUMERS * 16;        // weight rows per CTA iteration
-constexpr int KC = 128;                     // K per stage (bytes of int8)
-constexpr int STAGES = 6;
-constexpr int SCALE_AHEAD = 3;              // scale words prefetched this many chunks ahead
+constexpr int ROWS = 64;                    // weight rows per CTA iteration (4 fragments of 16)
+constexpr int KC = 128;                     // K per stage (bytes of int8) = four 32-blocks
 
 template <int NH>
 struct GCfg {
+    static constexpr int STAGES = NH == 1 ? 6 : 5;            // three CTAs fit on an SM either way
     static constexpr uint32_t W_BYTES = ROWS * KC;            // 8 KB
     static constexpr uint32_t X_HALF = 8 * NH * 128;          // one 64-wide half of the X slice
     static constexpr uint32_t X_BYTES = 2 * X_HALF;
     static constexpr uint32_t STAGE = W_BYTES + X_BYTES;
-    static constexpr uint32_t OFF_BAR = STAGES * STAGE;
-    static constexpr uint32_t SMEM = OFF_BAR + 2 * STAGES * 8 + 1024;
+    static constexpr uint32_t OFF_BAR = STAGES * STAGE;       // full[S], empty[S]
+    static constexpr uint32_t OFF_RBAR = OFF_BAR + 2 * STAGES * 8;   // reduction full, empty
+    static constexpr uint32_t OFF_RED = OFF_RBAR + 16;
+    // partial sums handed between warps, one activation half at a time: [warp][3 fragments][4][lane]
+    static constexpr uint32_t RED_BYTES = CONSUMERS * 3 * 4 * 32 * 4;
+    static constexpr uint32_t SMEM = OFF_RED + RED_BYTES + 1024;
 };
 
 // 4 int8 (one 32-bit word) -> two fp16x2 holding the exact integers (q0,q1), (q2,q3).
@@ -56,7 +63,7 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t
 }
 
 // Not volatile: a pure function of its registers, so the compiler may interleave the MMAs of
-// independent 32-blocks.
+// independent fragments.
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1, const float (&c)[4]) {
     asm(
@@ -67,16 +74,27 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
           "f"(c[2]), "f"(c[3]));
 }
 
-// Four scale bytes (blocks 4c .. 4c+3 of a row) as one little-endian word; bytes past the row's
-// last block read as 127 (2^0; their data is zero-filled).
-__device__ __forceinline__ uint32_t scale_word(const uint8_t *row, int c, int nblk, bool vec) {
-    const int b0 = 4 * c;
-    if (vec && b0 + 4 <= nblk) return __ldg(reinterpret_cast<const uint32_t *>(row + b0));
-    uint32_t w = 0;
+// Scale bytes of blocks 16 G .. 16 G + 15 of one row (the four 32-blocks of four consecutive
+// stages) as four little-endian words; bytes past the row's last block read as 127 (2^0; their
+// data is zero-filled).  vec: 2 = the row is 16-byte aligned, 1 = 4-byte aligned, 0 = bytes.
+__device__ __forceinline__ uint4 scale_group(const uint8_t *row, int G, int nblk, int vec) {
+    const int b0 = 16 * G;
+    if (vec == 2 && b0 + 16 <= nblk) return __ldg(reinterpret_cast<const uint4 *>(row + b0));
+    uint32_t v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w |= static_cast<uint32_t>(b0 + i < nblk ? __ldg(row + b0 + i) : 127) << (8 * i);
-    return w;
+    for (int j = 0; j < 4; ++j) {
+        const int bj = b0 + 4 * j;
+        if (vec >= 1 && bj + 4 <= nblk) {
+            v[j] = __ldg(reinterpret_cast<const uint32_t *>(row + bj));
+        } else {
+            uint32_t x = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                x |= static_cast<uint32_t>(bj + i < nblk ? __ldg(row + bj + i) : 127) << (8 * i);
+            v[j] = x;
+        }
+    }
+    return make_uint4(v[0], v[1], v[2], v[3]);
 }
 
 // True if some byte of w is 0x00 or 0xFF (the scale codes the shift decode does not cover).
@@ -87,63 +105,6 @@ __device__ __forceinline__ bool has_special_byte(uint32_t w) {
     return (z | f) != 0u;
 }
 
-// 2^(byte b of w - 127) as fp32 for bytes 1..254: the byte moved into the exponent field.
-template <int B>
-__device__ __forceinline__ float scale_fast(uint32_t w) {
-    const uint32_t bits = (B < 3 ? (w << (23 - 8 * B)) : (w >> 1)) & 0x7F800000u;
-    return __uint_as_float(bits);
-}
-
-// One 64-row x 128-k stage: four 32-blocks, each two MMAs per activation half, the block's fp32
-// partial sum scaled by its power of two.
-template <int NH, bool EXACT>
-__device__ __forceinline__ void consume_stage(float (&acc)[NH][4], const uint8_t *st,
-                                              const uint8_t *xs, int r0, uint32_t sw, int g, int t,
-                                              uint32_t e0w, uint32_t e1w) {
-    using G = GCfg<NH>;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        // weights: bytes 32 b + 8 t .. +8 of rows r0, r0 + 8 (16-byte chunk 2b + t/2)
-        const uint32_t wc = ((static_cast<uint32_t>(2 * b + (t >> 1)) ^ sw) << 4) +
-                            static_cast<uint32_t>((t & 1) * 8);
-        const uint2 wa = *reinterpret_cast<const uint2 *>(st + r0 * 128 + wc);
-        const uint2 wb = *reinterpret_cast<const uint2 *>(st + (r0 + 8) * 128 + wc);
-        // activations: halves 32 b + 8 t .. +8 of X rows g (and g + 8)
-        const uint8_t *xhalf = xs + static_cast<uint32_t>(b >> 1) * G::X_HALF;
-        const uint32_t xc = static_cast<uint32_t>(4 * (b & 1) + t);
-        const uint32_t xo = (xc ^ static_cast<uint32_t>(g & 7)) << 4;
-        const uint4 xa = *reinterpret_cast<const uint4 *>(xhalf + g * 128 + xo);
-        uint32_t a0[4], a1[4];
-        i8x4_to_f16x2(wa.x, a0[0], a0[2]);
-        i8x4_to_f16x2(wb.x, a0[1], a0[3]);
-        i8x4_to_f16x2(wa.y, a1[0], a1[2]);
-        i8x4_to_f16x2(wb.y, a1[1], a1[3]);
-        float sa, sbv;
-        if constexpr (EXACT) {
-            sa = ue8m0_to_f32((e0w >> (8 * b)) & 0xFF);
-            sbv = ue8m0_to_f32((e1w >> (8 * b)) & 0xFF);
-        } else {
-            sa = b == 0 ? scale_fast<0>(e0w) : b == 1 ? scale_fast<1>(e0w)
-                                             : b == 2 ? scale_fast<2>(e0w) : scale_fast<3>(e0w);
-            sbv = b == 0 ? scale_fast<0>(e1w) : b == 1 ? scale_fast<1>(e1w)
-                                              : b == 2 ? scale_fast<2>(e1w) : scale_fast<3>(e1w);
-        }
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            uint4 xv = xa;
-            if (h == 1) xv = *reinterpret_cast<const uint4 *>(xhalf + (g + 8) * 128 + xo);
-            const float z[4] = {0.f, 0.f, 0.f, 0.f};
-            float p[4], q[4];
-            mma_16816(p, a0, xv.x, xv.y, z);
-            mma_16816(q, a1, xv.z, xv.w, p);
-            acc[h][0] = fmaf(sa, q[0], acc[h][0]);
-            acc[h][1] = fmaf(sa, q[1], acc[h][1]);
-            acc[h][2] = fmaf(sbv, q[2], acc[h][2]);
-            acc[h][3] = fmaf(sbv, q[3], acc[h][3]);
-        }
-    }
-}
-
 // NH = number of 8-column activation halves (1 for M <= 8, 2 for M <= 16).
 template <int NH>
 __global__ void __launch_bounds__(THREADS)
@@ -152,6 +113,7 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                __half *__restrict__ Y, int64_t ldy, int N, int K, int epi, unsigned *err,
                uint64_t timeout_ns) {
     using G = GCfg<NH>;
+    constexpr int STAGES = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,9 +122,12 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     auto full_bar = [&](int s) { return sb + G::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + G::OFF_BAR + 8u * (STAGES + s); };
+    const uint32_t red_full = sb + G::OFF_RBAR, red_empty = sb + G::OFF_RBAR + 8;
+    float *red = reinterpret_cast<float *>(smem + G::OFF_RED);
 
     const int nrb = (N + ROWS - 1) / ROWS;     // 64-row blocks
-    const int nkc = (K + KC - 1) / KC;         // 128-wide K chunks
+    const int nkc = (K + KC - 1) / KC;         // 128-wide K chunks (stages)
+    const int ngrp = (nkc + 3) / 4;            // groups of four stages (one 16-byte scale load)
     const int nblk = K / 32;
 
     if (threadIdx.x == 0) {
@@ -170,6 +135,8 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), CONSUMERS);
         }
+        mbar_init(red_full, 32 * CONSUMERS);
+        mbar_init(red_empty, 32 * CONSUMERS);
         fence_barrier_init();
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
@@ -211,71 +178,150 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     }
 
     // ---------------------------------------------------------------------- consumers
+    const int w = warp;         // the 32-block of every stage this warp takes
     const int g = lane >> 2;    // fragment row group / activation row
-    const int t = lane & 3;     // quad position: k offset 8 t inside a block
-    const int r0 = warp * 16 + g;              // weight rows r0 and r0 + 8 of the 64-row tile
-    const uint32_t sw = static_cast<uint32_t>(r0 & 7);   // 128-byte swizzle phase (same for r0+8)
-    uint32_t stage = 0, phase = 0;
+    const int t = lane & 3;     // quad position: k offset 8 t inside the block
+    // weights: bytes 32 w + 8 t .. +8 of rows 16 f + g and 16 f + g + 8 (swizzle phase g for all)
+    const uint32_t wc = ((static_cast<uint32_t>(2 * w + (t >> 1)) ^ static_cast<uint32_t>(g)) << 4) +
+                        static_cast<uint32_t>((t & 1) * 8);
+    // activations: halves 32 w + 8 t .. +8 of X row g (row g + 8 is 1 KB further on)
+    const uint32_t xoff = static_cast<uint32_t>(w >> 1) * G::X_HALF + static_cast<uint32_t>(g) * 128 +
+                          ((static_cast<uint32_t>(4 * (w & 1) + t) ^ static_cast<uint32_t>(g)) << 4);
+    // byte w of two scale words (a 16-byte scale group holds block w of stage j in byte 4 j + w)
+    const uint32_t sel = static_cast<uint32_t>(w) | (static_cast<uint32_t>(4 + w) << 4);
+    uint32_t stage = 0, phase = 0, rphase = 0;
     bool ok = true;
     for (int rb = blockIdx.x; rb < nrb && ok; rb += gridDim.x) {
-        const int n0 = rb * ROWS + r0;
-        const uint8_t *srow0 = SW + static_cast<int64_t>(min(n0, N - 1)) * ldsw;
-        const uint8_t *srow1 = SW + static_cast<int64_t>(min(n0 + 8, N - 1)) * ldsw;
-        float acc[NH][4];
+        // this lane loads the scale rows of fragment t (rows 16 t + g and 16 t + g + 8) and shares
+        // them with the other lanes of its quad
+        const int nA = rb * ROWS + 16 * t + g;
+        const uint8_t *srowA = SW + static_cast<int64_t>(min(nA, N - 1)) * ldsw;
+        const uint8_t *srowB = SW + static_cast<int64_t>(min(nA + 8, N - 1)) * ldsw;
+        float acc[4][NH][4];
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
+        for (int f = 0; f < 4; ++f)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[h][i] = 0.f;
-        // scale words for chunks kc .. kc + SCALE_AHEAD - 1, rotated each chunk
-        uint32_t s0[SCALE_AHEAD], s1[SCALE_AHEAD];
+            for (int h = 0; h < NH; ++h)
 #pragma unroll
-        for (int i = 0; i < SCALE_AHEAD; ++i) {
-            s0[i] = i < nkc ? scale_word(srow0, i, nblk, sw_vec) : 0x7F7F7F7Fu;
-            s1[i] = i < nkc ? scale_word(srow1, i, nblk, sw_vec) : 0x7F7F7F7Fu;
-        }
-        for (int kc = 0; kc < nkc; ++kc) {
-            const uint32_t e0w = s0[0], e1w = s1[0];
-#pragma unroll
-            for (int i = 0; i + 1 < SCALE_AHEAD; ++i) {
-                s0[i] = s0[i + 1];
-                s1[i] = s1[i + 1];
+                for (int i = 0; i < 4; ++i) acc[f][h][i] = 0.f;
+        uint4 rawA = scale_group(srowA, 0, nblk, sw_vec);
+        uint4 rawB = scale_group(srowB, 0, nblk, sw_vec);
+        for (int G0 = 0; G0 < ngrp && ok; ++G0) {
+            const uint4 cA = rawA, cB = rawB;
+            if (G0 + 1 < ngrp) {        // one group ahead
+                rawA = scale_group(srowA, G0 + 1, nblk, sw_vec);
+                rawB = scale_group(srowB, G0 + 1, nblk, sw_vec);
             }
-            const int nxt = kc + SCALE_AHEAD;
-            s0[SCALE_AHEAD - 1] = nxt < nkc ? scale_word(srow0, nxt, nblk, sw_vec) : 0x7F7F7F7Fu;
-            s1[SCALE_AHEAD - 1] = nxt < nkc ? scale_word(srow1, nxt, nblk, sw_vec) : 0x7F7F7F7Fu;
-
-            if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
-                ok = false;
-                break;
+            // this warp's block of each of the group's four stages, stage j in byte j
+            const uint32_t pA = __byte_perm(__byte_perm(cA.x, cA.y, sel), __byte_perm(cA.z, cA.w, sel),
+                                            0x5410u);
+            const uint32_t pB = __byte_perm(__byte_perm(cB.x, cB.y, sel), __byte_perm(cB.z, cB.w, sel),
+                                            0x5410u);
+            uint32_t e0[4], e1[4];      // scale bytes of rows 16 f + g (e0) and 16 f + g + 8 (e1)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                e0[f] = __shfl_sync(0xffffffffu, pA, (g << 2) | f);
+                e1[f] = __shfl_sync(0xffffffffu, pB, (g << 2) | f);
             }
-            const uint8_t *st = smem + stage * G::STAGE;   // plain shared loads, schedulable
-            const uint8_t *xs = st + G::W_BYTES;
-            // Scale words of this stage: the fast decode builds 2^(e-127) by shifting the byte into
-            // the fp32 exponent field; codes 0x00 (subnormal 2^-127) and 0xFF (NaN) take the exact
-            // decode, chosen for the whole warp so the branch stays uniform.
-            const bool exact = __any_sync(0xffffffffu, has_special_byte(e0w) || has_special_byte(e1w));
-            if (exact)
-                consume_stage<NH, true>(acc, st, xs, r0, sw, g, t, e0w, e1w);
-            else
-                consume_stage<NH, false>(acc, st, xs, r0, sw, g, t, e0w, e1w);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(stage));
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1;
+            // The fast decode builds 2^(e-127) by shifting the byte into the fp32 exponent field;
+            // codes 0x00 (subnormal 2^-127) and 0xFF (NaN) take the exact decode, chosen for the
+            // whole warp so the branch stays uniform.
+            bool special = false;
+#pragma unroll
+            for (int f = 0; f < 4; ++f) special |= has_special_byte(e0[f]) || has_special_byte(e1[f]);
+            const bool exact = __any_sync(0xffffffffu, special);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (4 * G0 + j >= nkc) break;
+                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *st = smem + stage * G::STAGE;   // plain shared loads, schedulable
+                const uint8_t *xs = st + G::W_BYTES;
+                const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
+                uint4 xb = xa;
+                if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const uint2 wa = *reinterpret_cast<const uint2 *>(st + (16 * f + g) * 128 + wc);
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(st + (16 * f + g + 8) * 128 + wc);
+                    uint32_t a0[4], a1[4];
+                    i8x4_to_f16x2(wa.x, a0[0], a0[2]);
+                    i8x4_to_f16x2(wb.x, a0[1], a0[3]);
+                    i8x4_to_f16x2(wa.y, a1[0], a1[2]);
+                    i8x4_to_f16x2(wb.y, a1[1], a1[3]);
+                    const uint32_t b0 = (e0[f] >> (8 * j)) & 0xFFu, b1 = (e1[f] >> (8 * j)) & 0xFFu;
+                    const float sa = exact ? ue8m0_to_f32(b0) : __uint_as_float(b0 << 23);
+                    const float sbv = exact ? ue8m0_to_f32(b1) : __uint_as_float(b1 << 23);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        const uint4 xv = h == 0 ? xa : xb;
+                        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                        float p[4], q[4];
+                        mma_16816(p, a0, xv.x, xv.y, z);
+                        mma_16816(q, a1, xv.z, xv.w, p);
+                        acc[f][h][0] = fmaf(sa, q[0], acc[f][h][0]);
+                        acc[f][h][1] = fmaf(sa, q[1], acc[f][h][1]);
+                        acc[f][h][2] = fmaf(sbv, q[2], acc[f][h][2]);
+                        acc[f][h][3] = fmaf(sbv, q[3], acc[f][h][3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
             }
         }
         if (!ok) break;
-        // D fragment: acc[h][0..1] -> row n0, activations 8h + 2t (+1); acc[h][2..3] -> n0 + 8
+        // Row block done: warp w finishes fragment w.  Every warp hands the other three fragments'
+        // sums over through shared memory, one activation half at a time; the four partial sums of
+        // a fragment are added in warp order.  Waits are bounded like the stage waits.
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
+            if (!mbar_wait(red_empty, rphase ^ 1, timeout_ns)) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                if (f == w) continue;
+                const int slot = f < w ? f : f - 1;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) red[((w * 3 + slot) * 4 + i) * 32 + lane] = acc[f][h][i];
+            }
+            mbar_arrive(red_full);
+            if (!mbar_wait(red_full, rphase, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            float own[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) own[i] = acc[0][h][i];
+#pragma unroll
+            for (int f = 1; f < 4; ++f)
+                if (f == w)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) own[i] = acc[f][h][i];
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < CONSUMERS; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    sum[i] += u == w ? own[i] : red[((u * 3 + (w < u ? w : w - 1)) * 4 + i) * 32 + lane];
+            mbar_arrive(red_empty);
+            rphase ^= 1;
+            // D fragment: sum[0..1] -> row n0, activations 8h + 2t (+1); sum[2..3] -> n0 + 8
+            const int n0 = rb * ROWS + 16 * w + g;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int m = 8 * h + 2 * t + (i & 1);
                 const int n = n0 + ((i & 2) ? 8 : 0);
                 if (m < M && n < N) {
                     __half *dst = Y + static_cast<int64_t>(m) * ldy + n;
-                    float x = acc[h][i];
+                    float x = sum[i];
                     if (epi & EPI_ACC_BIT) x += __half2float(*dst);   // Y = relu?(X W^T + Y_old)
                     if (epi & EPI_RELU_BIT) x = fmaxf(x, 0.0f);
                     *dst = __float2half_rn(x);
@@ -305,7 +351,8 @@ cudaError_t launch_nh(const __half *X, int64_t ldx, int M, const qgemm_tensor *W
     const int per_sm = 232448 / G::SMEM;       // CTAs that fit in one SM's shared memory
     int grid = ctx.num_sms * (per_sm < 1 ? 1 : per_sm);
     if (grid > nrb) grid = nrb;
-    const int sw_vec = (reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0) ? 1 : 0;
+    const uintptr_t sp = reinterpret_cast<uintptr_t>(W->scales);
+    const int sw_vec = (sp % 16 == 0 && W->lds % 16 == 0) ? 2 : (sp % 4 == 0 && W->lds % 4 == 0) ? 1 : 0;
     kern<<<grid, THREADS, G::SMEM, ctx.stream>>>(tmW, tmX, M, W->scales, W->lds, sw_vec, Y, ldy, N,
                                                  K, ctx.epi, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();

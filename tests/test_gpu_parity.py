@@ -314,6 +314,32 @@ def test_w8_gemv_extreme_scales(dev, orc):
     assert torch.isnan(Y[:, 3].cpu()).all() and not torch.isnan(Y[:, 4].cpu()).any()
 
 
+@pytest.mark.parametrize("M,scale_pad", [(2, 48), (16, 48), (5, 36), (12, 40)])
+def test_w8_gemv_padded_strides_and_repeatable(dev, orc, M, scale_pad):
+    """Views into wider buffers: weight rows K + 64 bytes apart, X rows K + 24 halves apart and
+    scale rows `scale_pad` bytes apart (48: 16-byte aligned rows whose 33 blocks end inside a
+    16-byte group; 36: 4-byte aligned; 40: 8-byte aligned).  N = 200 leaves a partial 64-row
+    block.  Two calls give bit-identical outputs."""
+    N, K = 200, 1056
+    nblk = K // 32
+    d = synth.w8_inputs(M, N, K, seed=40 + M)
+    w_full = torch.zeros(N, K + 64, dtype=torch.uint8)
+    w_full[:, :K] = d["w"]
+    s_full = torch.full((N, scale_pad), 255, dtype=torch.uint8)     # padding would poison as NaN
+    s_full[:, :nblk] = d["sw"]
+    x_full = torch.zeros(M, K + 24, dtype=torch.float16)
+    x_full[:, :K] = d["x"]
+    wv, sv, xv = w_full.to(dev)[:, :K], s_full.to(dev)[:, :nblk], x_full.to(dev)[:, :K]
+    W = q.qgemm_create_tensor(q.INT8, wv, sv)
+    Y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_w8_gemv(xv, W, Y)
+    res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    _check(Y, res, orc, what=f"w8 gemv padded M={M} lds={scale_pad}")
+    Y2 = torch.empty_like(Y)
+    q.qgemm_w8_gemv(xv, W, Y2)
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+
+
 @pytest.mark.parametrize("M", [1, 8, 16])
 def test_w8_gemv_full_size_sampled(dev, orc, M):
     d = synth.workload("w8_decode", M=M)
