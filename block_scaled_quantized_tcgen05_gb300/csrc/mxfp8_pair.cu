@@ -377,6 +377,8 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tmem_wait_st();
             tc_fence_before();
+            // the slot's scale bytes were read through the generic proxy; its next fill is a TMA write
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * s);
         }

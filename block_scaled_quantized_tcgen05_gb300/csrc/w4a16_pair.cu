@@ -331,6 +331,8 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 tmem_st_32x32b_x32(tmem_base + ((q * 32) << 16) + A_COL0 + stage * A_COLS, out);
                 tmem_wait_st();
                 tc_fence_before();
+                // the raw weights were read through the generic proxy; the slot's next fill is a TMA write
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * stage);
             }

@@ -105,6 +105,70 @@ __device__ __forceinline__ bool has_special_byte(uint32_t w) {
     return (z | f) != 0u;
 }
 
+// Up to four stages of one scale group (stages 4 G0 .. 4 G0 + 3 that exist).  e0[f] / e1[f] hold the
+// scale bytes of rows 16 f + g / 16 f + g + 8 for this warp's block of each stage (stage j in byte
+// j).  EXACT selects the decode for the whole group: the shift decode builds 2^(e-127) by moving the
+// byte into the fp32 exponent field; codes 0x00 (subnormal 2^-127) and 0xFF (NaN) need the exact one.
+template <int NH, bool EXACT, int STAGES>
+__device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t *smem, uint32_t sb,
+                                          uint32_t stage_bytes, uint32_t off_bar, int nst,
+                                          uint32_t wrow, uint32_t xoff, const uint32_t (&e0)[4],
+                                          const uint32_t (&e1)[4], uint32_t &stage, uint32_t &phase,
+                                          int lane, uint64_t timeout_ns) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j >= nst) break;
+        const uint32_t full = sb + off_bar + 8u * stage, empty = full + 8u * STAGES;
+        if (!mbar_wait(full, phase, timeout_ns)) return false;
+        // Reconverge before the warp-wide mma.sync.aligned: lane 0 alone took the arrive branch of the
+        // previous stage and every lane polls the barrier on its own.
+        __syncwarp();
+        const uint8_t *st = smem + stage * stage_bytes;    // plain shared loads, schedulable
+        const uint8_t *xs = st + ROWS * KC;
+        const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
+        uint4 xb = xa;
+        if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
+        const uint32_t sh = 8u * static_cast<uint32_t>(j);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) {
+            const uint2 wa = *reinterpret_cast<const uint2 *>(st + wrow + f * 16 * 128);
+            const uint2 wb = *reinterpret_cast<const uint2 *>(st + wrow + (f * 16 + 8) * 128);
+            uint32_t a0[4], a1[4];
+            i8x4_to_f16x2(wa.x, a0[0], a0[2]);
+            i8x4_to_f16x2(wb.x, a0[1], a0[3]);
+            i8x4_to_f16x2(wa.y, a1[0], a1[2]);
+            i8x4_to_f16x2(wb.y, a1[1], a1[3]);
+            const uint32_t b0 = (e0[f] >> sh) & 0xFFu, b1 = (e1[f] >> sh) & 0xFFu;
+            const float sa = EXACT ? ue8m0_to_f32(b0) : __uint_as_float(b0 << 23);
+            const float sbv = EXACT ? ue8m0_to_f32(b1) : __uint_as_float(b1 << 23);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                const uint4 xv = h == 0 ? xa : xb;
+                const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                float p[4], q[4];
+                mma_16816(p, a0, xv.x, xv.y, z);
+                mma_16816(q, a1, xv.z, xv.w, p);
+                acc[f][h][0] = fmaf(sa, q[0], acc[f][h][0]);
+                acc[f][h][1] = fmaf(sa, q[1], acc[f][h][1]);
+                acc[f][h][2] = fmaf(sbv, q[2], acc[f][h][2]);
+                acc[f][h][3] = fmaf(sbv, q[3], acc[f][h][3]);
+            }
+        }
+        // Hand the stage back.  Its operands were read through the generic proxy and the producer's next
+        // TMA writes it through the async proxy: each lane orders its reads before that write with a
+        // proxy fence (measured on this GPU: without it, whole 64-row blocks picked up data of the next
+        // fill now and then).
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty);
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+        }
+    }
+    return true;
+}
+
 // NH = number of 8-column activation halves (1 for M <= 8, 2 for M <= 16).
 template <int NH>
 __global__ void __launch_bounds__(THREADS)
@@ -182,8 +246,9 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int g = lane >> 2;    // fragment row group / activation row
     const int t = lane & 3;     // quad position: k offset 8 t inside the block
     // weights: bytes 32 w + 8 t .. +8 of rows 16 f + g and 16 f + g + 8 (swizzle phase g for all)
-    const uint32_t wc = ((static_cast<uint32_t>(2 * w + (t >> 1)) ^ static_cast<uint32_t>(g)) << 4) +
-                        static_cast<uint32_t>((t & 1) * 8);
+    const uint32_t wrow = static_cast<uint32_t>(g) * 128 +
+                          ((static_cast<uint32_t>(2 * w + (t >> 1)) ^ static_cast<uint32_t>(g)) << 4) +
+                          static_cast<uint32_t>((t & 1) * 8);
     // activations: halves 32 w + 8 t .. +8 of X row g (row g + 8 is 1 KB further on)
     const uint32_t xoff = static_cast<uint32_t>(w >> 1) * G::X_HALF + static_cast<uint32_t>(g) * 128 +
                           ((static_cast<uint32_t>(4 * (w & 1) + t) ^ static_cast<uint32_t>(g)) << 4);
@@ -217,63 +282,19 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                             0x5410u);
             const uint32_t pB = __byte_perm(__byte_perm(cB.x, cB.y, sel), __byte_perm(cB.z, cB.w, sel),
                                             0x5410u);
+            // the lanes together hold every row of the block: one vote decides the decode
+            const bool exact = __any_sync(0xffffffffu, has_special_byte(pA) || has_special_byte(pB));
             uint32_t e0[4], e1[4];      // scale bytes of rows 16 f + g (e0) and 16 f + g + 8 (e1)
 #pragma unroll
             for (int f = 0; f < 4; ++f) {
                 e0[f] = __shfl_sync(0xffffffffu, pA, (g << 2) | f);
                 e1[f] = __shfl_sync(0xffffffffu, pB, (g << 2) | f);
             }
-            // The fast decode builds 2^(e-127) by shifting the byte into the fp32 exponent field;
-            // codes 0x00 (subnormal 2^-127) and 0xFF (NaN) take the exact decode, chosen for the
-            // whole warp so the branch stays uniform.
-            bool special = false;
-#pragma unroll
-            for (int f = 0; f < 4; ++f) special |= has_special_byte(e0[f]) || has_special_byte(e1[f]);
-            const bool exact = __any_sync(0xffffffffu, special);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (4 * G0 + j >= nkc) break;
-                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *st = smem + stage * G::STAGE;   // plain shared loads, schedulable
-                const uint8_t *xs = st + G::W_BYTES;
-                const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
-                uint4 xb = xa;
-                if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const uint2 wa = *reinterpret_cast<const uint2 *>(st + (16 * f + g) * 128 + wc);
-                    const uint2 wb = *reinterpret_cast<const uint2 *>(st + (16 * f + g + 8) * 128 + wc);
-                    uint32_t a0[4], a1[4];
-                    i8x4_to_f16x2(wa.x, a0[0], a0[2]);
-                    i8x4_to_f16x2(wb.x, a0[1], a0[3]);
-                    i8x4_to_f16x2(wa.y, a1[0], a1[2]);
-                    i8x4_to_f16x2(wb.y, a1[1], a1[3]);
-                    const uint32_t b0 = (e0[f] >> (8 * j)) & 0xFFu, b1 = (e1[f] >> (8 * j)) & 0xFFu;
-                    const float sa = exact ? ue8m0_to_f32(b0) : __uint_as_float(b0 << 23);
-                    const float sbv = exact ? ue8m0_to_f32(b1) : __uint_as_float(b1 << 23);
-#pragma unroll
-                    for (int h = 0; h < NH; ++h) {
-                        const uint4 xv = h == 0 ? xa : xb;
-                        const float z[4] = {0.f, 0.f, 0.f, 0.f};
-                        float p[4], q[4];
-                        mma_16816(p, a0, xv.x, xv.y, z);
-                        mma_16816(q, a1, xv.z, xv.w, p);
-                        acc[f][h][0] = fmaf(sa, q[0], acc[f][h][0]);
-                        acc[f][h][1] = fmaf(sa, q[1], acc[f][h][1]);
-                        acc[f][h][2] = fmaf(sbv, q[2], acc[f][h][2]);
-                        acc[f][h][3] = fmaf(sbv, q[3], acc[f][h][3]);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
+            const int nst = min(4, nkc - 4 * G0);
+            ok = exact ? run_group<NH, true, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst, wrow, xoff,
+                                                     e0, e1, stage, phase, lane, timeout_ns)
+                       : run_group<NH, false, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst, wrow, xoff,
+                                                      e0, e1, stage, phase, lane, timeout_ns);
         }
         if (!ok) break;
         // Row block done: warp w finishes fragment w.  Every warp hands the other three fragments'

@@ -118,3 +118,5 @@ def test_attention_full_size_sampled(dev, orc):
                         heads=heads, qrows=rows)
     got = O[torch.from_numpy(heads).to(dev), torch.from_numpy(rows).to(dev)]
     _check(got, res, orc, "attention 32x4096x4096 sampled")
+    O2 = _run(d, dev)
+    assert torch.equal(O2.view(torch.int16), O.view(torch.int16))     # repeatable bit for bit

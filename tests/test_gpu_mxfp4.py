@@ -178,3 +178,7 @@ def test_mxfp4_full_size_sampled(dev, orc):
     rows = np.concatenate([[0, 127, 128, 8191], rows])
     res = _oracle(orc, d, rows)
     _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="mxfp4 8192^3 sampled")
+    for _ in range(2):                                                  # repeatable bit for bit
+        C2 = torch.empty_like(C)
+        q.qgemm_mxfp4(A, B, C2)
+        assert torch.equal(C2.view(torch.int16), C.view(torch.int16))

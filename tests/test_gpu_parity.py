@@ -215,6 +215,11 @@ def test_mxfp8_full_size_sampled(dev, orc):
     res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy(), rows=rows)
     got = C[torch.from_numpy(rows).to(dev)]
     _check(got, res, orc, what="mxfp8 8192^3 sampled")
+    # the whole product is repeatable bit for bit (no timing-dependent stage reuse)
+    for _ in range(2):
+        C2 = torch.empty_like(C)
+        q.qgemm_mxfp8(A, B, C2)
+        assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
 
 
 # ------------------------------------------------------------------------------- fp16
@@ -236,6 +241,9 @@ def test_gemm_f16_full_size_sampled(dev, orc):
     rows = np.concatenate([[0, 4095], np.sort(np.random.default_rng(1).choice(4096, 30, replace=False))])
     res = orc.gemm_f16(d["a"].numpy(), d["b"].numpy(), rows=rows)
     _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="f16 4096^3 sampled")
+    C2 = torch.empty_like(C)
+    q.gemm_f16(d["a"].to(dev), d["b"].to(dev), C2)
+    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))     # repeatable bit for bit
 
 
 # ------------------------------------------------------------------------------ W4A16
@@ -284,6 +292,10 @@ def test_w4a16_full_size_sampled(dev, orc):
     rows = np.concatenate([[0, 4095], np.sort(np.random.default_rng(2).choice(4096, 14, replace=False))])
     res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy(), rows=rows)
     _check(C[torch.from_numpy(rows).to(dev)], res, orc, what="w4a16 sampled")
+    for _ in range(2):                                                  # repeatable bit for bit
+        C2 = torch.empty_like(C)
+        q.qgemm_w4a16(d["a"].to(dev), W, C2)
+        assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
 
 
 # ------------------------------------------------------------------------------- GEMV
@@ -349,6 +361,12 @@ def test_w8_gemv_full_size_sampled(dev, orc, M):
     cols = np.concatenate([[0, 28671], np.sort(np.random.default_rng(M).choice(28672, 2046, replace=False))])
     res = orc.w8_gemv(d["x"].numpy(), d["w"].numpy()[cols], d["sw"].numpy()[cols])
     _check(Y[:, torch.from_numpy(cols).to(dev)], res, orc, what=f"w8 gemv 28672x8192 M={M}")
+    # every output is repeatable bit for bit: a stage handed back to the producer before its reads
+    # are ordered shows up here as whole 64-row blocks that change from call to call
+    for _ in range(8):
+        Y2 = torch.empty_like(Y)
+        q.qgemm_w8_gemv(d["x"].to(dev), W, Y2)
+        assert torch.equal(Y2.view(torch.int16), Y.view(torch.int16))
 
 
 # -------------------------------------------------------------------- failure detection

@@ -129,3 +129,6 @@ def test_w4a16_f16s_full_size_sampled(dev, orc):
     res = orc.w4a16_f16s(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy(), rows=rows)
     _check(C[torch.from_numpy(rows).to(dev)], res, orc, rows=None,
            what="w4a16 fp16-scale 4096x14336x4096 sampled")
+    C2 = torch.empty_like(C)
+    q.qgemm_w4a16_f16s(d["a"].to(dev), d["w"].to(dev), d["sw"].to(dev), C2)
+    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))     # repeatable bit for bit
