@@ -232,6 +232,10 @@ cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb
 // accumulator rows in TMEM (two accumulators).  The leader (rank 0) arms each stage's full
 // barrier with both CTAs' bytes and issues the MMAs; its commits are multicast to both CTAs'
 // barriers; one lane per epilogue warp of both CTAs releases an accumulator on the leader.
+// Last wave: when the tiles left after the last full wave of pairs fit twice into one wave, each
+// of them is computed as two 256 x 128 halves (N = 128 MMAs, one 64-column B box per CTA) by two
+// pairs, so the last wave takes half a tile's time instead of a whole one (4096^3: 256 tiles on 76
+// pairs are 3.37 waves; this way 3.5 tile times instead of 4).
 constexpr int P_BM = 128;       // rows per CTA (the pair covers 256)
 constexpr int P_BN = 256;       // columns per pair tile (128 stored per CTA)
 constexpr int P_BK = 64;
@@ -250,9 +254,32 @@ constexpr uint32_t P_OFF_SLOT = P_OFF_BAR + (2 * P_STAGES + 5) * 8;
 constexpr uint32_t P_SMEM_BYTES = P_OFF_SLOT + 16 + 1024;
 static_assert(P_SMEM_BYTES <= 232448, "smem");
 
-// kind::f16, D fp32, A K-major, B MN-major, N = 256, M = 256 (pair)
+// kind::f16, D fp32, A K-major, B MN-major, N = 256 (or 128 for a half tile), M = 256 (pair)
 constexpr uint32_t P_IDESC = (1u << 4) | (1u << 16) | (static_cast<uint32_t>(P_BN >> 3) << 17) |
                            (static_cast<uint32_t>(256 >> 4) << 24);
+constexpr uint32_t P_IDESC_HALF = (1u << 4) | (1u << 16) | (static_cast<uint32_t>((P_BN / 2) >> 3) << 17) |
+                                (static_cast<uint32_t>(256 >> 4) << 24);
+
+// Work items of a pair kernel: whole tiles, then (when the leftover tiles fit twice into one wave
+// of pairs) each leftover tile as two column halves.  half < 0 marks a whole tile.
+struct PairWork {
+    int full_items, n_items;
+    __device__ __forceinline__ PairWork(int num_tiles, int npairs) {
+        const int rem = num_tiles % npairs;
+        const bool split = rem > 0 && 2 * rem <= npairs;
+        full_items = num_tiles - (split ? rem : 0);
+        n_items = full_items + (split ? 2 * rem : 0);
+    }
+    __device__ __forceinline__ void item(int it, int &tile, int &half) const {
+        if (it < full_items) {
+            tile = it;
+            half = -1;
+        } else {
+            tile = full_items + ((it - full_items) >> 1);
+            half = (it - full_items) & 1;
+        }
+    }
+};
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -279,6 +306,7 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const int tiles_n = (N + P_BN - 1) / P_BN;
     const int num_tiles = tiles_m * tiles_n;
     const int KT = (K + P_BK - 1) / P_BK;
+    const PairWork work(num_tiles, npairs);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
@@ -309,23 +337,27 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                int mb, nb;
+            for (int it = pair; it < work.n_items && ok; it += npairs) {
+                int tile, half, mb, nb;
+                work.item(it, tile, half);
                 tile_coords(tile, tiles_m, tiles_n, mb, nb);
                 const int m0 = mb * 2 * P_BM + static_cast<int>(rank) * P_BM;
-                const int nh = nb * P_BN + static_cast<int>(rank) * (P_BN / 2);
+                // a whole tile: 128 columns per CTA; a half tile: 64 columns per CTA
+                const int nh = half < 0 ? nb * P_BN + static_cast<int>(rank) * (P_BN / 2)
+                                        : nb * P_BN + half * (P_BN / 2) + static_cast<int>(rank) * 64;
+                const uint32_t tx = 2 * (P_A_BYTES + (half < 0 ? P_B_BYTES : P_B_ATOM));
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (P_A_BYTES + P_B_BYTES));
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t sA = sb + P_OFF_A + stage * P_A_BYTES;
                     const uint32_t sB = sb + P_OFF_B + stage * P_B_BYTES;
                     tma_load_2d_pair(sA, &tmA, lead_full, kt * P_BK, m0);
                     tma_load_2d_pair(sB, &tmB, lead_full, nh, kt * P_BK);
-                    tma_load_2d_pair(sB + P_B_ATOM, &tmB, lead_full, nh + 64, kt * P_BK);
+                    if (half < 0) tma_load_2d_pair(sB + P_B_ATOM, &tmB, lead_full, nh + 64, kt * P_BK);
                     ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -345,7 +377,10 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if (rank == 0) {
             uint32_t stage = 0, phase = 0, acc_it = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+            for (int it = pair; it < work.n_items && ok; it += npairs) {
+                int tile, half;
+                work.item(it, tile, half);
+                const uint32_t idesc = half < 0 ? P_IDESC : P_IDESC_HALF;
                 const uint32_t ab = acc_it & 1;
                 if (!mbar_wait_cluster(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                     ok = false;
@@ -363,7 +398,7 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         const uint64_t bdesc = smem_desc(sb + P_OFF_B + stage * P_B_BYTES, P_B_ATOM, 1024, SWZ_128B);
 #pragma unroll
                         for (uint32_t j = 0; j < P_BK / 16; ++j)
-                            mma_f16_pair(tmem_base + ab * P_BN, adesc + 2 * j, bdesc + 128 * j, P_IDESC,
+                            mma_f16_pair(tmem_base + ab * P_BN, adesc + 2 * j, bdesc + 128 * j, idesc,
                                          (kt > 0 || j > 0) ? 1u : 0u);
                         tc_commit_pair(empty_bar(stage), 3);
                     }
@@ -387,8 +422,9 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     } else {
         const uint32_t q = warp & 3;
         uint32_t acc_it = 0;
-        for (int tile = pair; tile < num_tiles; tile += npairs) {
-            int mb, nb;
+        for (int it = pair; it < work.n_items; it += npairs) {
+            int tile, half, mb, nb;
+            work.item(it, tile, half);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
             if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
@@ -396,10 +432,16 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 break;
             }
             tc_fence_after();
-            epilogue_tile<P_BN, 2>(tmem_base + ab * P_BN, q, lane, C, ldc,
-                                 mb * 2 * P_BM + static_cast<int>(rank) * P_BM, nb * P_BN, M, N,
-                                 c_vec != 0, map_to_cta(tmem_empty(ab), 0),
-                                 sb + P_OFF_EPI + (warp - 2) * 2048, epi);
+            const int m0 = mb * 2 * P_BM + static_cast<int>(rank) * P_BM;
+            if (half < 0)
+                epilogue_tile<P_BN, 2>(tmem_base + ab * P_BN, q, lane, C, ldc, m0, nb * P_BN, M, N,
+                                       c_vec != 0, map_to_cta(tmem_empty(ab), 0),
+                                       sb + P_OFF_EPI + (warp - 2) * 2048, epi);
+            else
+                epilogue_tile<P_BN / 2, 2>(tmem_base + ab * P_BN, q, lane, C, ldc, m0,
+                                           nb * P_BN + half * (P_BN / 2), M, N, c_vec != 0,
+                                           map_to_cta(tmem_empty(ab), 0),
+                                           sb + P_OFF_EPI + (warp - 2) * 2048, epi);
             ++acc_it;
         }
     }

@@ -246,6 +246,20 @@ def test_gemm_f16_full_size_sampled(dev, orc):
     assert torch.equal(C2.view(torch.int16), C.view(torch.int16))     # repeatable bit for bit
 
 
+@pytest.mark.parametrize("M,N,K", [(2560, 2048, 512), (2304, 2144, 320)])
+def test_gemm_f16_last_wave_halves(dev, orc, M, N, K):
+    """More pair tiles than one wave (80 and 81 tiles on 76 pairs): the leftover tiles run as two
+    256 x 128 halves each (for N = 2144 one half lies wholly past N); every output checked."""
+    d = synth.f16_inputs(M, N, K, seed=M + N)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.gemm_f16(d["a"].to(dev), d["b"].to(dev), C)
+    res = orc.gemm_f16(d["a"].numpy(), d["b"].numpy())
+    _check(C, res, orc, what=f"f16 {M}x{N}x{K} last-wave halves")
+    C2 = torch.empty_like(C)
+    q.gemm_f16(d["a"].to(dev), d["b"].to(dev), C2)
+    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
+
+
 # ------------------------------------------------------------------------------ W4A16
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 256), (256, 640, 1024)])
 def test_w4a16_matches_oracle(dev, orc, M, N, K):
