@@ -12,8 +12,13 @@
  * overwritten ("mode multiply", same page, section "The real matmul2d API").
  *
  * Conventions that hold for every call:
- *   - All data, scale and output pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates, frees or retains device memory; a qgemm_tensor only borrows pointers.
+ *   - All data, scale and output pointers are DEVICE pointers owned by the caller (host pointers
+ *     for qgemm_mxfp8_host).  The library never frees or retains them; a qgemm_tensor only
+ *     borrows pointers.  The device memory the library takes for itself is stated at each call
+ *     that uses it: the scale scratch of the CTA-pair block-scaled GEMMs (from a per-device
+ *     pool), the staging buffers of qgemm_mxfp8_host, the fixed array of qgemm_mxfp8_noalloc.
+ *   - Results are repeatable: the same inputs on the same GPU give the same output bits (every
+ *     sum is taken in a fixed order, independent of timing).
  *   - Matrices are row-major with the reduction dimension K contiguous ("K-major"), except the
  *     right operand of gemm_f16, which is B[K, N] row-major (N contiguous).
  *   - Row strides are given in BYTES for qgemm_tensor planes and in ELEMENTS for plain fp16
