@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -21,7 +22,8 @@ __device__ unsigned int g_device_error_word;
 
 thread_local char g_last_msg[512] = "";
 
-uint64_t g_timeout_ns = 4000000000ull;
+// bound on every device-side wait; set from any host thread, read at each launch
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 
 constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
@@ -64,7 +66,7 @@ qgemm_status get_ctx(void *stream, qgi::LaunchCtx *ctx) {
     }
     ctx->stream = static_cast<cudaStream_t>(stream);
     ctx->err = d.err;
-    ctx->timeout_ns = g_timeout_ns;
+    ctx->timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     ctx->num_sms = d.num_sms;
     ctx->device = dev;
     return QGEMM_OK;
@@ -210,7 +212,9 @@ const char *qgemm_status_string(qgemm_status s) {
 
 const char *qgemm_last_error_message(void) { return g_last_msg; }
 
-void qgemm_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns < 1000000ull ? 1000000ull : ns; }
+void qgemm_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns, std::memory_order_relaxed);
+}
 
 qgemm_status qgemm_create_tensor(qgemm_tensor **out, qgemm_dtype dt, int64_t rows, int64_t k,
                                  const void *data, int64_t data_row_stride_bytes,
