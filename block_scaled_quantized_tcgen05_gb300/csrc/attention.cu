@@ -90,6 +90,24 @@ __device__ __forceinline__ float ex2_poly(float x) {
     return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
+// Packed fp32 pairs: (d0, d1) = (a0 b0 + c0, a1 b1 + c1) and (d0, d1) += (a0, a1), one
+// instruction each, each lane rounded as its scalar counterpart.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 // One key tile of one query row: the running maximum m (log2 units) is given; writes
 // P = 2^(s c - m) as fp16 pairs into TMEM columns scol .. scol + 63 of this warp's lanes and
 // returns the row sum of P.  One pair in four is exponentiated on the FMA pipe, the rest by
@@ -97,6 +115,7 @@ __device__ __forceinline__ float ex2_poly(float x) {
 template <bool MASK>
 __device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int valid, float c,
                                               float m, uint32_t scol) {
+    // row sum in four fp32 lanes (two packed pairs), scaled scores formed a pair at a time
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {                      // 64 keys -> 32 packed columns
@@ -104,15 +123,16 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int vali
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int k0 = 64 * h + 2 * i;
-            const float x0 = fmaf(__uint_as_float(v[k0]), c, -m);
-            const float x1 = fmaf(__uint_as_float(v[k0 + 1]), c, -m);
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), c, c, -m, -m);
             float p0 = (i & 3) == 3 ? ex2_poly(x0) : ex2_approx(x0);
             float p1 = (i & 3) == 3 ? ex2_poly(x1) : ex2_approx(x1);
             if (MASK) {
                 p0 = k0 < valid ? p0 : 0.0f;
                 p1 = k0 + 1 < valid ? p1 : 0.0f;
             }
-            acc[i & 3] += p0 + p1;
+            const int a = 2 * (i & 1);
+            add2(acc[a], acc[a + 1], p0, p1);
             pk[i] = pack_f16x2(p0, p1);
         }
         tmem_st_32x32b_x32(scol + 32 * h, pk);
@@ -126,10 +146,21 @@ __device__ __forceinline__ float tile_max(const uint32_t (&v)[128], int valid) {
     float mx[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+    if constexpr (!MASK) {
+        // three-input maximum: 64 instructions for the 128 scores, eight independent chains
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-        const float x = __uint_as_float(v[i]);
-        mx[i & 7] = fmaxf(mx[i & 7], MASK ? (i < valid ? x : -INFINITY) : x);
+        for (int i = 0; i < 128; i += 2) {
+            const int k = (i >> 1) & 7;
+            asm("max.f32 %0, %1, %2, %3;"
+                : "=f"(mx[k])
+                : "f"(mx[k]), "f"(__uint_as_float(v[i])), "f"(__uint_as_float(v[i + 1])));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+            const float x = __uint_as_float(v[i]);
+            mx[i & 7] = fmaxf(mx[i & 7], i < valid ? x : -INFINITY);
+        }
     }
     return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
