@@ -532,6 +532,24 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // 2^(e - 127) as fp32 built from the exponent bits: e = 0 is the subnormal 2^-127,
 // e = 255 is NaN.
+// Packed fp32 pairs: (d0, d1) = (a0 b0 + c0, a1 b1 + c1) and (d0, d1) += (a0, a1), one
+// instruction each, each lane rounded as its scalar counterpart.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ float ue8m0_to_f32(uint32_t e) {
     uint32_t bits = (e == 0u) ? 0x00400000u : (e == 255u ? 0x7FC00000u : (e << 23));
     return __uint_as_float(bits);
