@@ -74,26 +74,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// 2^x on the FMA pipe, for x <= 9 (larger x is never formed here): x = n + f with n the nearest
-// integer (added to a float's exponent field by the round-to-nearest of x + 1.5 * 2^23) and
-// f in [-1/2, 1/2]; 2^f by a cubic fitted here for least maximum relative error on that interval
-// (7.5e-5, below the half-ulp 2.4e-4 of the fp16 the result is rounded to).  Inputs below -126
-// give 2^-126 or less, where an exact value would be at most that.
-__device__ __forceinline__ float ex2_poly(float x) {
-    x = fmaxf(x, -126.0f);
-    const float t = x + 12582912.0f;                  // 1.5 * 2^23: rounds x to an integer
-    const int n = __float_as_int(t) - 0x4B400000;
-    const float f = x - (t - 12582912.0f);
-    float p = fmaf(0.0551715f, f, 0.24261096f);
-    p = fmaf(p, f, 0.69326099f);
-    p = fmaf(p, f, 0.99992808f);
-    return __int_as_float(__float_as_int(p) + (n << 23));
-}
-
 // One key tile of one query row: the running maximum m (log2 units) is given; writes
 // P = 2^(s c - m) as fp16 pairs into TMEM columns scol .. scol + 63 of this warp's lanes and
-// returns the row sum of P.  One pair in four is exponentiated on the FMA pipe, the rest by
-// ex2.approx, so that neither pipe alone sets the pace.  MASK: keys >= valid give P = 0.
+// returns the row sum of P.  Every exponential is one ex2.approx (measured: moving a share of them
+// to a cubic on the FMA pipe costs more issue slots than it saves).  MASK: keys >= valid give 0.
 template <bool MASK>
 __device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int valid, float c,
                                               float m, uint32_t scol) {
@@ -107,8 +91,8 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int vali
             const int k0 = 64 * h + 2 * i;
             float x0, x1;
             fma2(x0, x1, __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), c, c, -m, -m);
-            float p0 = (i & 3) == 3 ? ex2_poly(x0) : ex2_approx(x0);
-            float p1 = (i & 3) == 3 ? ex2_poly(x1) : ex2_approx(x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
             if (MASK) {
                 p0 = k0 < valid ? p0 : 0.0f;
                 p1 = k0 + 1 < valid ? p1 : 0.0f;
