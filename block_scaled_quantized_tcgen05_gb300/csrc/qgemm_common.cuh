@@ -284,18 +284,17 @@ __device__ __forceinline__ void epilogue_tile_early(uint32_t tmem_base, uint32_t
     constexpr int NCH = BN / 32;
     uint32_t p[NCH][16];
 #pragma unroll
-    for (int h = 0; h < 2 * NCH; ++h) {     // 16 columns per read keeps the raw values few
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem_base + ((q * 32) << 16) + h * 16, v);
+    for (int ch = 0; ch < NCH; ++ch) {      // 32 columns per read: one wait per 32 (each wait
+        uint32_t v[32];                     // covers every load in flight, so fewer is faster)
+        tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
         tmem_wait_ld();
         if (relu) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.0f));
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaxf(__uint_as_float(v[i]), 0.0f));
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            p[h >> 1][(h & 1) * 8 + i] = pack_f16x2(__uint_as_float(v[2 * i]),
-                                                    __uint_as_float(v[2 * i + 1]));
+        for (int i = 0; i < 16; ++i)
+            p[ch][i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
     }
     tc_fence_before();
     __syncwarp();
