@@ -10,11 +10,6 @@
 
 namespace qg {
 
-__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
 __device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t r;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
@@ -52,38 +47,34 @@ __device__ __forceinline__ void fused_consts(uint32_t e, uint32_t &s2, uint32_t 
     c2 = c1032 | (c72 << 16);
 }
 
+// The +8 bias (the nibble's sign bit flipped) and the 1024 exponent go in with one lop3,
+// (b & 0x00F0000F) ^ 0x64806408: inside the mask it flips bit 3 of each kept nibble, outside it
+// writes the exponent bits.
 __device__ __forceinline__ void i4x8_to_f16_fused(uint32_t v, uint32_t s2, uint32_t c2,
                                                   uint32_t (&o)[4]) {
-    const uint32_t u = v ^ 0x88888888u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t b = __byte_perm(u, 0u, 0x4040u | (j << 8) | j);   // byte j in both halves
+        const uint32_t b = __byte_perm(v, 0u, 0x4040u | (j << 8) | j);   // byte j in both halves
         uint32_t tv;
-        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(tv) : "r"(b), "r"(0x00F0000Fu), "r"(0x64006400u));
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(tv) : "r"(b), "r"(0x00F0000Fu), "r"(0x64806408u));
         o[j] = h2_fma(tv, s2, c2);
     }
 }
 
 // 8 int4 (one 32-bit word, k = 8w .. 8w+7, even k in low nibbles) times the fp16x2 scale ->
-// four fp16x2 words in k order.
+// four fp16x2 words in k order.  Each pair comes out of the same spread as the fused path; one
+// fp16x2 FMA with per-half constants (1, 1/16) and (-1032, -72) gives the exact (q_lo, q_hi),
+// and the multiply by the scale is the one rounding.
 __device__ __forceinline__ void i4x8_to_f16(uint32_t v, uint32_t s2, uint32_t (&o)[4]) {
-    const uint32_t u = v ^ 0x88888888u;  // q + 8 in every nibble
-    const uint32_t MAGIC = 0x64006400u;   // fp16 1024.0 in both halves
-    const uint32_t t0 = (u & 0x000F000Fu) | MAGIC;         // 1024 + u(k0), 1024 + u(k4)
-    const uint32_t t1 = (u & 0x00F000F0u) | MAGIC;         // 1024 + 16 u(k1), ... (k5)
-    const uint32_t t2 = ((u >> 8) & 0x000F000Fu) | MAGIC;  // k2, k6
-    const uint32_t t3 = ((u >> 8) & 0x00F000F0u) | MAGIC;  // k3, k7
-    const uint32_t B1032 = 0x64086408u;   // 1032.0
-    const uint32_t R16 = 0x2C002C00u;     // 1/16
-    const uint32_t N72 = 0xD480D480u;     // -72.0
-    const uint32_t h0 = h2_mul(h2_sub(t0, B1032), s2);         // (q0, q4) * s
-    const uint32_t h1 = h2_mul(h2_fma(t1, R16, N72), s2);      // (q1, q5) * s
-    const uint32_t h2 = h2_mul(h2_sub(t2, B1032), s2);         // (q2, q6) * s
-    const uint32_t h3 = h2_mul(h2_fma(t3, R16, N72), s2);      // (q3, q7) * s
-    o[0] = __byte_perm(h0, h1, 0x5410);  // (q0, q1)
-    o[1] = __byte_perm(h2, h3, 0x5410);  // (q2, q3)
-    o[2] = __byte_perm(h0, h1, 0x7632);  // (q4, q5)
-    o[3] = __byte_perm(h2, h3, 0x7632);  // (q6, q7)
+    const uint32_t ONE_R16 = 0x2C003C00u;   // (1, 1/16)
+    const uint32_t BIAS = 0xD480E408u;      // (-1032, -72)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = __byte_perm(v, 0u, 0x4040u | (j << 8) | j);   // byte j in both halves
+        uint32_t tv;
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(tv) : "r"(b), "r"(0x00F0000Fu), "r"(0x64806408u));
+        o[j] = h2_mul(h2_fma(tv, ONE_R16, BIAS), s2);
+    }
 }
 
 }  // namespace qg

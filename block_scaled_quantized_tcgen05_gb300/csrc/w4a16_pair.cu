@@ -256,9 +256,11 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         int nxt_ti = KG > 1 ? 0 : 1, nxt_g = KG > 1 ? 1 : 0;
         const uint8_t *p1 = total > 0 ? group_ptr(nxt_ti, nxt_g) : nullptr;
         uint4 nxt = p1 ? ld_nc_v4(p1) : unit;
-        uint32_t stage = 0, phase = 0;
-        for (int it = 0; it < total; ++it) {
-            const int ti = it / KT, kt = it - ti * KT;
+        // each warp walks only its own k-tiles, every other one (KT is a multiple of SPG >= 4, so
+        // both parities visit every scale group in order)
+        uint32_t stage = static_cast<uint32_t>(parity), phase = 0;
+        int ti = 0, kt = parity;
+        for (int it = parity; it < total; it += 2) {
             const int g = kt / SPG;
             if (ti != cur_ti || g != cur_g) {    // move to the next scale group, prefetch one more
                 cur = nxt;
@@ -271,36 +273,35 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const uint8_t *pn = group_ptr(nxt_ti, nxt_g);
                 nxt = pn ? ld_nc_v4(pn) : unit;
             }
-            if ((it & 1) == parity) {
-                if (!mbar_wait(raw_full(stage), phase, timeout_ns)) {
-                    if (lane == 0) atomicOr(err, ERR_PRODUCER);
-                    break;
-                }
-                tc_fence_after();   // the MMAs that last read this TMEM slot have completed
-                const uint8_t *raw = smem + OFF_RAW + stage * RAW_BYTES + r * (BK / 2);
-                const uint4 lo = *reinterpret_cast<const uint4 *>(raw);        // k  0..31
-                const uint4 hi = *reinterpret_cast<const uint4 *>(raw + 16);   // k 32..63
-                // this stage's two block scales: bytes 2 (kt % 8), + 1 of the group (UE8M0), or
-                // the fp16 pair in word kt % 4 (fp16 scales)
-                const int sbyte = SB == 1 ? (kt & 7) * 2 : (kt & 3) * 4;
-                const int wsel = sbyte >> 2;
-                const uint32_t word = wsel == 0 ? cur.x : wsel == 1 ? cur.y : wsel == 2 ? cur.z : cur.w;
-                uint32_t out[32];
-                if constexpr (SB == 2) {
+            if (!mbar_wait(raw_full(stage), phase, timeout_ns)) {
+                if (lane == 0) atomicOr(err, ERR_PRODUCER);
+                break;
+            }
+            tc_fence_after();   // the MMAs that last read this TMEM slot have completed
+            const uint8_t *raw = smem + OFF_RAW + stage * RAW_BYTES + r * (BK / 2);
+            const uint4 lo = *reinterpret_cast<const uint4 *>(raw);        // k  0..31
+            const uint4 hi = *reinterpret_cast<const uint4 *>(raw + 16);   // k 32..63
+            // this stage's two block scales: bytes 2 (kt % 8), + 1 of the group (UE8M0), or
+            // the fp16 pair in word kt % 4 (fp16 scales)
+            const int sbyte = SB == 1 ? (kt & 7) * 2 : (kt & 3) * 4;
+            const int wsel = sbyte >> 2;
+            const uint32_t word = wsel == 0 ? cur.x : wsel == 1 ? cur.y : wsel == 2 ? cur.z : cur.w;
+            uint32_t out[32];
+            if constexpr (SB == 2) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t s2 = __byte_perm(word, 0u, h ? 0x3232u : 0x1010u);
-                        const uint4 d = h ? hi : lo;
-                        const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t s2 = __byte_perm(word, 0u, h ? 0x3232u : 0x1010u);
+                    const uint4 d = h ? hi : lo;
+                    const uint32_t words[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint32_t o[4];
-                            i4x8_to_f16(words[w], s2, o);   // exact q, then one rounding of q*s
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t o[4];
+                        i4x8_to_f16(words[w], s2, o);   // exact q, then one rounding of q*s
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
-                        }
+                        for (int j = 0; j < 4; ++j) out[16 * h + 4 * w + j] = o[j];
                     }
-                } else {
+                }
+            } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t e = (word >> (8 * ((sbyte & 3) + h))) & 0xFFu;
@@ -327,18 +328,22 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         }
                     }
                 }
-                }
-                tmem_st_32x32b_x32(tmem_base + ((q * 32) << 16) + A_COL0 + stage * A_COLS, out);
-                tmem_wait_st();
-                tc_fence_before();
-                // the raw weights were read through the generic proxy; the slot's next fill is a TMA write
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * stage);
             }
-            if (++stage == STAGES) {
-                stage = 0;
+            tmem_st_32x32b_x32(tmem_base + ((q * 32) << 16) + A_COL0 + stage * A_COLS, out);
+            tmem_wait_st();
+            tc_fence_before();
+            // the raw weights were read through the generic proxy; the slot's next fill is a TMA write
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed_cluster(lead_full + 8u * stage);
+            stage += 2;
+            if (stage >= STAGES) {
+                stage -= STAGES;
                 phase ^= 1;
+            }
+            if ((kt += 2) >= KT) {
+                kt -= KT;
+                ++ti;
             }
         }
     } else {
