@@ -217,12 +217,13 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                                  ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                                  : 0;
         const int total = my_tiles * KT;
+        // k-tiles are issued and consumed in order: tile and k index kept as running counters
+        int iss_tile = static_cast<int>(blockIdx.x), iss_kt = 0, iss_mb = 0, iss_nb = 0;
+        if (total > 0) tile_coords(iss_tile, tiles_m, tiles_n, iss_mb, iss_nb);
         auto issue = [&](int it) {
             if (it < total) {
-                const int tile = blockIdx.x + (it / KT) * gridDim.x;
-                const int kt = it % KT;
-                int mb, nb;
-                tile_coords(tile, tiles_m, tiles_n, mb, nb);
+                const int kt = iss_kt;
+                const int nb = iss_nb;
                 const uint32_t rs = sb + OFF_RAW + (it % RAW) * RAW_SLOT_BYTES;
                 const int blk = kt * 2 + h;                     // scale block index along K
 #pragma unroll
@@ -237,6 +238,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                         cp_async_4_full(rs + RAW_DATA_BYTES + (i * CONV_THREADS + ct) * 4, ssrc);
                     }
                 }
+                if (++iss_kt == KT) {
+                    iss_kt = 0;
+                    iss_tile += static_cast<int>(gridDim.x);
+                    if (it + 1 < total) tile_coords(iss_tile, tiles_m, tiles_n, iss_mb, iss_nb);
+                }
             }
             cp_async_commit();
         };
@@ -244,8 +250,9 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
         for (int p = 0; p < RAW; ++p) issue(p);
         uint32_t stage = 0, phase = 0;
         bool ok = true;
+        int kt = 0, cur_tile = static_cast<int>(blockIdx.x), mb_cur = 0, nb_cur = 0;
+        if (!SF_VEC && total > 0) tile_coords(cur_tile, tiles_m, tiles_n, mb_cur, nb_cur);
         for (int it = 0; it < total; ++it) {
-            const int kt = it % KT;
             cp_async_wait<RAW - 1>();
             if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
                 ok = false;
@@ -254,11 +261,6 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             const uint8_t *rs = smem + OFF_RAW + (it % RAW) * RAW_SLOT_BYTES;
             const uint32_t sB = sb + OFF_B + stage * B_BYTES;
             const int blk = kt * 2 + h;
-            int nb_cur = 0;
-            if constexpr (!SF_VEC) {
-                int mb_cur;
-                tile_coords(blockIdx.x + (it / KT) * gridDim.x, tiles_m, tiles_n, mb_cur, nb_cur);
-            }
 #pragma unroll
             for (int i = 0; i < UNITS; ++i) {
                 const uint4 d = *reinterpret_cast<const uint4 *>(rs + (i * CONV_THREADS + ct) * 16);
@@ -296,6 +298,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
+            }
+            if (++kt == KT) {
+                kt = 0;
+                cur_tile += static_cast<int>(gridDim.x);
+                if (!SF_VEC && it + 1 < total) tile_coords(cur_tile, tiles_m, tiles_n, mb_cur, nb_cur);
             }
         }
         cp_async_wait<0>();

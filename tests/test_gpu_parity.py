@@ -283,6 +283,30 @@ def test_w4a16_pair_path_ragged(dev, orc, M, N, K):
     _check(C, res, orc, what=f"w4a16 pair {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("scale_pad", [0, 9])
+def test_w4a16_one_cta_route_several_tiles_per_cta(dev, orc, scale_pad):
+    """K % 512 != 0 takes the one-CTA route with cp.async staging; 16 x 10 = 160 tiles of
+    128 x 256 on at most 152 CTAs, so some CTAs walk two tiles and the tile and k counters roll
+    over.  scale_pad = 9: scale rows 9 bytes apart (not 4-byte aligned), the byte-load instance."""
+    M, N, K = 2048, 2560, 256
+    nblk = K // 32
+    d = synth.w4a16_inputs(M, N, K, seed=1234 + scale_pad)
+    if scale_pad:
+        s_full = torch.full((N, scale_pad), 255, dtype=torch.uint8)
+        s_full[:, :nblk] = d["sw"]
+        sv = s_full.to(dev)[:, :nblk]
+    else:
+        sv = d["sw"].to(dev)
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), sv)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(d["a"].to(dev), W, C)
+    rows = np.concatenate([np.arange(0, 8), np.arange(M - 8, M),
+                           np.sort(np.random.default_rng(3).choice(M, 48, replace=False))])
+    res = orc.w4a16(d["a"].numpy()[rows], d["w"].numpy(), d["sw"].numpy())
+    _check(C[torch.from_numpy(rows).to(dev)], res, orc, what=f"w4a16 one-CTA route lds pad {scale_pad}")
+    assert not torch.isnan(C).any()
+
+
 def test_w4a16_scales_outside_fused_window(dev, orc):
     """Scale exponents on both sides of the fused conversion's window (117..132) take the exact
     general path; every block gets one of 104, 110, 116, 117, 132, 133, 139."""
