@@ -105,9 +105,49 @@ __device__ __forceinline__ bool has_special_byte(uint32_t w) {
     return (z | f) != 0u;
 }
 
-// Up to four stages of one scale group (stages 4 G0 .. 4 G0 + 3 that exist).  e0[f] / e1[f] hold the
-// scale bytes of rows 16 f + g / 16 f + g + 8 for this warp's block of each stage (stage j in byte
-// j).  EXACT selects the decode for the whole group: the shift decode builds 2^(e-127) by moving the
+// The products of one stage: this warp's 32-block for all 64 rows, accumulated into acc with the
+// stage's block scales (byte sh / 8 of e0[f], e1[f]).  Plain shared loads and pure MMAs, so two calls
+// in a row can be interleaved by the compiler.
+template <int NH, bool EXACT>
+__device__ __forceinline__ void stage_math(float (&acc)[4][NH][4], const uint8_t *st, uint32_t wrow,
+                                           uint32_t xoff, const uint32_t (&e0)[4],
+                                           const uint32_t (&e1)[4], uint32_t sh) {
+    const uint8_t *xs = st + ROWS * KC;
+    const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
+    uint4 xb = xa;
+    if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+        const uint2 wa = *reinterpret_cast<const uint2 *>(st + wrow + f * 16 * 128);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(st + wrow + (f * 16 + 8) * 128);
+        uint32_t a0[4], a1[4];
+        i8x4_to_f16x2(wa.x, a0[0], a0[2]);
+        i8x4_to_f16x2(wb.x, a0[1], a0[3]);
+        i8x4_to_f16x2(wa.y, a1[0], a1[2]);
+        i8x4_to_f16x2(wb.y, a1[1], a1[3]);
+        const uint32_t b0 = (e0[f] >> sh) & 0xFFu, b1 = (e1[f] >> sh) & 0xFFu;
+        const float sa = EXACT ? ue8m0_to_f32(b0) : __uint_as_float(b0 << 23);
+        const float sbv = EXACT ? ue8m0_to_f32(b1) : __uint_as_float(b1 << 23);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const uint4 xv = h == 0 ? xa : xb;
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            float p[4], q[4];
+            mma_16816(p, a0, xv.x, xv.y, z);
+            mma_16816(q, a1, xv.z, xv.w, p);
+            acc[f][h][0] = fmaf(sa, q[0], acc[f][h][0]);
+            acc[f][h][1] = fmaf(sa, q[1], acc[f][h][1]);
+            acc[f][h][2] = fmaf(sbv, q[2], acc[f][h][2]);
+            acc[f][h][3] = fmaf(sbv, q[3], acc[f][h][3]);
+        }
+    }
+}
+
+// Up to four stages of one scale group (stages 4 G0 .. 4 G0 + 3 that exist), taken two at a time:
+// both are waited for, their products formed together (twice the independent work between the
+// warp's waits), added to acc in stage order, and both handed back.  e0[f] / e1[f] hold the scale
+// bytes of rows 16 f + g / 16 f + g + 8 for this warp's block of each stage (stage j in byte j).
+// EXACT selects the decode for the whole group: the shift decode builds 2^(e-127) by moving the
 // byte into the fp32 exponent field; codes 0x00 (subnormal 2^-127) and 0xFF (NaN) need the exact one.
 template <int NH, bool EXACT, int STAGES>
 __device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t *smem, uint32_t sb,
@@ -116,55 +156,34 @@ __device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t 
                                           const uint32_t (&e1)[4], uint32_t &stage, uint32_t &phase,
                                           int lane, uint64_t timeout_ns) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 4; j += 2) {
         if (j >= nst) break;
-        const uint32_t full = sb + off_bar + 8u * stage, empty = full + 8u * STAGES;
-        if (!mbar_wait(full, phase, timeout_ns)) return false;
-        // Reconverge before the warp-wide mma.sync.aligned: lane 0 alone took the arrive branch of the
-        // previous stage and every lane polls the barrier on its own.
-        __syncwarp();
-        const uint8_t *st = smem + stage * stage_bytes;    // plain shared loads, schedulable
-        const uint8_t *xs = st + ROWS * KC;
-        const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
-        uint4 xb = xa;
-        if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
-        const uint32_t sh = 8u * static_cast<uint32_t>(j);
-#pragma unroll
-        for (int f = 0; f < 4; ++f) {
-            const uint2 wa = *reinterpret_cast<const uint2 *>(st + wrow + f * 16 * 128);
-            const uint2 wb = *reinterpret_cast<const uint2 *>(st + wrow + (f * 16 + 8) * 128);
-            uint32_t a0[4], a1[4];
-            i8x4_to_f16x2(wa.x, a0[0], a0[2]);
-            i8x4_to_f16x2(wb.x, a0[1], a0[3]);
-            i8x4_to_f16x2(wa.y, a1[0], a1[2]);
-            i8x4_to_f16x2(wb.y, a1[1], a1[3]);
-            const uint32_t b0 = (e0[f] >> sh) & 0xFFu, b1 = (e1[f] >> sh) & 0xFFu;
-            const float sa = EXACT ? ue8m0_to_f32(b0) : __uint_as_float(b0 << 23);
-            const float sbv = EXACT ? ue8m0_to_f32(b1) : __uint_as_float(b1 << 23);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                const uint4 xv = h == 0 ? xa : xb;
-                const float z[4] = {0.f, 0.f, 0.f, 0.f};
-                float p[4], q[4];
-                mma_16816(p, a0, xv.x, xv.y, z);
-                mma_16816(q, a1, xv.z, xv.w, p);
-                acc[f][h][0] = fmaf(sa, q[0], acc[f][h][0]);
-                acc[f][h][1] = fmaf(sa, q[1], acc[f][h][1]);
-                acc[f][h][2] = fmaf(sbv, q[2], acc[f][h][2]);
-                acc[f][h][3] = fmaf(sbv, q[3], acc[f][h][3]);
-            }
+        const bool two = j + 1 < nst;
+        uint32_t stage2 = stage + 1, phase2 = phase;
+        if (stage2 == STAGES) {
+            stage2 = 0;
+            phase2 ^= 1;
         }
-        // Hand the stage back.  Its operands were read through the generic proxy and the producer's next
-        // TMA writes it through the async proxy: each lane orders its reads before that write with a
-        // proxy fence (measured on this GPU: without it, whole 64-row blocks picked up data of the next
-        // fill now and then).
+        const uint32_t full = sb + off_bar + 8u * stage, full2 = sb + off_bar + 8u * stage2;
+        if (!mbar_wait(full, phase, timeout_ns)) return false;
+        if (two && !mbar_wait(full2, phase2, timeout_ns)) return false;
+        // Reconverge before the warp-wide mma.sync.aligned: lane 0 alone took the arrive branch of the
+        // previous stages and every lane polls the barriers on its own.
+        __syncwarp();
+        stage_math<NH, EXACT>(acc, smem + stage * stage_bytes, wrow, xoff, e0, e1, 8u * j);
+        if (two) stage_math<NH, EXACT>(acc, smem + stage2 * stage_bytes, wrow, xoff, e0, e1, 8u * (j + 1));
+        // Hand the stages back.  Their operands were read through the generic proxy and the producer's
+        // next TMA writes them through the async proxy: each lane orders its reads before that write
+        // with a proxy fence (measured on this GPU: without it, whole 64-row blocks picked up data of
+        // the next fill now and then).
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty);
-        if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+        if (lane == 0) {
+            mbar_arrive(full + 8u * STAGES);
+            if (two) mbar_arrive(full2 + 8u * STAGES);
         }
+        stage = two ? (stage2 + 1 == STAGES ? 0 : stage2 + 1) : stage2;
+        phase = two ? (stage2 + 1 == STAGES ? phase2 ^ 1 : phase2) : phase2;
     }
     return true;
 }
