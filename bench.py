@@ -364,8 +364,9 @@ def run_ours(args, ws, rank, local):
                               "frac_of_fp8_spec_4500": round(mx_tflops / SPEC_FP8_TFLOPS, 4)}
     value = (whole_job_rate(ws, flops["mxfp8"], mean["mxfp8"]) / 1e12
              if mx_tflops is not None else None)
-    # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM)
-    launches = sum(2 if k.startswith("mxfp") else 1 for k in kernels) * args.steps
+    # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM), one
+    # qgemm_w4a16 call two (the GEMM + the outlier-row pass)
+    launches = sum(2 if k.startswith("mxfp") or k == "w4a16" else 1 for k in kernels) * args.steps
     line = {
         "metric": METRIC, "value": round(value, 2) if value is not None else None,
         "unit": "TFLOP/s", "n_gpus": ws,

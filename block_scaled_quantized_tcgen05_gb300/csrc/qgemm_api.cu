@@ -430,7 +430,11 @@ static qgemm_status w4a16_impl(const void *A_f16, int64_t lda, int64_t M, const 
     e = qgi::launch_w4a16(static_cast<const __half *>(A_f16), lda, (int)M, W,
                           static_cast<__half *>(C_f16), ldc, ctx, &enc);
     if (!enc) return QGEMM_ERR_CUDA;
-    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16 launch");
+    if (e != cudaSuccess) return cuda_fail(e, "qgemm_w4a16 launch");
+    // rows with nonzero weights under scale bytes outside the fold window, from the definition
+    e = qgi::launch_w4a16_outliers(static_cast<const __half *>(A_f16), lda, (int)M, W,
+                                   static_cast<__half *>(C_f16), ldc, ctx);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_w4a16 outlier-row launch");
 }
 
 static qgemm_status w4a16_f16s_impl(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,

@@ -76,6 +76,11 @@ cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64
                             bool *encode_ok);
 cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor *W, __half *C,
                          int64_t ldc, const LaunchCtx &ctx, bool *encode_ok);
+// Exact recomputation of the outlier rows of an int4 view (a nonzero weight in a block whose
+// UE8M0 byte is outside 103..139 and not 255) after launch_w4a16 on the same stream, under the
+// same ctx.epi (w4a16_outlier.cu).
+cudaError_t launch_w4a16_outliers(const __half *A, int64_t lda, int M, const qgemm_tensor *W,
+                                  __half *C, int64_t ldc, const LaunchCtx &ctx);
 // CTA-pair W4A16 with the dequantised weights in TMEM (w4a16_pair.cu).
 bool w4a16_pair_eligible(int M, const qgemm_tensor *W);
 cudaError_t launch_w4a16_pair(const __half *A, int64_t lda, int M, const qgemm_tensor *W,

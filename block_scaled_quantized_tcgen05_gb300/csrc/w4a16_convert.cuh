@@ -2,13 +2,73 @@
 //
 // A packed word holds 8 int4 weights of one row, k = 8w .. 8w + 7, even k in the low nibble of
 // each byte (two's complement).  The fp16 weight is q * 2^(e - 127) with e the row's UE8M0 scale
-// byte for that 32-block of k; it is exact for 103 <= e <= 139 (fp16 normal and subnormal range
-// for |q| <= 8).  Output words are fp16x2 pairs in k order (low half = even k).
+// byte for that 32-block of k.  That product is an fp16 value for every q in -8..7 exactly when
+// 103 <= e <= 139 (the fold window: 2^-24 is the smallest fp16 subnormal, 8 * 2^12 the largest
+// power of two times 8 below 65504).  Output words are fp16x2 pairs in k order (low half = even k).
+//
+// Outside the window the converters write 0 (and NaN for the NaN code 255, since q * NaN is NaN
+// for every q, zero included).  A block that holds only zero weights is then still exact; a row
+// with a nonzero weight in an out-of-window block (an "outlier row", w4_row_is_outlier) is
+// recomputed exactly by w4a16_outlier_kernel, which runs after the GEMM on the same stream.
 #pragma once
 
 #include <cstdint>
 
 namespace qg {
+
+constexpr uint32_t W4_FOLD_LO = 103;   // fold window of UE8M0 bytes, inclusive
+constexpr uint32_t W4_FOLD_HI = 139;
+constexpr uint32_t UE8M0_NAN = 255;
+
+// A byte outside the fold window that is not the NaN code.
+__device__ __forceinline__ bool w4_byte_outside(uint32_t e) {
+    return e != UE8M0_NAN && (e - W4_FOLD_LO) > (W4_FOLD_HI - W4_FOLD_LO);
+}
+
+// True when the 32-block b of a packed int4 row (16 bytes at wrow + 16 b, 16-byte aligned) holds
+// a nonzero weight.  int4 zero is the nibble 0, so the bytes are all zero exactly when every q is.
+__device__ __forceinline__ bool w4_block_live(const uint8_t *wrow, int b) {
+    const uint4 d = __ldg(reinterpret_cast<const uint4 *>(wrow + 16 * b));
+    return (d.x | d.y | d.z | d.w) != 0u;
+}
+
+// Outlier row: some block's scale byte lies outside the fold window (and is not 255) while the
+// block holds a nonzero weight.  srow: the row's nblk scale bytes; wrow: its packed weights.
+// Sixteen (or four) scale bytes are tested at a time when srow is 16- (or 4-) byte aligned.
+__device__ __forceinline__ uint32_t w4_outside4(uint32_t w) {
+    // per byte: 0xFF where e - 103 (mod 256) > 36 and e != 255
+    return __vcmpgtu4(__vsub4(w, 0x67676767u), 0x24242424u) & ~__vcmpeq4(w, 0xFFFFFFFFu);
+}
+
+__device__ __forceinline__ bool w4_row_is_outlier(const uint8_t *srow, const uint8_t *wrow,
+                                                  int nblk) {
+    int b = 0;
+    if ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0) {
+        for (; b + 16 <= nblk; b += 16) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(srow + b));
+            if ((w4_outside4(v.x) | w4_outside4(v.y) | w4_outside4(v.z) | w4_outside4(v.w)) == 0u)
+                continue;
+            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t out = w4_outside4(ws[i]);
+                for (int j = 0; j < 4; ++j)
+                    if (((out >> (8 * j)) & 0xFFu) && w4_block_live(wrow, b + 4 * i + j)) return true;
+            }
+        }
+    }
+    if ((reinterpret_cast<uintptr_t>(srow + b) & 3u) == 0) {
+        for (; b + 4 <= nblk; b += 4) {
+            const uint32_t out = w4_outside4(__ldg(reinterpret_cast<const uint32_t *>(srow + b)));
+            if (out) {
+                for (int j = 0; j < 4; ++j)
+                    if (((out >> (8 * j)) & 0xFFu) && w4_block_live(wrow, b + j)) return true;
+            }
+        }
+    }
+    for (; b < nblk; ++b)
+        if (w4_byte_outside(__ldg(srow + b)) && w4_block_live(wrow, b)) return true;
+    return false;
+}
 
 __device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t r;
@@ -21,15 +81,14 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     return r;
 }
 
-// fp16 bits of 2^(e-127) for e in [103, 142] (subnormals below 2^-14); outside that range the
-// nearest representable behaviour: 0 below, +inf above.
+// fp16x2 scale the general conversion multiplies by: 2^(e-127) inside the fold window
+// (subnormal below 2^-14), NaN for 255, 0 for every other byte (see the file comment).
 __device__ __forceinline__ uint32_t ue8m0_to_f16x2(uint32_t e) {
-    const int x = static_cast<int>(e) - 127;
     uint32_t h;
-    if (x > 15) h = 0x7C00u;
-    else if (x >= -14) h = static_cast<uint32_t>(x + 15) << 10;
-    else if (x >= -24) h = 1u << (x + 24);
-    else h = 0u;
+    if (e == UE8M0_NAN) h = 0x7E00u;
+    else if (w4_byte_outside(e)) h = 0u;
+    else if (e >= 113u) h = (e - 112u) << 10;   // 2^(e-127) >= 2^-14: normal
+    else h = 1u << (e - 103u);                  // 2^-24 .. 2^-15: subnormal
     return h | (h << 16);
 }
 

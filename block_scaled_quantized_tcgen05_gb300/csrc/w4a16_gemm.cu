@@ -16,7 +16,8 @@
 //              turn 32 nibbles into fp16 (q + 8 placed in the mantissa of 1024, minus 1032; the
 //              high nibble as 1024 + 16 (q + 8), times 1/16, minus 72), multiply by the fp16
 //              power of two 2^(e-127) and store 16-byte chunks at their swizzled position.
-// The fp16 weight q * 2^(e-127) is exact for 103 <= e <= 139.
+// The fp16 weight q * 2^(e-127) is exact for 103 <= e <= 139; other bytes give 0 (NaN for 255)
+// and the rows where that matters are rewritten by w4a16_outlier.cu (w4a16_convert.cuh).
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -46,7 +47,8 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_RAW = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_BAR = OFF_RAW + RAW * RAW_SLOT_BYTES;
 constexpr uint32_t OFF_SLOT = OFF_BAR + (2 * STAGES + 5) * 8;
-constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
+constexpr uint32_t OFF_FLAGS = OFF_SLOT + 16;   // [2][BN] outlier-column flags (accumulate)
+constexpr uint32_t SMEM_BYTES = OFF_FLAGS + 2 * BN + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // kind::f16, D fp32, A and B fp16, both K-major, N = 256, M = 128.
@@ -65,6 +67,72 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- accumulate epilogue with outlier rows --------------------------------------------------
+// When the output is accumulated (C = relu?(A W^T + C_old)), the columns of outlier weight rows
+// (w4_row_is_outlier) are neither read nor written here: w4a16_outlier_kernel computes them from
+// the old C afterwards.  The four epilogue warps mark the tile's 256 weight rows in shared memory
+// (flags[c] != 0: skip column n0 + c) before the tile's accumulator is ready.
+__device__ __forceinline__ void mark_outlier_cols(uint8_t *flags, int t, int n0, int N, int K,
+                                                  const uint8_t *W, int64_t ldw,
+                                                  const uint8_t *SW, int64_t ldsw) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = t + 128 * h;
+        const int n = n0 + c;
+        flags[c] = (n < N && w4_row_is_outlier(SW + static_cast<int64_t>(n) * ldsw,
+                                               W + static_cast<int64_t>(n) * ldw, K / 32))
+                       ? 1 : 0;
+    }
+}
+
+// Barrier of the four epilogue warps (named barrier 2, 128 threads) that also ANDs `ok` over
+// them: every epilogue thread reaches it once per tile, so a wait that ran out in one warp
+// stops all four together.
+__device__ __forceinline__ bool epi_bar_and(bool ok) {
+    uint32_t all_ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(all_ok)
+        : "r"(ok ? 1u : 0u)
+        : "memory");
+    return all_ok != 0;
+}
+
+// Drain one 128 x BN accumulator with C = relu?(acc + C_old), skipping flagged columns (element
+// stores; used only for tiles that hold an outlier column).  Every lane arrives on tmem_empty
+// after the last TMEM read, as epilogue_tile does.
+__device__ __forceinline__ void epilogue_acc_masked(uint32_t tmem_base, uint32_t q, uint32_t lane,
+                                                    __half *C, int64_t ldc, int m0, int n0, int M,
+                                                    int N, uint32_t tmem_empty, int epi,
+                                                    const uint8_t *flags) {
+    const int row = m0 + static_cast<int>(q * 32 + lane);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+        }
+        const uint32_t skip = __ballot_sync(0xFFFFFFFFu, flags[ch * 32 + lane] != 0);
+        if (row >= M) continue;
+        __half *crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int col = n0 + ch * 32 + i;
+            if (col < N && !((skip >> i) & 1u)) {
+                float x = __uint_as_float(v[i]) + __half2float(crow[col]);
+                if (epi & EPI_RELU_BIT) x = fmaxf(x, 0.0f);
+                crow[col] = __float2half_rn(x);
+            }
+        }
+    }
 }
 
 template <bool SF_VEC>
@@ -193,18 +261,35 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
     } else if (warp < 6) {
         // ------------------------------------------------------------------- epilogue
         const uint32_t q = warp & 3;
+        const bool acc_mode = (epi & EPI_ACC_BIT) != 0;
         uint32_t acc_it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
-            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
+            uint8_t *flags = smem + OFF_FLAGS + ab * BN;
+            if (acc_mode)
+                mark_outlier_cols(flags, static_cast<int>(threadIdx.x) - 64, nb * BN, N, K, W, ldw,
+                                  SW, ldsw);
+            bool got = mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns);
+            if (acc_mode) got = epi_bar_and(got);
+            if (!got) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), 0u, epi);
+            bool masked = false;
+            if (acc_mode) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    masked |= __any_sync(0xFFFFFFFFu, flags[c * 32 + lane] != 0);
+            }
+            if (masked)
+                epilogue_acc_masked(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                    tmem_empty(ab), epi, flags);
+            else
+                epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                  c_vec != 0, tmem_empty(ab), 0u, epi);
             ++acc_it;
         }
     } else {
@@ -334,12 +419,15 @@ constexpr uint32_t T_OFF_EPI = T_OFF_STG + 2 * T_STG;   // 4 epilogue warps x 2 
 constexpr uint32_t T_OFF_BAR = T_OFF_EPI + 4 * 2048;
 // raw_full[S], conv_full[S], empty[S], tmem_full[2], tmem_empty[2], drain, then the TMEM slot
 constexpr uint32_t T_OFF_SLOT = T_OFF_BAR + (3 * STAGES + 5) * 8;
-constexpr uint32_t T_SMEM_BYTES = T_OFF_SLOT + 16 + 1024;
+constexpr uint32_t T_OFF_FLAGS = T_OFF_SLOT + 16;
+constexpr uint32_t T_SMEM_BYTES = T_OFF_FLAGS + 2 * BN + 1024;
 static_assert(T_SMEM_BYTES <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(T_THREADS, 1)
 w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                 const __grid_constant__ CUtensorMap tmS, __half *__restrict__ C, int64_t ldc,
+                 const __grid_constant__ CUtensorMap tmS, const uint8_t *__restrict__ W,
+                 int64_t ldw, const uint8_t *__restrict__ SW, int64_t ldsw,
+                 __half *__restrict__ C, int64_t ldc,
                  int c_vec, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
@@ -475,18 +563,36 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp < 6) {
         // ------------------------------------------------------------------- epilogue
         const uint32_t q = warp & 3;
+        const bool acc_mode = (epi & EPI_ACC_BIT) != 0;
         uint32_t acc_it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
-            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
+            uint8_t *flags = smem + T_OFF_FLAGS + ab * BN;
+            if (acc_mode)
+                mark_outlier_cols(flags, static_cast<int>(threadIdx.x) - 64, nb * BN, N, K, W, ldw,
+                                  SW, ldsw);
+            bool got = mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns);
+            if (acc_mode) got = epi_bar_and(got);
+            if (!got) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), sb + T_OFF_EPI + (warp - 2) * 2048, epi);
+            bool masked = false;
+            if (acc_mode) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    masked |= __any_sync(0xFFFFFFFFu, flags[c * 32 + lane] != 0);
+            }
+            if (masked)
+                epilogue_acc_masked(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                    tmem_empty(ab), epi, flags);
+            else
+                epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                  c_vec != 0, tmem_empty(ab), sb + T_OFF_EPI + (warp - 2) * 2048,
+                                  epi);
             ++acc_it;
         }
     } else {
@@ -597,7 +703,8 @@ cudaError_t launch_w4a16(const __half *A, int64_t lda, int M, const qgemm_tensor
                                              T_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         w4a16_tma_kernel<<<grid, T_THREADS, T_SMEM_BYTES, ctx.stream>>>(
-            tmA, tmW, tmS, C, ldc, c_vec, M, N, K, ctx.epi, ctx.err, ctx.timeout_ns);
+            tmA, tmW, tmS, W->data, W->ld, W->scales, W->lds, C, ldc, c_vec, M, N, K, ctx.epi,
+            ctx.err, ctx.timeout_ns);
         return cudaGetLastError();
     }
     const bool sf_vec = reinterpret_cast<uintptr_t>(W->scales) % 4 == 0 && W->lds % 4 == 0;

@@ -30,7 +30,9 @@
 // stage on its full barrier, which collects both CTAs' activation bytes and one relaxed arrival
 // from each converter warp of both CTAs after its tcgen05.st completed; commits are multicast;
 // every wait is bounded.  Used for K % 512 == 0 with 16-byte aligned scale rows (scales are read
-// 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.
+// 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.  Scale bytes outside the
+// fold window convert to zero weights (w4a16_convert.cuh); when the output is accumulated, the
+// columns of outlier rows are left to w4a16_outlier.cu, which runs next and needs the old C.
 //
 // The same kernel, instantiated with SB = 2, runs the custom-format escape hatch: int4 weights
 // with arbitrary fp16 scales per 32-block ("TensorOps: quantized matmul ...", "M2 = block-32 fp16
@@ -94,7 +96,8 @@ template <int SB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ CUtensorMap tmC, int c_tma,
-                  const uint8_t *__restrict__ scales, int64_t lds, __half *__restrict__ C,
+                  const uint8_t *__restrict__ scales, int64_t lds,
+                  const uint8_t *__restrict__ wdata, int64_t ldw, __half *__restrict__ C,
                   int64_t ldc, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
@@ -357,13 +360,21 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         for (int tile = pair; tile < num_tiles; tile += npairs) {
             int wb, tb;
             tile_coords(tile, tiles_w, tiles_t, wb, tb);
+            const int n0 = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32);
+            const int n = n0 + static_cast<int>(lane);
+            // Accumulating: an outlier row's column is left to w4a16_outlier_kernel, which needs
+            // the old C (checked while the tile's MMAs run).
+            bool skip = false;
+            if constexpr (SB == 1) {
+                if ((epi & EPI_ACC_BIT) && n < N)
+                    skip = w4_row_is_outlier(scales + static_cast<int64_t>(n) * lds,
+                                             wdata + static_cast<int64_t>(n) * ldw, K / 32);
+            }
             if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
             tc_fence_after();
-            const int n0 = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32);
-            const int n = n0 + static_cast<int>(lane);
             const int m0 = tb * BT + static_cast<int>(half) * (BT / 2);
             const uint32_t stg = sb + OFF_EPI + (warp - 2) * EPI_BYTES;
             if (c_tma) {   // the previous tile's stores have finished reading the staging
@@ -424,7 +435,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     for (int c = 0; c < 32; ++c)
                         st_shared_u16(stg + ch * 2048 + c * 64 + lane * 2,
                                       __half_as_ushort(__float2half_rn(__uint_as_float(v[c]))));
-                } else if (n < N) {
+                } else if (n < N && !skip) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int m = m0 + ch * 32 + c;
@@ -491,8 +502,8 @@ cudaError_t launch_pair_impl(const __half *A, int64_t lda, int M, const qgemm_te
     int pairs = ctx.num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     w4a16_pair_kernel<SB><<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmX, tmW, tmC, c_tma, W->scales, W->lds, C, ldc, M, N, K, ctx.epi, ctx.err,
-        ctx.timeout_ns);
+        tmX, tmW, tmC, c_tma, W->scales, W->lds, W->data, W->ld, C, ldc, M, N, K, ctx.epi,
+        ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
 }
 

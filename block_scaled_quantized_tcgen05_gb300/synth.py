@@ -222,6 +222,91 @@ def w4a16_f16s_inputs(M: int, N: int, K: int, seed: int, w_std: float = 0.02):
             "M": M, "N": N, "K": K}
 
 
+W4_SCALE_KINDS = 9
+
+
+def w4a16_scale_extremes_inputs(M: int, N: int, K: int, seed: int):
+    """int4 weights whose UE8M0 scale bytes span the whole byte range, within rows and across
+    them, with activations shaped so that the outputs stay well inside the fp16 range.
+
+    Activations: N(0, 1) times 2^8 on even 32-blocks of k and times 2^-12 on odd ones, so a
+    block with a small scale byte is placed on an even block and one with a large byte on an
+    odd block.  Weight row n is of kind n % 9 (``kind`` in the result):
+      0  every block live, bytes in 103..117 (even blocks) / 118..139 (odd blocks);
+      1  kind 0 with four blocks emptied (all q = 0) under bytes from {0, 1, 60, 102, 140, 180, 254};
+      2  live even blocks under bytes 102, 60, 1 and 0 only (every other block emptied);
+      3  kind 0 plus one or two live odd blocks under bytes from {140, 143, 146};
+      4  kind 0 plus live {0, 1, 60, 102} (even), one live 140 or 146 (odd), empty 180 and 254;
+      5  kind 0 with one live block under byte 255 (NaN);
+      6  kind 0 with one empty block under byte 255;
+      7  kind 0 with one live odd block under byte 180 or 254 (overflows fp16);
+      8  every block live under byte 102.
+    Kinds 2, 3, 4, 7 and 8 hold nonzero weights in blocks whose byte is outside 103..139 and
+    not 255."""
+    g = generator(seed)
+    nblk = K // BLOCK
+    if nblk < 8:
+        raise ValueError("K must be at least 256")
+    even = torch.arange(nblk) % 2 == 0
+    amp = torch.where(even, 2.0 ** 8, 2.0 ** -12).repeat_interleave(BLOCK)
+    a = (normal((M, K), g) * amp).to(torch.float16)
+    q = torch.randint(-8, 8, (N, K), generator=g, dtype=torch.int8)
+    q[q == 0] = 1                              # every block of a live row holds nonzero weights
+    sw = torch.empty(N, nblk, dtype=torch.uint8)
+    sw[:, even] = torch.randint(103, 118, (N, int(even.sum())), generator=g, dtype=torch.uint8)
+    sw[:, ~even] = torch.randint(118, 140, (N, int((~even).sum())), generator=g, dtype=torch.uint8)
+    ev_idx = torch.nonzero(even).flatten()
+    od_idx = torch.nonzero(~even).flatten()
+
+    def pick(idx, n_pick):
+        return idx[torch.randperm(idx.numel(), generator=g)[:n_pick]]
+
+    def choice(vals, n_pick):
+        v = torch.tensor(vals, dtype=torch.uint8)
+        return v[torch.randint(0, len(vals), (n_pick,), generator=g)]
+
+    def empty_block(n, b):
+        q[n, b * BLOCK:(b + 1) * BLOCK] = 0
+
+    kind = torch.arange(N) % W4_SCALE_KINDS
+    for n in range(N):
+        k_ = int(kind[n])
+        if k_ == 1:
+            bs = pick(torch.arange(nblk), 4)
+            sw[n, bs] = choice([0, 1, 60, 102, 140, 180, 254], 4)
+            for b in bs.tolist():
+                empty_block(n, b)
+        elif k_ == 2:
+            bs = pick(ev_idx, 4)
+            sw[n, bs] = torch.tensor([102, 60, 1, 0], dtype=torch.uint8)
+            keep = set(bs.tolist())
+            for b in range(nblk):
+                if b not in keep:
+                    empty_block(n, b)
+        elif k_ == 3:
+            bs = pick(od_idx, 1 + int(torch.randint(0, 2, (1,), generator=g)))
+            sw[n, bs] = choice([140, 143, 146], bs.numel())
+        elif k_ == 4:
+            be = pick(ev_idx, 4)
+            sw[n, be] = torch.tensor([0, 1, 60, 102], dtype=torch.uint8)
+            bo = pick(od_idx, 3)
+            sw[n, bo] = torch.tensor([int(choice([140, 146], 1)), 180, 254], dtype=torch.uint8)
+            empty_block(n, int(bo[1]))
+            empty_block(n, int(bo[2]))
+        elif k_ == 5:
+            sw[n, int(pick(torch.arange(nblk), 1))] = 255
+        elif k_ == 6:
+            b = int(pick(torch.arange(nblk), 1))
+            sw[n, b] = 255
+            empty_block(n, b)
+        elif k_ == 7:
+            sw[n, int(pick(od_idx, 1))] = 180 if (n // W4_SCALE_KINDS) % 2 == 0 else 254
+        elif k_ == 8:
+            sw[n, :] = 102
+    return {"a": a.contiguous(), "w": pack_int4(q), "w_values": q, "sw": sw.contiguous(),
+            "kind": kind, "M": M, "N": N, "K": K}
+
+
 def attention_inputs(BH: int, Lq: int, Lk: int, d: int, seed: int, q_std: float = 1.0):
     """fp16 Q [BH, Lq, d], K and V [BH, Lk, d] from N(0, 1) (Q times q_std: a larger q_std makes
     the softmax rows peakier); scale 1/sqrt(d)."""

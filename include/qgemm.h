@@ -99,7 +99,9 @@ qgemm_status qgemm_create_tensor(qgemm_tensor **out, qgemm_dtype dt, int64_t row
 qgemm_status qgemm_tensor_slice(const qgemm_tensor *t, int64_t row0, int64_t nrows, int64_t k0,
                                 int64_t nk, qgemm_tensor **out);
 
-/* Free the view (host memory only; never touches device memory).  NULL is a no-op. */
+/* Free the view (host memory only; never touches device memory).  NULL is a no-op.
+ * Passage: the pages have no counterpart (a Metal tensor is reference-counted); a view here is a
+ * plain host object, so its owner frees it. */
 void qgemm_destroy_tensor(qgemm_tensor *t);
 
 /* Read back a view's fields (any out-pointer may be NULL). */
@@ -203,9 +205,15 @@ qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, vo
  *   A   device fp16 [M, K], row stride lda elements.
  *   W   QGEMM_INT4 view [N, K] with UE8M0 scales [N, K / 32].
  *   C   device fp16 [M, N], row stride ldc.
- * Numerics: each weight is dequantised to fp16 exactly as q * 2^(e - 127), which is exact for
- * scale bytes 103 <= e <= 139 (|w| between 2^-24 and 2^15); outside that range the dequantised
- * fp16 weight is rounded (or overflows to inf for e >= 141 and q = -8).
+ * Numerics: the defined product for every scale byte.  Inside the fold window 103 <= e <= 139
+ * each weight becomes the fp16 value q * 2^(e - 127) (exact: |w| lies in [2^-24, 2^15]) and the
+ * tensor cores form the fp32 sum.  Byte 255 is NaN and makes the row's outputs NaN (q * NaN is
+ * NaN for every q, zero included).  A block with any other byte contributes exactly zero when
+ * its weights are all zero; a weight row with a nonzero weight in such a block (an outlier row)
+ * is computed again by a second kernel on the same stream: fp32 partial sums per 32-block, each
+ * times its 2^(e - 127) and summed in fp64, one fp16 rounding (with the epilogue of the _ex call
+ * applied to that sum).  Outlier rows cost M * K fused multiply-adds each on the CUDA cores; the
+ * second kernel is launched by every call and, with no outlier row, only reads the scale plane.
  * Requirements: K % 64 == 0; A, C 16-byte aligned; lda, ldc multiples of 8; W data 16-byte
  * aligned with a 16-byte multiple row stride; any M, N.
  * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA. */
@@ -316,7 +324,11 @@ qgemm_status qgemm_w8_gemv_ex(const void *X_f16, int64_t ldx, int64_t M, const q
  * Errors: INVALID_ARG (null t or out); CUDA. */
 qgemm_status qgemm_dequant_debug(const qgemm_tensor *t, float *out, void *stream);
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).
+ * Passage: "Optimize custom machine learning operations with Metal tensors", section "Creating
+ * quantized tensors with scale factors" (a failed creation hands back an error object the caller
+ * can read) and "TileLang Metal Backend Internals", section 5.8 "Developer Checklist" (an
+ * unsupported shape should produce a clear error). */
 const char *qgemm_status_string(qgemm_status s);
 
 /* Detail of the last error returned on the calling thread (static per-thread buffer). */

@@ -164,3 +164,30 @@ def test_int4_f16_scale_encoder_matches_plain_restatement():
             assert s[r, b].item() == float(want_s)
             want_q = np.clip(np.round(blk / float(want_s)), -8, 7)       # half to even
             assert np.array_equal(q[r, 32 * b:32 * b + 32].numpy(), want_q.astype(np.int8))
+
+
+def test_w4a16_scale_extremes_row_kinds():
+    """The scale-extremes workload holds what its row kinds promise: live blocks (some nonzero
+    weight) under bytes outside 103..139 exactly in kinds 2, 3, 4, 7 and 8; byte 255 in kinds 5
+    and 6 (live in 5, emptied in 6); and bytes 0, 1, 60, 102, 140, 180, 254 all present."""
+    N, K = 90, 1024
+    d = synth.w4a16_scale_extremes_inputs(8, N, K, seed=3)
+    qv = d["w_values"].numpy().reshape(N, K // 32, 32)
+    sw = d["sw"].numpy().astype(np.int64)
+    kind = d["kind"].numpy()
+    live = (qv != 0).any(axis=2)
+    outside = ((sw < 103) | (sw > 139)) & (sw != 255)
+    has_live_outside = (live & outside).any(axis=1)
+    assert np.array_equal(has_live_outside, np.isin(kind, [2, 3, 4, 7, 8]))
+    nan_live = ((sw == 255) & live).any(axis=1)
+    nan_dead = ((sw == 255) & ~live).any(axis=1)
+    assert np.array_equal(nan_live, kind == 5) and np.array_equal(nan_dead, kind == 6)
+    for byte in (0, 1, 60, 102, 140, 180, 254, 255):
+        assert (sw == byte).any(), byte
+    # packing agrees with the values (even k in the low nibble)
+    p = d["w"].numpy()
+    lo = (p & 15).astype(np.int8)
+    hi = (p >> 4).astype(np.int8)
+    unpacked = np.stack([np.where(lo > 7, lo - 16, lo), np.where(hi > 7, hi - 16, hi)],
+                        axis=2).reshape(N, K)
+    assert np.array_equal(unpacked, d["w_values"].numpy())
