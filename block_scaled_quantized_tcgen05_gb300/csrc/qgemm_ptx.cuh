@@ -34,6 +34,18 @@ __device__ __forceinline__ uint32_t lane_id() {
     return l;
 }
 
+// ------------------------------------------------------------- programmatic dependent launch
+// The grid launched next on the stream with programmatic stream serialization may start once
+// every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory operations are
+// visible (returns at once when the grid was launched without that dependency).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -144,6 +144,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                   uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    griddep_launch_dependents();   // the outlier-row pass may take the room this CTA leaves
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -431,6 +432,7 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                  int c_vec, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    griddep_launch_dependents();   // the outlier-row pass may take the room this CTA leaves
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;

@@ -16,17 +16,25 @@
 // with the block partials scaled and summed in fp64 (every 2^(e-127) and every fp32 partial
 // times it is a double, so nothing over- or underflows before the single fp16 rounding).
 //
-// Grid: x over 256-row groups of W (one thread tests one row), y over 512-token groups of A.
-// Each CTA lists its group's outlier rows in shared memory and, for each, has its eight warps
-// take the tokens of its token group in turn: lane l reads the 16-byte chunks l, l + 32, ... of
-// the token's activation row (8 k each, four chunks per block), the four lanes of a block add
-// their partials in a fixed order, and the fp64 block terms are added by a fixed shuffle tree,
-// so the result does not depend on timing.  With no outlier row (the usual case) a CTA only
-// reads its rows' scale bytes.
+// Grid: x over 256-row groups of W (one thread tests one row), y over token groups of A (as
+// many as fit beside x in one CTA per SM).  Each CTA marks its group's outlier rows in a 256-bit
+// mask in shared memory and, for each in row order, has its eight warps take the tokens of its
+// token group in turn: lane l
+// reads the 16-byte chunks l, l + 32, ... of the token's activation row (8 k each, four chunks
+// per block), the four lanes of a block add their partials in a fixed order, and the fp64 block
+// terms are added by a fixed shuffle tree, so the result does not depend on timing.
+//
+// The kernel is launched with programmatic stream serialization and the GEMM kernels release it
+// at their start (griddepcontrol.launch_dependents), so its CTAs take the SM room the GEMM leaves
+// (about 10 K registers and 1.8 KB of shared memory per SM) and read the scale plane while the GEMM
+// runs.  Every thread then waits for the GEMM to complete (griddepcontrol.wait) before touching
+// C -- and before exiting, so that this grid's completion, which later work on the stream waits
+// for, implies the GEMM's.  With no outlier row (the usual case) that wait is all that is left.
 #include <cuda_fp16.h>
 
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
+#include "qgemm_ptx.cuh"
 #include "w4a16_convert.cuh"
 
 namespace {
@@ -34,7 +42,7 @@ namespace {
 using namespace qg;
 
 constexpr int OT_ROWS = 256;     // weight rows tested per CTA (one per thread)
-constexpr int OT_TOKENS = 512;   // tokens per CTA
+constexpr int OT_MIN_TOKENS = 64;   // smallest token group worth a CTA of its own
 constexpr int OT_THREADS = 256;
 constexpr int OT_WARPS = OT_THREADS / 32;
 
@@ -55,32 +63,35 @@ __device__ __forceinline__ float nibble_f(uint32_t w, int j) {
     return static_cast<float>(static_cast<int>(w << (28 - 4 * j)) >> 28);
 }
 
-__global__ void __launch_bounds__(OT_THREADS)
+__global__ void __launch_bounds__(OT_THREADS, 6)   // <= 40 registers: fits beside the GEMMs
 w4a16_outlier_kernel(const __half *__restrict__ A, int64_t lda, int M,
                      const uint8_t *__restrict__ W, int64_t ldw, const uint8_t *__restrict__ S,
-                     int64_t lds, int N, int K, __half *__restrict__ C, int64_t ldc, int epi) {
-    __shared__ int rows[OT_ROWS];
-    __shared__ int count;
+                     int64_t lds, int N, int K, __half *__restrict__ C, int64_t ldc, int epi,
+                     int tokens_per_cta) {
+    __shared__ uint32_t mask[OT_ROWS / 32];   // bit t of word w: row 32 w + t of the group
     const int t = static_cast<int>(threadIdx.x);
-    if (t == 0) count = 0;
-    __syncthreads();
-    const int n = static_cast<int>(blockIdx.x) * OT_ROWS + t;
-    if (n < N && w4_row_is_outlier(S + static_cast<int64_t>(n) * lds,
-                                   W + static_cast<int64_t>(n) * ldw, K / 32))
-        rows[atomicAdd(&count, 1)] = n;
-    __syncthreads();
-    const int cnt = count;
-    if (cnt == 0) return;
-
     const int warp = t >> 5, lane = t & 31;
+    const int n = static_cast<int>(blockIdx.x) * OT_ROWS + t;
+    const bool mine = n < N && w4_row_is_outlier(S + static_cast<int64_t>(n) * lds,
+                                                 W + static_cast<int64_t>(n) * ldw, K / 32);
+    const uint32_t bits = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0) mask[warp] = bits;
+    __syncthreads();
+    uint32_t any = 0;
+#pragma unroll
+    for (int w = 0; w < OT_ROWS / 32; ++w) any |= mask[w];
+    griddep_wait();   // the GEMM has written C (see the file comment)
+    if (any == 0) return;
+
     const int nchunk = K / 8;   // 16-byte activation chunks per token row (a multiple of 4)
-    for (int i = 0; i < cnt; ++i) {
-        const int nn = rows[i];
+    for (int r = 0; r < OT_ROWS; ++r) {
+        if (!((mask[r >> 5] >> (r & 31)) & 1u)) continue;
+        const int nn = static_cast<int>(blockIdx.x) * OT_ROWS + r;
         const uint8_t *wrow = W + static_cast<int64_t>(nn) * ldw;
         const uint8_t *srow = S + static_cast<int64_t>(nn) * lds;
-        for (int64_t m0 = static_cast<int64_t>(blockIdx.y) * OT_TOKENS; m0 < M;
-             m0 += static_cast<int64_t>(gridDim.y) * OT_TOKENS) {
-            const int m_end = static_cast<int>(m0 + OT_TOKENS < M ? m0 + OT_TOKENS : M);
+        for (int64_t m0 = static_cast<int64_t>(blockIdx.y) * tokens_per_cta; m0 < M;
+             m0 += static_cast<int64_t>(gridDim.y) * tokens_per_cta) {
+            const int m_end = static_cast<int>(m0 + tokens_per_cta < M ? m0 + tokens_per_cta : M);
             for (int m = static_cast<int>(m0) + warp; m < m_end; m += OT_WARPS) {
                 const __half *arow = A + static_cast<int64_t>(m) * lda;
                 double acc = 0.0;
@@ -129,11 +140,25 @@ cudaError_t launch_w4a16_outliers(const __half *A, int64_t lda, int M, const qge
                                   __half *C, int64_t ldc, const LaunchCtx &ctx) {
     const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
     const int gx = (N + OT_ROWS - 1) / OT_ROWS;
-    int gy = (M + OT_TOKENS - 1) / OT_TOKENS;
+    // token groups: as many as fit one CTA per SM beside the row groups, at least 64 tokens each
+    int gy = ctx.num_sms / gx;
+    const int max_gy = (M + OT_MIN_TOKENS - 1) / OT_MIN_TOKENS;
+    if (gy > max_gy) gy = max_gy;
     if (gy > 65535) gy = 65535;
-    w4a16_outlier_kernel<<<dim3(gx, gy), OT_THREADS, 0, ctx.stream>>>(
-        A, lda, M, W->data, W->ld, W->scales, W->lds, N, K, C, ldc, ctx.epi);
-    return cudaGetLastError();
+    if (gy < 1) gy = 1;
+    const int tokens = static_cast<int>((static_cast<int64_t>(M) + gy - 1) / gy);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, gy);
+    cfg.blockDim = dim3(OT_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, w4a16_outlier_kernel, A, lda, M, W->data, W->ld, W->scales,
+                              W->lds, N, K, C, ldc, ctx.epi, tokens);
 }
 
 }  // namespace qgi

@@ -101,6 +101,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                   int64_t ldc, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    griddep_launch_dependents();   // the outlier-row pass may take the room this CTA leaves
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
