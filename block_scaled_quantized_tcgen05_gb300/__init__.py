@@ -18,7 +18,7 @@ __all__ = [
     "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
     "qgemm_mxfp8", "qgemm_mxfp8_host", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
-    "qgemm_selftest_wait_timeout",
+    "qgemm_selftest_wait_timeout", "qgemm_sm_clock_probe",
 ]
 
 F16, E4M3, INT8, INT4, E2M1 = 0, 1, 2, 3, 4
@@ -88,6 +88,7 @@ def load_library():
         "qgemm_poll_device_error": (S, [P, ctypes.POINTER(ctypes.c_uint32)]),
         "qgemm_set_wait_timeout_ns": (None, [U64]),
         "qgemm_selftest_wait_timeout": (S, [U64, P]),
+        "qgemm_sm_clock_probe": (S, [U64, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -341,3 +342,10 @@ def qgemm_set_wait_timeout_ns(ns: int):
 def qgemm_selftest_wait_timeout(timeout_ns: int, stream=None):
     _check(load_library().qgemm_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
            "qgemm_selftest_wait_timeout")
+
+
+def qgemm_sm_clock_probe(window_ns: int, out, stream=None):
+    """Write (SM cycles, global-timer ns) over `window_ns` into the two int64 elements of the
+    device tensor `out` (from the GPU, on `stream`)."""
+    _check(load_library().qgemm_sm_clock_probe(int(window_ns), _ptr(out), _stream(stream)),
+           "qgemm_sm_clock_probe")

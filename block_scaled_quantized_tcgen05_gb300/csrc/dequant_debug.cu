@@ -99,6 +99,30 @@ __global__ void selftest_wait_kernel(unsigned *err, uint64_t timeout_ns) {
     __syncthreads();
 }
 
+// One thread reads the SM cycle counter and the global nanosecond timer, naps in 0.5 us steps
+// until window_ns of global time have passed (the timer always advances, so the loop ends), reads
+// both again and stores out[0] = cycles, out[1] = nanoseconds.  The ratio is the SM clock over
+// the window, whatever else the GPU runs meanwhile.  Launched as a programmatic dependent of the
+// kernel before it on the stream, it runs beside that kernel when the kernel releases its
+// dependents early (the library's GEMMs do) and then waits for it to complete, so that the
+// probe's completion implies that kernel's.
+__global__ void clock_probe_kernel(uint64_t window_ns, unsigned long long *out) {
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        const long long c0 = clock64();
+        uint64_t t = t0;
+        while (t - t0 < window_ns) {
+            __nanosleep(500);
+            t = globaltimer_ns();
+        }
+        const long long c1 = clock64();
+        const uint64_t t1 = globaltimer_ns();
+        out[0] = static_cast<unsigned long long>(c1 - c0);
+        out[1] = static_cast<unsigned long long>(t1 - t0);
+    }
+    griddep_wait();
+}
+
 int grid_for(int64_t total, int num_sms) {
     int64_t g = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
@@ -131,6 +155,24 @@ cudaError_t launch_empty_sum_epilogue(__half *C, int64_t ldc, int64_t M, int64_t
     if (!(ctx.epi & EPI_RELU) || M * N == 0) return cudaSuccess;                        // C unchanged
     relu_inplace_f16_kernel<<<grid_for(M * N, ctx.num_sms), 256, 0, ctx.stream>>>(C, ldc, M, N);
     return cudaGetLastError();
+}
+
+cudaError_t launch_clock_probe(uint64_t window_ns, uint64_t *out, const LaunchCtx &ctx) {
+    // A programmatic dependent: it starts only once every CTA of the kernel before it is running
+    // (a probe launched on its own stream could take an SM first and hold back a CTA of a
+    // persistent GEMM with a fixed tile order, which then waits for it).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, clock_probe_kernel, window_ns,
+                              reinterpret_cast<unsigned long long *>(out));
 }
 
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, const LaunchCtx &ctx) {

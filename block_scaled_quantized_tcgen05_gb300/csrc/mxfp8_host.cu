@@ -10,7 +10,8 @@
 // call's downloads still occupy the other direction of the link.
 //
 // Device memory: the two buffer sets grow to the largest shape seen and stay allocated (per
-// device) until the process exits.
+// device) until the process exits; the repacked scale planes (B's once per call, then one row
+// chunk of A's at a time) come from the library's stream-ordered pool, as for qgemm_mxfp8.
 #include <cstdio>
 #include <mutex>
 
@@ -142,8 +143,23 @@ extern "C" qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tens
         if ((e = cudaEventRecord(h.ev_a[nch], h.up)) != cudaSuccess) return cuda_err(e, "event record");
     }
 
-    // the product of each row chunk on the caller's stream, then its download
+    // the product of each row chunk on the caller's stream, then its download.  On the CTA-pair
+    // route B's scale plane is repacked once, right after B lands, and each chunk repacks only
+    // its rows of A (into one buffer reused chunk after chunk: the stream orders them).
     if ((e = cudaStreamWaitEvent(s, h.ev_b, 0)) != cudaSuccess) return cuda_err(e, "ordering");
+    const qgemm_tensor bc{QGEMM_E4M3, N, K, dB, K, dSB, kb};
+    const qgemm_tensor a_first{QGEMM_E4M3, M < step ? M : step, K, dA, K, dSA, kb};
+    const bool pair_b = K > 0 && N > 128;
+    void *pack = nullptr;
+    size_t pack_b_bytes = 0;
+    if (pair_b) {
+        pack_b_bytes = (qgi::mxfp8_pack_bytes(&bc) + 255) & ~size_t(255);
+        if ((e = qgi::scratch_alloc(pack_b_bytes + qgi::mxfp8_pack_bytes(&a_first), ctx, &pack)) !=
+            cudaSuccess)
+            return cuda_err(e, "scale scratch");
+        if ((e = qgi::launch_mxfp8_sf_pack(&bc, pack, ctx)) != cudaSuccess)
+            return cuda_err(e, "scale repack of B");
+    }
     nch = 0;
     for (int64_t r0 = 0; r0 < M; r0 += step, ++nch) {
         const int64_t rows = M - r0 < step ? M - r0 : step;
@@ -152,9 +168,16 @@ extern "C" qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tens
             e = qgi::launch_fill_zero_f16(dC + r0 * ldcd, ldcd, rows, N, ctx);
         } else {
             const qgemm_tensor ac{QGEMM_E4M3, rows, K, dA + r0 * K, K, dSA + r0 * kb, kb};
-            const qgemm_tensor bc{QGEMM_E4M3, N, K, dB, K, dSB, kb};
             bool enc = true;
-            e = qgi::launch_mxfp8(&ac, &bc, dC + r0 * ldcd, ldcd, ctx, &enc);
+            if (pair_b && qgi::mxfp8_pair_eligible(&ac, &bc)) {
+                uint8_t *pack_a = static_cast<uint8_t *>(pack) + pack_b_bytes;
+                e = qgi::launch_mxfp8_sf_pack(&ac, pack_a, ctx);
+                if (e == cudaSuccess)
+                    e = qgi::launch_mxfp8_pair_packed(&ac, &bc, dC + r0 * ldcd, ldcd, pack_a, pack,
+                                                      ctx, &enc);
+            } else {
+                e = qgi::launch_mxfp8(&ac, &bc, dC + r0 * ldcd, ldcd, ctx, &enc);
+            }
             if (!enc) return QGEMM_ERR_CUDA;
         }
         if (e != cudaSuccess) return cuda_err(e, "GEMM launch");
@@ -168,6 +191,8 @@ extern "C" qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tens
                                    h.down)) != cudaSuccess)
             return cuda_err(e, "download of C");
     }
+    if (pack && (e = qgi::scratch_free(pack, ctx)) != cudaSuccess)
+        return cuda_err(e, "scale scratch");
     // the set is free once its downloads are done; the caller's stream completes with them
     if ((e = cudaEventRecord(bs.free_ev, h.down)) != cudaSuccess ||
         (e = cudaEventRecord(h.ev_out, h.down)) != cudaSuccess ||

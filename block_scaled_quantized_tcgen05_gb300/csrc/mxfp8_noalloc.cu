@@ -9,7 +9,8 @@
 // makes no cudaMalloc, no pool allocation and no allocating library call.
 //
 // The array's price and its rules:
-//  * every GPU on which the library is loaded holds NOALLOC_SCRATCH_BYTES for it until exit;
+//  * every GPU on which the array has been placed (see below) holds NOALLOC_SCRATCH_BYTES for it
+//    until exit;
 //  * a shape whose repacked scales need more than that is rejected (QGEMM_ERR_UNSUPPORTED_SHAPE),
 //    nothing is launched;
 //  * all calls on one device share the array: calls that overlap on the GPU (different streams
@@ -19,7 +20,13 @@
 //    the repack kernel rewrites every byte the GEMM then reads;
 //  * host code cannot use the array's name as a device address (it names a host-side stand-in), so
 //    the first call on each device looks the address up with cudaGetSymbolAddress, with that
-//    device current, and caches it; that first call should come before any stream capture.
+//    device current, and caches it; that first call should come before any stream capture;
+//  * the array lives in this file's own module, which CUDA loads lazily by default: the driver
+//    places the 8 MiB in device memory at that first lookup, not when the library is loaded, so a
+//    caller that reserves the rest of device memory for itself makes one call on each device
+//    before it does (with CUDA_MODULE_LOADING=EAGER the array is placed when the context is made);
+//  * the cached address belongs to the device's current context: after cudaDeviceReset (or any
+//    teardown of the primary context) the library must not be used again in this process.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -45,11 +45,7 @@
 // scale warps loading the repacked scales from global memory instead of shared memory (+2%);
 // direct 16-byte row stores from the epilogue instead of the staged, sector-wide ones (+4%);
 // the scale blocks as 2-D tensor boxes 16 bytes wide (+0.6%); raster groups of 8 or 32 pair rows
-// instead of 16 (+1%, +5%); L2 prefetch of A and B eight k-tiles ahead (+10%); clusters of four
-// (two pairs sharing the N tile, each B half loaded once and multicast to both pairs: +8%; only
-// 36 such clusters fit on the GPU's 152 SMs, and multicast halves L2 reads but not the shared
-// memory each SM writes and its tensor core reads, which is what bounds this kernel -- loading
-// half of B, with wrong results, is 9% faster, half of A 6%).
+// instead of 16 (+1%, +5%); L2 prefetch of A and B eight k-tiles ahead (+10%).
 #include "qgemm_common.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
@@ -209,6 +205,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     constexpr uint32_t SF_COLS_PER_STAGE = F::SF_COLS_PER_STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    griddep_launch_dependents();   // a dependent launch (e.g. a clock probe) may run beside
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -432,15 +429,32 @@ size_t pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
 }
 
 template <class F>
-cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
-                        void *scratch, const qgi::LaunchCtx &ctx, bool *encode_ok) {
-    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
-              K = static_cast<int>(A->k);
+SfPackOperand pack_operand(const qgemm_tensor *t, uint8_t *out) {
+    const int vec = (reinterpret_cast<uintptr_t>(t->scales) % 16 == 0 && t->lds % 16 == 0) ? 1 : 0;
+    return SfPackOperand{t->scales, t->lds, static_cast<int>(t->rows), static_cast<int>(t->k / 32),
+                         padded_blocks(t->rows), out, vec};
+}
+
+// Repack one or two operands' scale planes (nops = 1: opA only).
+template <class F>
+cudaError_t launch_sf_pack(const SfPackOperand &pa, const SfPackOperand &pb, int nops, int KT,
+                           cudaStream_t stream) {
+    const int rbp = nops == 2 && pb.rbp > pa.rbp ? pb.rbp : pa.rbp;
+    const dim3 pgrid(static_cast<unsigned>(rbp),
+                     static_cast<unsigned>((KT * F::W + PACK_KT - 1) / PACK_KT),
+                     static_cast<unsigned>(nops));
+    sf_pack_kernel<F::W><<<pgrid, 256, 0, stream>>>(pa, nops == 2 ? pb : pa, KT);
+    return cudaGetLastError();
+}
+
+// The CTA-pair GEMM on scale planes already repacked into packA / packB.
+template <class F>
+cudaError_t launch_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                               int64_t ldc, const uint8_t *packA, const uint8_t *packB,
+                               const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows);
     const int Kb = static_cast<int>(k_bytes<F>(A));
-    const int KT = (Kb + BK - 1) / BK;
     const int rbpA = padded_blocks(M), rbpB = padded_blocks(N);
-    uint8_t *packA = static_cast<uint8_t *>(scratch);
-    uint8_t *packB = packA + static_cast<size_t>(KT) * rbpA * 512 * F::W;
     CUtensorMap tmA, tmB;
     *encode_ok =
         qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, Kb, M, A->ld, BK, BM,
@@ -448,20 +462,9 @@ cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
         qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, Kb, N, B->ld, BK, BN / 2,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
-
-    auto vec16 = [](const qgemm_tensor *t) {
-        return (reinterpret_cast<uintptr_t>(t->scales) % 16 == 0 && t->lds % 16 == 0) ? 1 : 0;
-    };
-    const SfPackOperand pa{A->scales, A->lds, M, K / 32, rbpA, packA, vec16(A)};
-    const SfPackOperand pb{B->scales, B->lds, N, K / 32, rbpB, packB, vec16(B)};
-    const dim3 pgrid(static_cast<unsigned>(rbpA > rbpB ? rbpA : rbpB),
-                     static_cast<unsigned>((KT * F::W + PACK_KT - 1) / PACK_KT), 2);
-    sf_pack_kernel<F::W><<<pgrid, 256, 0, ctx.stream>>>(pa, pb, KT);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    e = cudaFuncSetAttribute(mx_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<F>::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(mx_pair_kernel<F>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Smem<F>::BYTES);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
     int pairs = ctx.num_sms / 2;
@@ -471,6 +474,19 @@ cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
         tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err,
         ctx.timeout_ns);
     return cudaGetLastError();
+}
+
+template <class F>
+cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
+                        void *scratch, const qgi::LaunchCtx &ctx, bool *encode_ok) {
+    const int KT = static_cast<int>((k_bytes<F>(A) + BK - 1) / BK);
+    uint8_t *packA = static_cast<uint8_t *>(scratch);
+    uint8_t *packB = packA + static_cast<size_t>(KT) * padded_blocks(A->rows) * 512 * F::W;
+    *encode_ok = true;
+    cudaError_t e = launch_sf_pack<F>(pack_operand<F>(A, packA), pack_operand<F>(B, packB), 2,
+                                      KT, ctx.stream);
+    if (e != cudaSuccess) return e;
+    return launch_pair_packed<F>(A, B, C, ldc, packA, packB, ctx, encode_ok);
 }
 
 }  // namespace
@@ -488,6 +504,24 @@ size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {
 cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
                               int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok) {
     return launch_pair<FmtE4M3>(A, B, C, ldc, scratch, ctx, encode_ok);
+}
+
+size_t mxfp8_pack_bytes(const qgemm_tensor *T) {
+    const int64_t KT = (k_bytes<FmtE4M3>(T) + BK - 1) / BK;
+    return static_cast<size_t>(KT) * padded_blocks(T->rows) * 512 * FmtE4M3::W;
+}
+
+cudaError_t launch_mxfp8_sf_pack(const qgemm_tensor *T, void *out, const LaunchCtx &ctx) {
+    const int KT = static_cast<int>((k_bytes<FmtE4M3>(T) + BK - 1) / BK);
+    const SfPackOperand op = pack_operand<FmtE4M3>(T, static_cast<uint8_t *>(out));
+    return launch_sf_pack<FmtE4M3>(op, op, 1, KT, ctx.stream);
+}
+
+cudaError_t launch_mxfp8_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                                     int64_t ldc, const void *packA, const void *packB,
+                                     const LaunchCtx &ctx, bool *encode_ok) {
+    return launch_pair_packed<FmtE4M3>(A, B, C, ldc, static_cast<const uint8_t *>(packA),
+                                       static_cast<const uint8_t *>(packB), ctx, encode_ok);
 }
 
 size_t mxfp4_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B) {

@@ -698,6 +698,19 @@ qgemm_status qgemm_poll_device_error(void *stream, uint32_t *code_out) {
     return QGEMM_OK;
 }
 
+qgemm_status qgemm_sm_clock_probe(uint64_t window_ns, uint64_t *out_dev, void *stream) {
+    if (!out_dev) return fail(QGEMM_ERR_INVALID_ARG, "out is NULL");
+    if (window_ns == 0 || window_ns > 1000000000ull)
+        return fail(QGEMM_ERR_INVALID_ARG, "window must be in 1 .. 1e9 ns (got %llu)",
+                    (unsigned long long)window_ns);
+    if (!aligned(out_dev, 8)) return fail(QGEMM_ERR_MISALIGNED, "out must be 8-byte aligned");
+    qgi::LaunchCtx ctx;
+    qgemm_status st = get_ctx(stream, &ctx);
+    if (st != QGEMM_OK) return st;
+    cudaError_t e = qgi::launch_clock_probe(window_ns, out_dev, ctx);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "clock probe launch");
+}
+
 qgemm_status qgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
     qgi::LaunchCtx ctx;
     qgemm_status st = get_ctx(stream, &ctx);

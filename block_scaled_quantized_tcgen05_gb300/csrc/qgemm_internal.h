@@ -58,6 +58,15 @@ size_t mxfp8_pair_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B);
 cudaError_t launch_mxfp8_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
                               int64_t ldc, void *scratch, const LaunchCtx &ctx, bool *encode_ok);
 
+// The two halves of launch_mxfp8_pair, for callers that repack an operand once and reuse it:
+// the repack of one view's scale plane into `out` (mxfp8_pack_bytes(T) bytes, 256-byte aligned),
+// and the CTA-pair GEMM on planes repacked that way.
+size_t mxfp8_pack_bytes(const qgemm_tensor *T);
+cudaError_t launch_mxfp8_sf_pack(const qgemm_tensor *T, void *out, const LaunchCtx &ctx);
+cudaError_t launch_mxfp8_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
+                                     int64_t ldc, const void *packA, const void *packB,
+                                     const LaunchCtx &ctx, bool *encode_ok);
+
 // MXFP4 (E2M1) GEMM on CTA pairs, same pipeline and scratch contract as launch_mxfp8_pair.
 size_t mxfp4_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B);
 cudaError_t launch_mxfp4_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
@@ -108,5 +117,6 @@ cudaError_t launch_fill_zero_f16(__half *C, int64_t ldc, int64_t M, int64_t N,
 cudaError_t launch_empty_sum_epilogue(__half *C, int64_t ldc, int64_t M, int64_t N,
                                       const LaunchCtx &ctx);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, const LaunchCtx &ctx);
+cudaError_t launch_clock_probe(uint64_t window_ns, uint64_t *out, const LaunchCtx &ctx);
 
 }  // namespace qgi

@@ -29,6 +29,9 @@
  *     returns QGEMM_ERR_CUDA.
  *   - Every device-side wait is bounded.  A kernel that gives up records a code in a device
  *     error word that qgemm_poll_device_error() reads; its outputs are then unspecified.
+ *   - The library caches per-device addresses (the error word, the fixed array of
+ *     qgemm_mxfp8_noalloc) in the device's primary context: after cudaDeviceReset, or any other
+ *     teardown of that context, the library must not be called again in the same process.
  */
 #ifndef QGEMM_H
 #define QGEMM_H
@@ -136,8 +139,9 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
  * path that cannot risk an allocation that blocks or fails in the middle of a request.
  * Same arguments, layouts, results and errors as qgemm_mxfp8.  Where qgemm_mxfp8 takes pooled
  * scratch for the repacked scale planes (M > 128 and N > 128), this call uses a fixed 8 MiB
- * device array compiled into the library instead (held on every device that loads the library
- * until exit) and makes no cudaMalloc, pool allocation or other allocating call.
+ * device array compiled into the library instead (held, once placed, on each device until exit)
+ * and makes no cudaMalloc, pool allocation or other allocating call.  M or N <= 128 runs the
+ * one-CTA kernel of qgemm_mxfp8, which needs no scratch.
  * Limits and rules:
  *   - a shape whose repacked scales need more than 8 MiB ((2 ceil(M/256) + 2 ceil(N/256)) *
  *     ceil(K/128) * 512 bytes, e.g. more than M = N = 16384 at K = 8192) is rejected with
@@ -146,7 +150,10 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
  *     wrong results -- issue them on one stream or synchronise between them;
  *   - the array keeps the last call's contents; every byte a call reads is first rewritten by it;
  *   - the first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current) and caches it; make that first call before any stream capture. */
+ *     with that device current) and caches it; make that first call before any stream capture;
+ *   - under CUDA's lazy module loading (the default) that first lookup is also when the driver
+ *     places the 8 MiB in the device's memory: a caller that reserves all remaining device memory
+ *     for itself makes one call on each device before it does so. */
 qgemm_status qgemm_mxfp8_noalloc(const qgemm_tensor *A, const qgemm_tensor *B, void *C,
                                  int64_t ldc, void *stream);
 
@@ -349,6 +356,20 @@ void qgemm_set_wait_timeout_ns(uint64_t ns);
  * error word and the kernel returns normally.  No output; use qgemm_poll_device_error().
  * Errors: CUDA. */
 qgemm_status qgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Measurement aid: the SM clock over a window of wall time, read on the GPU.  Launches one
+ * 32-thread block that reads the SM cycle counter (clock64) and the global nanosecond timer, naps
+ * until window_ns have passed on that timer, reads both again and writes out_dev[0] = cycles and
+ * out_dev[1] = nanoseconds elapsed (device memory, two uint64); cycles / nanoseconds is the clock
+ * in GHz.  The block is launched as a programmatic dependent of the kernel before it on `stream`:
+ * issued right after a qgemm_mxfp8 / qgemm_mxfp4 call on the same stream, it starts once every CTA
+ * of that GEMM runs, takes almost no room beside them, reports the clock the GEMM runs at (under a
+ * power cap the SM clock drops below its maximum) and completes only after the GEMM has; give it
+ * a window shorter than the GEMM.  After other work it simply runs next.
+ * The pages have no counterpart: benchmarks of compute-bound kernels need the clock they ran at.
+ * Errors: INVALID_ARG (out NULL, window 0 or above 1e9 ns), MISALIGNED (out not 8-byte
+ * aligned); CUDA. */
+qgemm_status qgemm_sm_clock_probe(uint64_t window_ns, uint64_t *out_dev, void *stream);
 
 #ifdef __cplusplus
 }

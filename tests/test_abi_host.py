@@ -220,3 +220,11 @@ def test_mxfp8_host_rejects_before_any_cuda_call(lib):
     assert lib.qgemm_mxfp8_host(e0, b, C, 256, None) == 0      # empty output: nothing to do
     for t in (a, b2, b, w8, e0):
         lib.qgemm_destroy_tensor(t)
+
+
+def test_clock_probe_argument_checks(lib):
+    # rejected before anything reaches a device
+    assert lib.qgemm_sm_clock_probe(100000, None, None) == 1                     # null out
+    assert lib.qgemm_sm_clock_probe(0, ctypes.c_void_p(FAKE), None) == 1         # empty window
+    assert lib.qgemm_sm_clock_probe(2 * 10 ** 9, ctypes.c_void_p(FAKE), None) == 1   # > 1 s
+    assert lib.qgemm_sm_clock_probe(100000, ctypes.c_void_p(FAKE + 4), None) == 3    # alignment

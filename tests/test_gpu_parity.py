@@ -420,3 +420,14 @@ def test_bounded_wait_gives_up_and_context_survives(dev, orc):
     q.qgemm_mxfp8(A, B, C)
     res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
     _check(C, res, orc, what="after self-test")
+
+
+def test_sm_clock_probe_reads_a_plausible_clock(dev):
+    """The clock probe's cycles over its window give an SM clock between 0.3 and 2.6 GHz (the
+    GPU's maximum is 2.07 GHz), and the window it measured is at least the one asked for."""
+    out = torch.zeros(2, dtype=torch.int64, device=dev)
+    q.qgemm_sm_clock_probe(200_000, out)
+    torch.cuda.synchronize()
+    cycles, ns = (int(v) for v in out.cpu())
+    assert ns >= 200_000
+    assert 0.3 < cycles / ns < 2.6, (cycles, ns)
