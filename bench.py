@@ -4,7 +4,8 @@ One step = one pass of every row of the hot path over its workload, inputs resid
   1. MXFP8 GEMM        M = N = K = 8192   (E4M3 + UE8M0 per 32 along K, per-row variance)
   2. fp16 GEMM         M = N = K = 4096
   3. W4A16 GEMM        M = 4096, N = 14336, K = 4096 (int4 weights, UE8M0 per 32)
-  4. W8 decode GEMV    M = 1, 8, 16; N = 28672, K = 8192 (weights rotate over two copies)
+  4. W8 decode GEMV    M = 1, 8, 16; N = 28672, K = 8192, each M as a run of four consecutive
+                       launches (a decode step's GEMVs; weights rotate over three copies)
 Each kernel is timed with CUDA events on the stream it is launched on.  The headline ``value``
 is the MXFP8 8192^3 GEMM in TFLOP/s; the GEMV in GB/s and the other rows are reported beside it.
 
@@ -213,7 +214,8 @@ def run_ours(args, ws, rank, local):
     if want("gemv"):
         gv = synth.workload("w8_decode", M=16)
         W8s = []
-        for copy in range(2):        # two weight copies (484 MB): no GEMV reads L2-resident weights
+        # three weight copies (727 MB): with two, ncu saw 27 MB of a 242 MB stream still hit in L2
+        for copy in range(3):
             w8 = gv["w"].to(dev) if copy == 0 else gv["w"].to(dev).clone()
             s8 = gv["sw"].to(dev) if copy == 0 else gv["sw"].to(dev).clone()
             W8s.append(q.qgemm_create_tensor(q.INT8, w8, s8))
@@ -239,7 +241,13 @@ def run_ours(args, ws, rank, local):
     # stream starts once the GEMM's CTAs all run (a programmatic dependent), reads cycles and
     # global time over 200 us of the GEMM's ~330 us and completes with the GEMM
     probe_buf = torch.zeros(max(1, args.steps), 2, dtype=torch.int64, device=dev)
+    probe_gemv = torch.zeros(max(1, args.steps), 2, dtype=torch.int64, device=dev)
     PROBE_NS = 200_000
+    PROBE_GEMV_NS = 20_000        # inside the last M = 1 decode GEMV of a run (about 39 us)
+    probe_on = [False, 0]
+    # GEMVs are timed as runs of consecutive launches, as a decode step issues them; a CUDA event
+    # between two kernels costs each one the whole kernel boundary (about 4 us here)
+    GEMV_RUN = 4
 
     def launch(k, i):
         if k == "mxfp8":
@@ -259,14 +267,19 @@ def run_ours(args, ws, rank, local):
         elif k == "w4a16":
             q.qgemm_w4a16(w4a, W4, w4c)
         else:
-            # consecutive GEMVs read different weight copies (484 MB in all, > L2)
+            # a decode run: GEMV_RUN launches back to back (each a programmatic dependent of the
+            # one before), consecutive launches reading different weight copies (727 MB in all)
             m = int(k[6:])
-            q.qgemm_w8_gemv(X16[:m], W8s[gemv_count[0] % 2], Ys[m])
-            gemv_count[0] += 1
+            for _ in range(GEMV_RUN):
+                q.qgemm_w8_gemv(X16[:m], W8s[gemv_count[0] % 3], Ys[m])
+                if m == 1 and _ == GEMV_RUN - 1 and probe_on[0]:
+                    q.qgemm_sm_clock_probe(PROBE_GEMV_NS, probe_gemv[probe_on[1]])
+                gemv_count[0] += 1
 
     def step(i, ev=None):
         if ev is not None:
             ev[0].record(stream)
+        probe_on[0], probe_on[1] = ev is not None, i
         for j, k in enumerate(kernels):
             launch(k, i)
             if ev is not None and k == "mxfp8":
@@ -312,16 +325,23 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError("a kernel wait timed out during the timed region")
 
     total_ms = t0.elapsed_time(t1)
-    if "mxfp8" in kernels and clocks is not None:
-        pr = probe_buf.cpu().tolist()
-        mhz = [1e3 * c / n for c, n in pr[:args.steps] if n > 0]
+    if clocks is not None:
         clocks["smi_sm_mhz"] = clocks["sm_mhz"]
-        if mhz:
-            clocks["sm_mhz"] = round(statistics.median(mhz), 1)
-            clocks["sm_mhz_source"] = ("median over the timed steps of a clock64 / globaltimer "
-                                       "probe run beside the MXFP8 GEMM (200 us of each launch)")
-            clocks["probe_mhz_min_max"] = [round(min(mhz), 1), round(max(mhz), 1)]
-    per = {k: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+        if "mxfp8" in kernels:
+            pr = probe_buf.cpu().tolist()
+            mhz = [1e3 * c / n for c, n in pr[:args.steps] if n > 0]
+            if mhz:
+                clocks["sm_mhz"] = round(statistics.median(mhz), 1)
+                clocks["sm_mhz_source"] = ("median over the timed steps of a clock64 / globaltimer "
+                                           "probe run beside the MXFP8 GEMM (200 us of each launch)")
+                clocks["probe_mhz_min_max"] = [round(min(mhz), 1), round(max(mhz), 1)]
+        if "gemv_m1" in kernels:
+            pr = probe_gemv.cpu().tolist()
+            mhz = [1e3 * c / n for c, n in pr[:args.steps] if n > 0]
+            if mhz:
+                clocks["sm_mhz_during_gemv_m1"] = round(statistics.median(mhz), 1)
+    per = {k: [evs[i][j].elapsed_time(evs[i][j + 1]) / (GEMV_RUN if k.startswith("gemv") else 1)
+               for i in range(args.steps)]
            for j, k in enumerate(kernels)}
     mean = {k: sum(v) / len(v) for k, v in per.items()}
     median = {k: statistics.median(v) for k, v in per.items()}
@@ -359,7 +379,8 @@ def run_ours(args, ws, rank, local):
             secondary[k] = {"us": round(mean[k] * 1e3, 2), "us_median": round(median[k] * 1e3, 2),
                             "gbs": round(gbs, 1),
                             "frac_of_measured_hbm": round(gbs / hbm, 4),
-                            "frac_of_spec_hbm_8000": round(gbs / SPEC_HBM_GBS, 4)}
+                            "frac_of_spec_hbm_8000": round(gbs / SPEC_HBM_GBS, 4),
+                            "timing": f"per launch, over runs of {GEMV_RUN} consecutive launches"}
     for k in ("mxfp8_relu", "mxfp8_accrelu"):
         if k in mean:
             tf = flops["mxfp8"] / (mean[k] * 1e-3) / 1e12
@@ -389,9 +410,9 @@ def run_ours(args, ws, rank, local):
              if mx_tflops is not None else None)
     # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM), one
     # qgemm_w4a16 call two (the GEMM + the outlier-row pass)
-    launches = sum(2 if k.startswith("mxfp") or k == "w4a16" else 1 for k in kernels) * args.steps
-    if "mxfp8" in kernels:
-        launches += args.steps                   # the clock probe beside each timed MXFP8 GEMM
+    launches = sum(2 if k.startswith("mxfp") or k == "w4a16" else GEMV_RUN if k.startswith("gemv")
+                   else 1 for k in kernels) * args.steps
+    launches += args.steps * (("mxfp8" in kernels) + ("gemv_m1" in kernels))   # clock probes
     line = {
         "metric": METRIC, "value": round(value, 2) if value is not None else None,
         "unit": "TFLOP/s", "n_gpus": ws,
@@ -402,7 +423,7 @@ def run_ours(args, ws, rank, local):
                    "headline": "mxfp8_8192 M=N=K=8192",
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2: each kernel's inputs are evicted by the rest of "
-                         "the step (>129 MB between reuses); GEMV weights rotate over 2 copies"},
+                         "the step (>129 MB between reuses); GEMV weights rotate over 3 copies"},
         "roofline": None if mx_tflops is None else {
             "kernel": "qgemm_mxfp8 = sf_pack_kernel<1> + mx_pair_kernel<FmtE4M3>", "bound": "tensor",
             "achieved": round(mx_tflops, 1), "peak": round(fp8_peak_burst, 1),
@@ -416,7 +437,8 @@ def run_ours(args, ws, rank, local):
             "traffic_unit": "bytes per call (ncu, dram read + write)",
             "algorithmic_bytes": 2 * 8192 * 8192 + 2 * 8192 * 256 + 2 * 8192 * 8192},
         "roofline_gemv": None if "gemv_m1" not in mean else {
-            "kernel": "qgemm_w8_gemv = w8_gemv_kernel, M = 1 (the decode row of the metric)",
+            "kernel": "qgemm_w8_gemv = w8_gemv_kernel, M = 1 (the decode row of the metric), "
+                      f"average launch of runs of {GEMV_RUN} back-to-back launches",
             "bound": "hbm", "achieved": secondary["gemv_m1"]["gbs"], "peak": hbm, "unit": "GB/s",
             "frac": round(secondary["gemv_m1"]["gbs"] / hbm, 4),
             "peak_source": f"{peak_kind} HBM copy bandwidth",

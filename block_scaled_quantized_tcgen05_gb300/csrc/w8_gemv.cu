@@ -34,22 +34,27 @@ using namespace qg;
 
 constexpr int CONSUMERS = 4;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
-constexpr int ROWS = 64;                    // weight rows per CTA iteration (4 fragments of 16)
 constexpr int KC = 128;                     // K per stage (bytes of int8) = four 32-blocks
 
-template <int NH>
+// NH: 8-column activation halves (1: M <= 8, 2: M <= 16); NF: 16-row weight fragments per CTA
+// (a row block is 16 NF rows).  M <= 8 takes 48-row blocks with six stages: 598 CTAs at
+// N = 28672, four per SM (16 consumer warps to hide the latency of the loads, conversions and
+// MMAs; with 64-row blocks only three fit and 448 row blocks fill 2.95 per SM).
+template <int NH, int NF, int STAGES_>
 struct GCfg {
-    static constexpr int STAGES = NH == 1 ? 6 : 5;            // three CTAs fit on an SM either way
-    static constexpr uint32_t W_BYTES = ROWS * KC;            // 8 KB
+    static constexpr int STAGES = STAGES_;
+    static constexpr int ROWS = 16 * NF;
+    static constexpr uint32_t W_BYTES = ROWS * KC;            // 6 or 8 KB
     static constexpr uint32_t X_HALF = 8 * NH * 128;          // one 64-wide half of the X slice
     static constexpr uint32_t X_BYTES = 2 * X_HALF;
     static constexpr uint32_t STAGE = W_BYTES + X_BYTES;
     static constexpr uint32_t OFF_BAR = STAGES * STAGE;       // full[S], empty[S]
     static constexpr uint32_t OFF_RBAR = OFF_BAR + 2 * STAGES * 8;   // reduction full, empty
     static constexpr uint32_t OFF_RED = OFF_RBAR + 16;
-    // partial sums handed between warps, one activation half at a time: [warp][3 fragments][4][lane]
-    static constexpr uint32_t RED_BYTES = CONSUMERS * 3 * 4 * 32 * 4;
+    // partial sums handed between warps, one activation half at a time: [warp][NF][4][lane]
+    static constexpr uint32_t RED_BYTES = CONSUMERS * NF * 4 * 32 * 4;
     static constexpr uint32_t SMEM = OFF_RED + RED_BYTES + 1024;
+    static_assert(STAGE % 1024 == 0, "stages stay 1 KB aligned for the 128-byte swizzle");
 };
 
 // 4 int8 (one 32-bit word) -> two fp16x2 holding the exact integers (q0,q1), (q2,q3).
@@ -108,16 +113,16 @@ __device__ __forceinline__ bool has_special_byte(uint32_t w) {
 // The products of one stage: this warp's 32-block for all 64 rows, accumulated into acc with the
 // stage's block scales (byte sh / 8 of e0[f], e1[f]).  Plain shared loads and pure MMAs, so two calls
 // in a row can be interleaved by the compiler.
-template <int NH, bool EXACT>
-__device__ __forceinline__ void stage_math(float (&acc)[4][NH][4], const uint8_t *st, uint32_t wrow,
-                                           uint32_t xoff, const uint32_t (&e0)[4],
-                                           const uint32_t (&e1)[4], uint32_t sh) {
-    const uint8_t *xs = st + ROWS * KC;
+template <int NH, int NF, bool EXACT>
+__device__ __forceinline__ void stage_math(float (&acc)[NF][NH][4], const uint8_t *st, uint32_t wrow,
+                                           uint32_t xoff, const uint32_t (&e0)[NF],
+                                           const uint32_t (&e1)[NF], uint32_t sh) {
+    const uint8_t *xs = st + 16 * NF * KC;
     const uint4 xa = *reinterpret_cast<const uint4 *>(xs + xoff);
     uint4 xb = xa;
     if constexpr (NH == 2) xb = *reinterpret_cast<const uint4 *>(xs + xoff + 8 * 128);
 #pragma unroll
-    for (int f = 0; f < 4; ++f) {
+    for (int f = 0; f < NF; ++f) {
         const uint2 wa = *reinterpret_cast<const uint2 *>(st + wrow + f * 16 * 128);
         const uint2 wb = *reinterpret_cast<const uint2 *>(st + wrow + (f * 16 + 8) * 128);
         uint32_t a0[4], a1[4];
@@ -149,11 +154,11 @@ __device__ __forceinline__ void stage_math(float (&acc)[4][NH][4], const uint8_t
 // bytes of rows 16 f + g / 16 f + g + 8 for this warp's block of each stage (stage j in byte j).
 // EXACT selects the decode for the whole group: the shift decode builds 2^(e-127) by moving the
 // byte into the fp32 exponent field; codes 0x00 (subnormal 2^-127) and 0xFF (NaN) need the exact one.
-template <int NH, bool EXACT, int STAGES>
-__device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t *smem, uint32_t sb,
+template <int NH, int NF, bool EXACT, int STAGES>
+__device__ __forceinline__ bool run_group(float (&acc)[NF][NH][4], const uint8_t *smem, uint32_t sb,
                                           uint32_t stage_bytes, uint32_t off_bar, int nst,
-                                          uint32_t wrow, uint32_t xoff, const uint32_t (&e0)[4],
-                                          const uint32_t (&e1)[4], uint32_t &stage, uint32_t &phase,
+                                          uint32_t wrow, uint32_t xoff, const uint32_t (&e0)[NF],
+                                          const uint32_t (&e1)[NF], uint32_t &stage, uint32_t &phase,
                                           int lane, uint64_t timeout_ns) {
 #pragma unroll
     for (int j = 0; j < 4; j += 2) {
@@ -170,8 +175,10 @@ __device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t 
         // Reconverge before the warp-wide mma.sync.aligned: lane 0 alone took the arrive branch of the
         // previous stages and every lane polls the barriers on its own.
         __syncwarp();
-        stage_math<NH, EXACT>(acc, smem + stage * stage_bytes, wrow, xoff, e0, e1, 8u * j);
-        if (two) stage_math<NH, EXACT>(acc, smem + stage2 * stage_bytes, wrow, xoff, e0, e1, 8u * (j + 1));
+        stage_math<NH, NF, EXACT>(acc, smem + stage * stage_bytes, wrow, xoff, e0, e1, 8u * j);
+        if (two)
+            stage_math<NH, NF, EXACT>(acc, smem + stage2 * stage_bytes, wrow, xoff, e0, e1,
+                                      8u * (j + 1));
         // Hand the stages back.  Their operands were read through the generic proxy and the producer's
         // next TMA writes them through the async proxy: each lane orders its reads before that write
         // with a proxy fence (measured on this GPU: without it, whole 64-row blocks picked up data of
@@ -188,18 +195,20 @@ __device__ __forceinline__ bool run_group(float (&acc)[4][NH][4], const uint8_t 
     return true;
 }
 
-// NH = number of 8-column activation halves (1 for M <= 8, 2 for M <= 16).
-template <int NH>
+// NH = number of 8-column activation halves (1 for M <= 8, 2 for M <= 16); NF, STAGES as GCfg.
+template <int NH, int NF, int STAGES_>
 __global__ void __launch_bounds__(THREADS)
 w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                int M, const uint8_t *__restrict__ SW, int64_t ldsw, int sw_vec,
                __half *__restrict__ Y, int64_t ldy, int N, int K, int epi, unsigned *err,
                uint64_t timeout_ns) {
-    using G = GCfg<NH>;
+    using G = GCfg<NH, NF, STAGES_>;
     constexpr int STAGES = G::STAGES;
+    constexpr int ROWS = G::ROWS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    griddep_launch_dependents();   // a dependent launch (e.g. a clock probe) may run beside
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -208,7 +217,7 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const uint32_t red_full = sb + G::OFF_RBAR, red_empty = sb + G::OFF_RBAR + 8;
     float *red = reinterpret_cast<float *>(smem + G::OFF_RED);
 
-    const int nrb = (N + ROWS - 1) / ROWS;     // 64-row blocks
+    const int nrb = (N + ROWS - 1) / ROWS;     // row blocks
     const int nkc = (K + KC - 1) / KC;         // 128-wide K chunks (stages)
     const int ngrp = (nkc + 3) / 4;            // groups of four stages (one 16-byte scale load)
     const int nblk = K / 32;
@@ -225,6 +234,9 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         tma_prefetch_desc(&tmX);
     }
     __syncthreads();
+    // Launched as a programmatic dependent: the CTAs may be resident before the kernel ahead of
+    // this one on the stream has finished.  Nothing in memory is touched before it has.
+    griddep_wait();
 
     if (warp == CONSUMERS) {
         // ------------------------------------------------------------------- producer
@@ -232,6 +244,9 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
+            // The weights are read once: evict-first lines in L2, so the stream replaces its own
+            // lines instead of pushing out (and writing back) what earlier kernels left there.
+            const uint64_t stream_once = l2_policy_evict_first();
             for (int rb = blockIdx.x; rb < nrb && ok; rb += gridDim.x) {
                 for (int kc = 0; kc < nkc; ++kc) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
@@ -240,7 +255,7 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     }
                     const uint32_t st = sb + stage * G::STAGE;
                     mbar_arrive_expect_tx(full_bar(stage), G::STAGE);
-                    tma_load_2d(st, &tmW, full_bar(stage), kc * KC, rb * ROWS);
+                    tma_load_2d_hint(st, &tmW, full_bar(stage), kc * KC, rb * ROWS, stream_once);
                     tma_load_2d(st + G::W_BYTES, &tmX, full_bar(stage), kc * KC, 0);
                     tma_load_2d(st + G::W_BYTES + G::X_HALF, &tmX, full_bar(stage), kc * KC + 64, 0);
                     ++issued;
@@ -277,22 +292,24 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     bool ok = true;
     for (int rb = blockIdx.x; rb < nrb && ok; rb += gridDim.x) {
         // this lane loads the scale rows of fragment t (rows 16 t + g and 16 t + g + 8) and shares
-        // them with the other lanes of its quad
+        // them with the other lanes of its quad (t >= NF: no fragment, neutral bytes)
+        const bool has_frag = t < NF;
         const int nA = rb * ROWS + 16 * t + g;
         const uint8_t *srowA = SW + static_cast<int64_t>(min(nA, N - 1)) * ldsw;
         const uint8_t *srowB = SW + static_cast<int64_t>(min(nA + 8, N - 1)) * ldsw;
-        float acc[4][NH][4];
+        float acc[NF][NH][4];
 #pragma unroll
-        for (int f = 0; f < 4; ++f)
+        for (int f = 0; f < NF; ++f)
 #pragma unroll
             for (int h = 0; h < NH; ++h)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[f][h][i] = 0.f;
-        uint4 rawA = scale_group(srowA, 0, nblk, sw_vec);
-        uint4 rawB = scale_group(srowB, 0, nblk, sw_vec);
+        const uint4 neutral = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        uint4 rawA = has_frag ? scale_group(srowA, 0, nblk, sw_vec) : neutral;
+        uint4 rawB = has_frag ? scale_group(srowB, 0, nblk, sw_vec) : neutral;
         for (int G0 = 0; G0 < ngrp && ok; ++G0) {
             const uint4 cA = rawA, cB = rawB;
-            if (G0 + 1 < ngrp) {        // one group ahead
+            if (G0 + 1 < ngrp && has_frag) {        // one group ahead
                 rawA = scale_group(srowA, G0 + 1, nblk, sw_vec);
                 rawB = scale_group(srowB, G0 + 1, nblk, sw_vec);
             }
@@ -303,22 +320,24 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                             0x5410u);
             // the lanes together hold every row of the block: one vote decides the decode
             const bool exact = __any_sync(0xffffffffu, has_special_byte(pA) || has_special_byte(pB));
-            uint32_t e0[4], e1[4];      // scale bytes of rows 16 f + g (e0) and 16 f + g + 8 (e1)
+            uint32_t e0[NF], e1[NF];    // scale bytes of rows 16 f + g (e0) and 16 f + g + 8 (e1)
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
+            for (int f = 0; f < NF; ++f) {
                 e0[f] = __shfl_sync(0xffffffffu, pA, (g << 2) | f);
                 e1[f] = __shfl_sync(0xffffffffu, pB, (g << 2) | f);
             }
             const int nst = min(4, nkc - 4 * G0);
-            ok = exact ? run_group<NH, true, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst, wrow, xoff,
-                                                     e0, e1, stage, phase, lane, timeout_ns)
-                       : run_group<NH, false, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst, wrow, xoff,
-                                                      e0, e1, stage, phase, lane, timeout_ns);
+            ok = exact ? run_group<NH, NF, true, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst,
+                                                         wrow, xoff, e0, e1, stage, phase, lane,
+                                                         timeout_ns)
+                       : run_group<NH, NF, false, STAGES>(acc, smem, sb, G::STAGE, G::OFF_BAR, nst,
+                                                          wrow, xoff, e0, e1, stage, phase, lane,
+                                                          timeout_ns);
         }
         if (!ok) break;
-        // Row block done: warp w finishes fragment w.  Every warp hands the other three fragments'
-        // sums over through shared memory, one activation half at a time; the four partial sums of
-        // a fragment are added in warp order.  Waits are bounded like the stage waits.
+        // Row block done: warp w < NF finishes fragment w.  Every warp hands its sums over through
+        // shared memory, one activation half at a time; the four partial sums of a fragment are
+        // added in warp order.  Waits are bounded like the stage waits.
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
             if (!mbar_wait(red_empty, rphase ^ 1, timeout_ns)) {
@@ -326,33 +345,33 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 break;
             }
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
+            for (int f = 0; f < NF; ++f) {
                 if (f == w) continue;
-                const int slot = f < w ? f : f - 1;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) red[((w * 3 + slot) * 4 + i) * 32 + lane] = acc[f][h][i];
+                for (int i = 0; i < 4; ++i) red[((w * NF + f) * 4 + i) * 32 + lane] = acc[f][h][i];
             }
             mbar_arrive(red_full);
             if (!mbar_wait(red_full, rphase, timeout_ns)) {
                 ok = false;
                 break;
             }
-            float own[4];
+            float own[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) own[i] = acc[0][h][i];
-#pragma unroll
-            for (int f = 1; f < 4; ++f)
+            for (int f = 0; f < NF; ++f)
                 if (f == w)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) own[i] = acc[f][h][i];
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            if (w < NF) {
 #pragma unroll
-            for (int u = 0; u < CONSUMERS; ++u)
+                for (int u = 0; u < CONSUMERS; ++u)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    sum[i] += u == w ? own[i] : red[((u * 3 + (w < u ? w : w - 1)) * 4 + i) * 32 + lane];
+                    for (int i = 0; i < 4; ++i)
+                        sum[i] += u == w ? own[i] : red[((u * NF + w) * 4 + i) * 32 + lane];
+            }
             mbar_arrive(red_empty);
             rphase ^= 1;
+            if (w >= NF) continue;
             // D fragment: sum[0..1] -> row n0, activations 8h + 2t (+1); sum[2..3] -> n0 + 8
             const int n0 = rb * ROWS + 16 * w + g;
 #pragma unroll
@@ -372,10 +391,11 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     if (!ok && lane == 0) atomicOr(err, ERR_EPILOGUE);
 }
 
-template <int NH>
+template <int NH, int NF, int STAGES>
 cudaError_t launch_nh(const __half *X, int64_t ldx, int M, const qgemm_tensor *W, __half *Y,
                       int64_t ldy, const qgi::LaunchCtx &ctx, bool *encode_ok) {
-    using G = GCfg<NH>;
+    using G = GCfg<NH, NF, STAGES>;
+    constexpr int ROWS = G::ROWS;
     const int N = static_cast<int>(W->rows), K = static_cast<int>(W->k);
     CUtensorMap tmW, tmX;
     *encode_ok = qgi::encode_tma_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->data, K, N, W->ld, KC,
@@ -383,19 +403,31 @@ cudaError_t launch_nh(const __half *X, int64_t ldx, int M, const qgemm_tensor *W
                  qgi::encode_tma_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, ldx * 2, 64,
                                     8 * NH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
-    auto kern = w8_gemv_kernel<NH>;
+    auto kern = w8_gemv_kernel<NH, NF, STAGES>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
     const int nrb = (N + ROWS - 1) / ROWS;
-    const int per_sm = 232448 / G::SMEM;       // CTAs that fit in one SM's shared memory
+    const int per_sm = 233472 / (G::SMEM + 1024);   // CTAs that fit in one SM's shared memory
     int grid = ctx.num_sms * (per_sm < 1 ? 1 : per_sm);
     if (grid > nrb) grid = nrb;
     const uintptr_t sp = reinterpret_cast<uintptr_t>(W->scales);
     const int sw_vec = (sp % 16 == 0 && W->lds % 16 == 0) ? 2 : (sp % 4 == 0 && W->lds % 4 == 0) ? 1 : 0;
-    kern<<<grid, THREADS, G::SMEM, ctx.stream>>>(tmW, tmX, M, W->scales, W->lds, sw_vec, Y, ldy, N,
-                                                 K, ctx.epi, ctx.err, ctx.timeout_ns);
-    return cudaGetLastError();
+    // A programmatic dependent of the kernel ahead on the stream: launch, set-up and barrier
+    // initialisation overlap that kernel's last CTAs (each kernel boundary otherwise costs about
+    // 3 us on this GPU, against a 38 us weight stream).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = G::SMEM;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, M, W->scales, W->lds, sw_vec, Y, ldy, N, K,
+                              ctx.epi, ctx.err, ctx.timeout_ns);
 }
 
 }  // namespace
@@ -404,8 +436,8 @@ namespace qgi {
 
 cudaError_t launch_w8_gemv(const __half *X, int64_t ldx, int M, const qgemm_tensor *W,
                            __half *Y, int64_t ldy, const LaunchCtx &ctx, bool *encode_ok) {
-    if (M <= 8) return launch_nh<1>(X, ldx, M, W, Y, ldy, ctx, encode_ok);
-    return launch_nh<2>(X, ldx, M, W, Y, ldy, ctx, encode_ok);
+    if (M <= 8) return launch_nh<1, 3, 6>(X, ldx, M, W, Y, ldy, ctx, encode_ok);
+    return launch_nh<2, 4, 5>(X, ldx, M, W, Y, ldy, ctx, encode_ok);
 }
 
 }  // namespace qgi
