@@ -260,27 +260,6 @@ constexpr uint32_t P_IDESC = (1u << 4) | (1u << 16) | (static_cast<uint32_t>(P_B
 constexpr uint32_t P_IDESC_HALF = (1u << 4) | (1u << 16) | (static_cast<uint32_t>((P_BN / 2) >> 3) << 17) |
                                 (static_cast<uint32_t>(256 >> 4) << 24);
 
-// Work items of a pair kernel: whole tiles, then (when the leftover tiles fit twice into one wave
-// of pairs) each leftover tile as two column halves.  half < 0 marks a whole tile.
-struct PairWork {
-    int full_items, n_items;
-    __device__ __forceinline__ PairWork(int num_tiles, int npairs) {
-        const int rem = num_tiles % npairs;
-        const bool split = rem > 0 && 2 * rem <= npairs;
-        full_items = num_tiles - (split ? rem : 0);
-        n_items = full_items + (split ? 2 * rem : 0);
-    }
-    __device__ __forceinline__ void item(int it, int &tile, int &half) const {
-        if (it < full_items) {
-            tile = it;
-            half = -1;
-        } else {
-            tile = full_items + ((it - full_items) >> 1);
-            half = (it - full_items) & 1;
-        }
-    }
-};
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,

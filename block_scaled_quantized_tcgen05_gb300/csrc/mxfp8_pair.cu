@@ -192,6 +192,7 @@ sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
 template <class F>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB64,
                const uint8_t *__restrict__ packA, const uint8_t *__restrict__ packB,
                int rbpA, int rbpB, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N,
                int K, int epi, unsigned *err, uint64_t timeout_ns) {
@@ -225,6 +226,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
     const int KT = (K + BK - 1) / BK;
+    const PairWork work(num_tiles, npairs);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -238,6 +240,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmB64);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(slot)), TMEM_COLS);
@@ -256,30 +259,36 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int issued = 0;
             bool ok = true;
             const uint64_t keep = l2_policy_evict_last();   // B panels are re-read by many tiles
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                int mb, nb;
+            for (int it = pair; it < work.n_items && ok; it += npairs) {
+                int tile, half, mb, nb;
+                work.item(it, tile, half);
                 tile_coords(tile, tiles_m, tiles_n, mb, nb);
                 const int m0 = mb * 2 * BM + static_cast<int>(rank) * BM;
-                const int nh = nb * BN + static_cast<int>(rank) * (BN / 2);
                 const int la = (2 * mb + static_cast<int>(rank)) * 32;   // packed A line
-                const int lb = 2 * nb * 32;                               // packed B line
+                // a whole tile: 128 B rows per CTA and both 128-row blocks of B scales; a half
+                // tile: 64 B rows per CTA and the one block of scales of its 128 columns
+                const int nh = half < 0 ? nb * BN + static_cast<int>(rank) * (BN / 2)
+                                        : nb * BN + half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
+                const int lb = (2 * nb + (half < 0 ? 0 : half)) * 32;     // packed B line
+                const uint32_t b_bytes = half < 0 ? B_BYTES : B_BYTES / 2;
+                const uint32_t sfb_bytes = half < 0 ? SFB_BYTES : SFB_BYTES / 2;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), L::STAGE_TX);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_BYTES + b_bytes));
                     tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
-                    tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, &tmB, lead_full, kt * BK,
-                                          nh, keep);
-                    mbar_arrive_expect_tx(sf_full(stage), L::SF_TX);
+                    tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, half < 0 ? &tmB : &tmB64,
+                                          lead_full, kt * BK, nh, keep);
+                    mbar_arrive_expect_tx(sf_full(stage), SFA_BYTES + sfb_bytes);
                     bulk_load(sb + OFF_SFA + stage * SFA_BYTES,
                               packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W,
                               SFA_BYTES, sf_full(stage));
                     bulk_load(sb + OFF_SFB + stage * SFB_BYTES,
                               packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W,
-                              SFB_BYTES, sf_full(stage));
+                              sfb_bytes, sf_full(stage));
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -304,7 +313,13 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint64_t bdesc0 = smem_desc(sb + OFF_B, 16, 1024, SWZ_128B);
             uint32_t acc_phase = 0, stage = 0, phase = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+            for (int it = pair; it < work.n_items && ok; it += npairs) {
+                int tile, half;
+                work.item(it, tile, half);
+                // N = 256, or 128 for a half tile
+                const uint32_t idesc = half < 0 ? F::IDESC
+                                                : (F::IDESC & ~(0x3Fu << 17)) |
+                                                      (static_cast<uint32_t>((BN / 2) >> 3) << 17);
                 if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns)) {
                     ok = false;
                     break;
@@ -325,7 +340,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (uint32_t j = 0; j < BK / 32; ++j) {
                         const uint32_t blk = j * W, w = blk >> 2, id = blk & 3;
                         F::mma(tmem_base, adesc + 2 * j, bdesc + 2 * j,
-                               F::IDESC | (id << 4) | (id << 29), sf_col + 4 * w,
+                               idesc | (id << 4) | (id << 29), sf_col + 4 * w,
                                sf_col + 4 * W + 8 * w, (kt > 0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit_pair(empty_bar(stage), 3);
@@ -351,8 +366,8 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // 4 W + 8 w .. 4 W + 8 w + 7 the B scales of rows i + 32 c.
         const uint32_t q = warp & 3;
         const uint32_t lead_full = map_to_cta(full_bar(0), 0);
-        const int my_tiles = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
-        const int total = my_tiles * KT;
+        const int my_items = pair < work.n_items ? (work.n_items - pair + npairs - 1) / npairs : 0;
+        const int total = my_items * KT;
         for (int it = 0; it < total; ++it) {
             const uint32_t s = static_cast<uint32_t>(it % STAGES);
             // the TMA of this stage was issued after the MMAs that last read this slot finished
@@ -385,8 +400,9 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t half = (warp - 2) >> 2;            // accumulator columns [128 h, 128 h + 128)
         const uint32_t lead_empty = map_to_cta(tmem_empty, 0);
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < num_tiles; tile += npairs) {
-            int mb, nb;
+        for (int it = pair; it < work.n_items; it += npairs) {
+            int tile, thalf, mb, nb;
+            work.item(it, tile, thalf);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
@@ -394,16 +410,27 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tc_fence_after();
             const int em0 = mb * 2 * BM + static_cast<int>(rank) * BM;
-            const int en0 = nb * BN + static_cast<int>(half) * (BN / 2);
-            if (epi & EPI_ACC_BIT)   // reads the old C: chunk by chunk
-                epilogue_tile<BN / 2, 3>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0, en0, M,
-                                         N, c_vec != 0, lead_empty,
-                                         sb + OFF_EPI + (warp - 2) * 2048, epi);
-            else
-                epilogue_tile_early<BN / 2>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0, en0,
-                                            M, N, c_vec != 0, lead_empty,
-                                            sb + OFF_EPI + (warp - 2) * 2048,
-                                            (epi & EPI_RELU_BIT) != 0);
+            const uint32_t stg = sb + OFF_EPI + (warp - 2) * 2048;
+            if (thalf < 0) {
+                const int en0 = nb * BN + static_cast<int>(half) * (BN / 2);
+                if (epi & EPI_ACC_BIT)   // reads the old C: chunk by chunk
+                    epilogue_tile<BN / 2, 3>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0,
+                                             en0, M, N, c_vec != 0, lead_empty, stg, epi);
+                else
+                    epilogue_tile_early<BN / 2>(tmem_base + half * (BN / 2), q, lane, C, ldc, em0,
+                                                en0, M, N, c_vec != 0, lead_empty, stg,
+                                                (epi & EPI_RELU_BIT) != 0);
+            } else {
+                // a half tile's 128 accumulator columns, 64 per warp of each lane quarter
+                const int en0 = nb * BN + thalf * (BN / 2) + static_cast<int>(half) * (BN / 4);
+                if (epi & EPI_ACC_BIT)
+                    epilogue_tile<BN / 4, 3>(tmem_base + half * (BN / 4), q, lane, C, ldc, em0,
+                                             en0, M, N, c_vec != 0, lead_empty, stg, epi);
+                else
+                    epilogue_tile_early<BN / 4>(tmem_base + half * (BN / 4), q, lane, C, ldc, em0,
+                                                en0, M, N, c_vec != 0, lead_empty, stg,
+                                                (epi & EPI_RELU_BIT) != 0);
+            }
             acc_phase ^= 1;
         }
     }
@@ -455,11 +482,13 @@ cudaError_t launch_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __h
     const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows);
     const int Kb = static_cast<int>(k_bytes<F>(A));
     const int rbpA = padded_blocks(M), rbpB = padded_blocks(N);
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmB64;
     *encode_ok =
         qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->data, Kb, M, A->ld, BK, BM,
                            CU_TENSOR_MAP_SWIZZLE_128B) &&
         qgi::encode_tma_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, Kb, N, B->ld, BK, BN / 2,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+        qgi::encode_tma_2d(&tmB64, CU_TENSOR_MAP_DATA_TYPE_UINT8, B->data, Kb, N, B->ld, BK, BN / 4,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (!*encode_ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(mx_pair_kernel<F>,
@@ -471,7 +500,7 @@ cudaError_t launch_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __h
     if (pairs > tiles) pairs = tiles;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     mx_pair_kernel<F><<<2 * pairs, THREADS, Smem<F>::BYTES, ctx.stream>>>(
-        tmA, tmB, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err,
+        tmA, tmB, tmB64, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err,
         ctx.timeout_ns);
     return cudaGetLastError();
 }

@@ -26,6 +26,30 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     nb = r / gsize;
 }
 
+// Work items of a persistent CTA-pair kernel: whole tiles, then -- when the tiles left after the
+// last full wave of pairs fit twice into one wave -- each leftover tile as two column halves, so
+// the last wave takes half a tile's time instead of a whole one.  half < 0 marks a whole tile.
+// A column of the product does not depend on the other columns, so the split leaves every output
+// bit unchanged.
+struct PairWork {
+    int full_items, n_items;
+    __device__ __forceinline__ PairWork(int num_tiles, int npairs) {
+        const int rem = num_tiles % npairs;
+        const bool split = rem > 0 && 2 * rem <= npairs;
+        full_items = num_tiles - (split ? rem : 0);
+        n_items = full_items + (split ? 2 * rem : 0);
+    }
+    __device__ __forceinline__ void item(int it, int &tile, int &half) const {
+        if (it < full_items) {
+            tile = it;
+            half = -1;
+        } else {
+            tile = full_items + ((it - full_items) >> 1);
+            half = (it - full_items) & 1;
+        }
+    }
+};
+
 __device__ __forceinline__ uint8_t *align_1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }

@@ -182,3 +182,19 @@ def test_mxfp4_full_size_sampled(dev, orc):
         C2 = torch.empty_like(C)
         q.qgemm_mxfp4(A, B, C2)
         assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
+
+
+def test_mxfp4_last_wave_half_tiles(dev, orc):
+    """2048 x 3072: 76 whole pair tiles, then 20 left over as two 256 x 128 halves each; every
+    element against the oracle, and the split columns bit-identical to whole tiles."""
+    M, N, K = 2048, 3072, 512
+    d = synth.mxfp4_inputs(M, N, K, seed=63, row_variance=True)
+    A, B, _keep = _views(d, dev)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_mxfp4(A, B, C)
+    _check(C, _oracle(orc, d), orc, what="mxfp4 half tiles")
+    Bs = q.qgemm_tensor_slice(B, 2304, 768, 0, K)
+    Cs = torch.full((M, 768), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_mxfp4(A, Bs, Cs)
+    torch.cuda.synchronize()
+    assert torch.equal(Cs.view(torch.int16), C[:, 2304:].view(torch.int16))

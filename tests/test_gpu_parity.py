@@ -222,6 +222,36 @@ def test_mxfp8_full_size_sampled(dev, orc):
         assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
 
 
+@pytest.mark.parametrize("epi", [None, (True, True)])
+def test_mxfp8_last_wave_half_tiles(dev, orc, epi):
+    """2048 x 3072 has 96 pair tiles: 76 whole ones, then 20 left over, each run as two 256 x 128
+    halves.  Every element against the oracle, and the columns of the split tiles bit-identical
+    to the same columns computed as whole tiles (B sliced to its last 768 rows: 24 whole tiles)."""
+    M, N, K = 2048, 3072, 256
+    d = synth.mxfp8_inputs(M, N, K, seed=61, row_variance=True)
+    A, B, (a, sa, b, sb) = _mx_views(d, dev)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    c_old = (torch.randn(M, N, generator=synth.generator(62)) * 3).to(torch.float16)
+    if epi:
+        C.copy_(c_old.to(dev))
+        q.qgemm_mxfp8_ex(A, B, C, accumulate=True, relu=True)
+    else:
+        q.qgemm_mxfp8(A, B, C)
+    res = orc.mxfp8(d["a"].numpy(), d["sa"].numpy(), d["b"].numpy(), d["sb"].numpy())
+    if epi:
+        res = orc.epilogue(res, c_old.numpy(), relu=True)
+    _check(C, res, orc, what=f"mxfp8 half tiles epi={epi}")
+    Bs = q.qgemm_tensor_slice(B, 2304, 768, 0, K)
+    Cs = torch.full((M, 768), float("nan"), dtype=torch.float16, device=dev)
+    if epi:
+        Cs.copy_(c_old[:, 2304:].to(dev))
+        q.qgemm_mxfp8_ex(A, Bs, Cs, accumulate=True, relu=True)
+    else:
+        q.qgemm_mxfp8(A, Bs, Cs)
+    torch.cuda.synchronize()
+    assert torch.equal(Cs.view(torch.int16), C[:, 2304:].view(torch.int16))
+
+
 # ------------------------------------------------------------------------------- fp16
 # (1024, 4864, 128): exactly one wave of 256 x 256 pair tiles on 76 pairs
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 328, 200), (96, 64, 512),
