@@ -8,27 +8,36 @@
 // exponentiated tile to the second product straight from registers when its layout allows.
 //
 // The GB300 form of that recipe:
-//   * one CTA per (head, 128 query rows), head dimension 128; K and V tiles of 128 keys arrive
-//     by TMA (3-D maps: d, row, head) into three stages of shared memory each, from two
-//     producer threads (K runs ahead of V); a K stage is released when its scores are done, a
-//     V stage when its P V is done;
-//   * S = Q K^T for a key tile is one tcgen05.mma chain (M = 128 queries, N = 128 keys,
-//     K = 128) into one of three 128-column TMEM buffers: the scores of tile j + 3 are issued
-//     right after P V of tile j, so the softmax never waits for a P V -> S chain to drain;
-//   * a TMEM lane is a query row, so each softmax thread owns a whole row: it reads its 128
-//     scores into registers (tcgen05.ld), and the row maximum, the exponentials and the row sum
-//     are in-register loops -- no exchange at all;
-//   * the thread writes its row of P = exp2(s * scale * log2 e - m) as fp16 back into the same
-//     TMEM columns (tcgen05.st) and the second product O += P V takes P as its A operand
-//     straight from TMEM (the GB300 counterpart of passing the cooperative tensor as the left
-//     input); V is read from shared memory as an MN-major operand (keys along K, d along N);
+//   * one CTA per (head, 256 query rows), held as two query tiles of 128 rows, head dimension
+//     128; K and V tiles of 128 keys arrive by TMA (3-D maps: d, row, head) from two producer
+//     threads (three K stages, two V stages), each shared by both query tiles;
+//   * TMEM holds, per query tile t, a 128-column score buffer S_t and a 128-column output
+//     accumulator O_t.  S_t = Q_t K_j^T is one tcgen05.mma chain (M = N = K = 128);
+//   * a TMEM lane is a query row, so each softmax thread owns a whole row: it takes the row's
+//     maximum over the tile's 128 scores, writes P = exp2(s * scale * log2 e - m) as fp16 back
+//     over its own scores (tcgen05.st), and the second product O_t += P V_j takes P as its A
+//     operand straight from TMEM (the GB300 counterpart of passing the cooperative tensor as
+//     the left input); V is read from shared memory as an MN-major operand;
+//   * two softmax warpgroups, one per query tile, alternate with the tensor pipe: the MMA warp
+//     issues, per key tile, one block with P V for tile 0 and the next scores of tile 0, then one
+//     with P V for tile 1 and the next scores of tile 1, so while one warpgroup exponentiates its
+//     scores the tensor pipe works for the other.  The whole MMA warp runs the loop and one
+//     elected lane issues (measured on GB300: a lone thread issues a tcgen05.mma in about 57
+//     cycles, an elected lane of a converged warp in about 14, and the pipe queues about 8 MMAs
+//     of 128 x 128 x 16 ahead); the waits before a block test their barriers together, so
+//     their latencies overlap;
 //   * the running maximum m is raised only when a tile's maximum exceeds it by more than 8 (in
-//     log2 units); P then stays below 2^8 in fp16 and the rescale of O in TMEM (read, multiply,
-//     write back, after the previous P V has completed) is rare;
-//   * after the last tile each thread divides its row of O by its row sum and stores it.
+//     log2 units); P then stays below 2^8 in fp16 and the rescale of O_t in TMEM (read, multiply,
+//     write back) is rare.  It needs no extra wait: the commit that reports S_t(j) ready also
+//     covers every MMA issued before it, P V of tile j - 1 included.  The first half of P is
+//     computed with m as it stands while the tile's maximum is taken; only when the maximum
+//     moves is it computed again;
+//   * after the last key tile each thread divides its row of O by its row sum and stores it.
 // Keys past Lk (TMA zero fill) are masked to -inf; query rows past Lq are computed and dropped.
-// Roles: warp 0 TMA producer of Q and K, warp 1 MMA issuer (one thread), warps 2-5 softmax and
-// epilogue, warp 6 TMA producer of V.
+// Roles: warp 0 TMA producer of Q and K, warp 1 MMA issuer (one elected lane) and TMEM owner,
+// warp 2 TMA producer of V, warp 3 idle, warps 4-7 softmax of query tile 0, warps 8-11 of query
+// tile 1
+// (warp w reads TMEM lane quarter w % 4).
 // Every wait is bounded; on a timeout the kernel records the error bit, stops issuing work,
 // waits for its MMAs, frees TMEM and returns.
 #include "qgemm_common.cuh"
@@ -39,28 +48,31 @@ namespace {
 
 using namespace qg;
 
-constexpr int BQ = 128;                 // query rows per CTA
+constexpr int BQ = 128;                 // query rows per query tile
+constexpr int QT = 2;                   // query tiles per CTA
 constexpr int BKV = 128;                // keys per tile
 constexpr int HD = 128;                 // head dimension
-constexpr int KV_STAGES = 3;
-constexpr int THREADS = 32 * 7;
+constexpr int K_STAGES = 3;
+constexpr int V_STAGES = 2;
+constexpr int SOFTMAX_WARP0 = 4;
+constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 4 * QT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NSB = 3;                  // score buffers of 128 columns from column 0
-constexpr uint32_t S_COL0 = 0;
-constexpr uint32_t O_COL = 128 * NSB;   // output accumulator, 128 columns
+__host__ __device__ constexpr uint32_t s_col(int t) { return 128u * t; }          // S_t
+__host__ __device__ constexpr uint32_t o_col(int t) { return 128u * (QT + t); }   // O_t
 
 constexpr uint32_t HALF_BYTES = 128 * 128;            // 128 rows x 64 halves (one swizzle span)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;       // 128 rows x 128 halves
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
-constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE_BYTES;
-// q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NSB], p_full[NSB],
-// pv_done[NSB], drain, then the TMEM slot
-constexpr int NBARS = 1 + 4 * KV_STAGES + 3 * NSB + 1;
+constexpr uint32_t OFF_K = OFF_Q + QT * TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE_BYTES;
+// q_full, k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[QT], p_full[QT], o_done[QT],
+// drain, then the TMEM slot
+constexpr int NBARS = 1 + 2 * K_STAGES + 2 * V_STAGES + 3 * QT + 1;
 constexpr uint32_t OFF_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(QT == 2, "the MMA issue order is written for two query tiles");
 
 // kind::f16, D fp32, A and B fp16, M = 128, N = 128.  S: both operands K-major.  P V: B (V) is
 // MN-major (bit 16): keys run along K with a 128-byte row per key, d along N.
@@ -74,48 +86,41 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// One key tile of one query row: the running maximum m (log2 units) is given; writes
-// P = 2^(s c - m) as fp16 pairs into TMEM columns scol .. scol + 63 of this warp's lanes and
-// returns the row sum of P.  Every exponential is one ex2.approx (measured: moving a share of them
-// to a cubic on the FMA pipe costs more issue slots than it saves).  MASK: keys >= valid give 0.
+// 64 keys of one query row (key k0 + i of the tile in v[i]): P = 2^(s c - m) as 32 fp16 pairs
+// in pk; returns their sum.  Every exponential is one ex2.approx (measured: taking a share of
+// them from a polynomial on the FMA pipe makes the softmax slower, not faster).  MASK: keys >=
+// valid give 0.
 template <bool MASK>
-__device__ __forceinline__ float softmax_tile(const uint32_t (&v)[128], int valid, float c,
-                                              float m, uint32_t scol) {
-    // row sum in four fp32 lanes (two packed pairs), scaled scores formed a pair at a time
+__device__ __forceinline__ float exp_half(const uint32_t (&v)[64], int k0, int valid, float c,
+                                          float m, uint32_t (&pk)[32]) {
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {                      // 64 keys -> 32 packed columns
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int k0 = 64 * h + 2 * i;
-            float x0, x1;
-            fma2(x0, x1, __uint_as_float(v[k0]), __uint_as_float(v[k0 + 1]), c, c, -m, -m);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            if (MASK) {
-                p0 = k0 < valid ? p0 : 0.0f;
-                p1 = k0 + 1 < valid ? p1 : 0.0f;
-            }
-            const int a = 2 * (i & 1);
-            add2(acc[a], acc[a + 1], p0, p1);
-            pk[i] = pack_f16x2(p0, p1);
+    for (int i = 0; i < 32; ++i) {
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), c, c, -m, -m);
+        float p0 = ex2_approx(x0);
+        float p1 = ex2_approx(x1);
+        if (MASK) {
+            p0 = k0 + 2 * i < valid ? p0 : 0.0f;
+            p1 = k0 + 2 * i + 1 < valid ? p1 : 0.0f;
         }
-        tmem_st_32x32b_x32(scol + 32 * h, pk);
+        const int a = 2 * (i & 1);
+        add2(acc[a], acc[a + 1], p0, p1);
+        pk[i] = pack_f16x2(p0, p1);
     }
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// Row maximum of the tile's raw scores; MASK: only keys < valid count.
+// Maximum of 64 raw scores (keys k0 .. k0 + 63 of the tile); MASK: only keys < valid count.
 template <bool MASK>
-__device__ __forceinline__ float tile_max(const uint32_t (&v)[128], int valid) {
+__device__ __forceinline__ float half_max(const uint32_t (&v)[64], int k0, int valid) {
     float mx[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
     if constexpr (!MASK) {
-        // three-input maximum: 64 instructions for the 128 scores, eight independent chains
+        // three-input maximum: 32 instructions for the 64 scores, eight independent chains
 #pragma unroll
-        for (int i = 0; i < 128; i += 2) {
+        for (int i = 0; i < 64; i += 2) {
             const int k = (i >> 1) & 7;
             asm("max.f32 %0, %1, %2, %3;"
                 : "=f"(mx[k])
@@ -123,9 +128,9 @@ __device__ __forceinline__ float tile_max(const uint32_t (&v)[128], int valid) {
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 64; ++i) {
             const float x = __uint_as_float(v[i]);
-            mx[i & 7] = fmaxf(mx[i & 7], i < valid ? x : -INFINITY);
+            mx[i & 7] = fmaxf(mx[i & 7], k0 + i < valid ? x : -INFINITY);
         }
     }
     return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -142,32 +147,35 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const int head = blockIdx.y;
-    const int q0 = blockIdx.x * BQ;
+    const int q0 = blockIdx.x * (QT * BQ);
     const int nkv = (Lk + BKV - 1) / BKV;
 
     const uint32_t q_full = sb + OFF_BAR;
     auto k_full = [&](int s) { return sb + OFF_BAR + 8u * (1 + s); };
-    auto v_full = [&](int s) { return sb + OFF_BAR + 8u * (1 + KV_STAGES + s); };
-    auto k_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 2 * KV_STAGES + s); };
-    auto v_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 3 * KV_STAGES + s); };
-    auto s_full = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + b); };
-    auto p_full = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + NSB + b); };
-    auto pv_done = [&](int b) { return sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + 2 * NSB + b); };
-    const uint32_t drain_bar = sb + OFF_BAR + 8u * (1 + 4 * KV_STAGES + 3 * NSB);
+    auto k_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + K_STAGES + s); };
+    auto v_full = [&](int s) { return sb + OFF_BAR + 8u * (1 + 2 * K_STAGES + s); };
+    auto v_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 2 * K_STAGES + V_STAGES + s); };
+    constexpr int B0 = 1 + 2 * K_STAGES + 2 * V_STAGES;
+    auto s_full = [&](int t) { return sb + OFF_BAR + 8u * (B0 + t); };
+    auto p_full = [&](int t) { return sb + OFF_BAR + 8u * (B0 + QT + t); };
+    auto o_done = [&](int t) { return sb + OFF_BAR + 8u * (B0 + 2 * QT + t); };
+    const uint32_t drain_bar = sb + OFF_BAR + 8u * (B0 + 3 * QT);
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < KV_STAGES; ++s) {
+        for (int s = 0; s < K_STAGES; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(v_full(s), 1);
             mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < V_STAGES; ++s) {
+            mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
-        for (int b = 0; b < NSB; ++b) {
-            mbar_init(s_full(b), 1);
-            mbar_init(p_full(b), 4);     // one arrival per softmax warp
-            mbar_init(pv_done(b), 1);
+        for (int t = 0; t < QT; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 4);     // one arrival per softmax warp of the tile
+            mbar_init(o_done(t), 1);
         }
         mbar_init(drain_bar, 1);
         fence_barrier_init();
@@ -184,148 +192,208 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = *slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer of Q and K
-        if (lane == 0) {
-            bool ok = true;
-            mbar_arrive_expect_tx(q_full, TILE_BYTES);
-            tma_load_3d(sb + OFF_Q, &tmQ, q_full, 0, q0, head);
-            tma_load_3d(sb + OFF_Q + HALF_BYTES, &tmQ, q_full, 64, q0, head);
-            int issued = 0;
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j % KV_STAGES;
-                if (!mbar_wait(k_empty(st), ((j / KV_STAGES) & 1) ^ 1, timeout_ns)) {
-                    ok = false;
-                    break;
+    // warpgroup 0 (producers, MMA issuer) needs few registers; the softmax warpgroups hold a row
+    // of 128 scores each: 72 x 128 + 208 x 256 <= 168 x 384, the registers the block is launched
+    // with.  One reallocation per warpgroup, outside the role branches.
+    if (warp < SOFTMAX_WARP0) {
+        regs_release<72>();
+        if (warp == 0) {
+            // ------------------------------------------------------ producer of Q and K
+            if (lane == 0) {
+                bool ok = true;
+                mbar_arrive_expect_tx(q_full, QT * TILE_BYTES);
+                for (int t = 0; t < QT; ++t) {
+                    tma_load_3d(sb + OFF_Q + t * TILE_BYTES, &tmQ, q_full, 0, q0 + t * BQ, head);
+                    tma_load_3d(sb + OFF_Q + t * TILE_BYTES + HALF_BYTES, &tmQ, q_full, 64, q0 + t * BQ,
+                                head);
                 }
-                const uint32_t sk = sb + OFF_K + st * TILE_BYTES;
-                mbar_arrive_expect_tx(k_full(st), TILE_BYTES);
-                tma_load_3d(sk, &tmK, k_full(st), 0, j * BKV, head);
-                tma_load_3d(sk + HALF_BYTES, &tmK, k_full(st), 64, j * BKV, head);
-                ++issued;
-            }
-            if (!ok) atomicOr(err, ERR_PRODUCER);
-            // no copy may be in flight when the CTA exits
-            bool drained = mbar_wait(q_full, 0, timeout_ns);
-            for (int i = max(0, issued - KV_STAGES); i < issued && drained; ++i)
-                drained = mbar_wait(k_full(i % KV_STAGES), (i / KV_STAGES) & 1, timeout_ns);
-            if (!drained) atomicOr(err, ERR_DRAIN);
-        }
-        __syncwarp();
-    } else if (warp == 6) {
-        // ----------------------------------------------------------- producer of V
-        if (lane == 0) {
-            bool ok = true;
-            int issued = 0;
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j % KV_STAGES;
-                if (!mbar_wait(v_empty(st), ((j / KV_STAGES) & 1) ^ 1, timeout_ns)) {
-                    ok = false;
-                    break;
+                int issued = 0;
+                for (int j = 0; j < nkv; ++j) {
+                    const int st = j % K_STAGES;
+                    if (!mbar_wait(k_empty(st), ((j / K_STAGES) & 1) ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sk = sb + OFF_K + st * TILE_BYTES;
+                    mbar_arrive_expect_tx(k_full(st), TILE_BYTES);
+                    tma_load_3d(sk, &tmK, k_full(st), 0, j * BKV, head);
+                    tma_load_3d(sk + HALF_BYTES, &tmK, k_full(st), 64, j * BKV, head);
+                    ++issued;
                 }
-                const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
-                mbar_arrive_expect_tx(v_full(st), TILE_BYTES);
-                tma_load_3d(sv, &tmV, v_full(st), 0, j * BKV, head);
-                tma_load_3d(sv + HALF_BYTES, &tmV, v_full(st), 64, j * BKV, head);
-                ++issued;
+                if (!ok) atomicOr(err, ERR_PRODUCER);
+                // no copy may be in flight when the CTA exits
+                bool drained = mbar_wait(q_full, 0, timeout_ns);
+                for (int i = max(0, issued - K_STAGES); i < issued && drained; ++i)
+                    drained = mbar_wait(k_full(i % K_STAGES), (i / K_STAGES) & 1, timeout_ns);
+                if (!drained) atomicOr(err, ERR_DRAIN);
             }
-            if (!ok) atomicOr(err, ERR_PRODUCER);
-            bool drained = true;
-            for (int i = max(0, issued - KV_STAGES); i < issued && drained; ++i)
-                drained = mbar_wait(v_full(i % KV_STAGES), (i / KV_STAGES) & 1, timeout_ns);
-            if (!drained) atomicOr(err, ERR_DRAIN);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // --------------------------------------------------------- MMA issuer
-            const uint64_t qdesc = smem_desc(sb + OFF_Q, 16, 1024, SWZ_128B);
-            bool ok = mbar_wait(q_full, 0, timeout_ns);
-            auto issue_s = [&](int j) -> bool {
-                const int b = j % NSB, st = j % KV_STAGES;
-                if (!mbar_wait(k_full(st), (j / KV_STAGES) & 1, timeout_ns)) return false;
-                tc_fence_after();
-                const uint64_t kdesc = smem_desc(sb + OFF_K + st * TILE_BYTES, 16, 1024, SWZ_128B);
+            __syncwarp();
+        } else if (warp == 2) {
+            // ----------------------------------------------------------- producer of V
+            if (lane == 0) {
+                bool ok = true;
+                int issued = 0;
+                for (int j = 0; j < nkv; ++j) {
+                    const int st = j % V_STAGES;
+                    if (!mbar_wait(v_empty(st), ((j / V_STAGES) & 1) ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
+                    mbar_arrive_expect_tx(v_full(st), TILE_BYTES);
+                    tma_load_3d(sv, &tmV, v_full(st), 0, j * BKV, head);
+                    tma_load_3d(sv + HALF_BYTES, &tmV, v_full(st), 64, j * BKV, head);
+                    ++issued;
+                }
+                if (!ok) atomicOr(err, ERR_PRODUCER);
+                bool drained = true;
+                for (int i = max(0, issued - V_STAGES); i < issued && drained; ++i)
+                    drained = mbar_wait(v_full(i % V_STAGES), (i / V_STAGES) & 1, timeout_ns);
+                if (!drained) atomicOr(err, ERR_DRAIN);
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ----------------------------------------------------------------- MMA issuer
+            // The whole warp runs the loop and waits; one elected lane issues (a loop run by one
+            // lane alone issues measurably slower).
+            bool ok = mbar_wait_warp(q_full, 0, timeout_ns);
+            const uint64_t qdesc0 = smem_desc(sb + OFF_Q, 16, 1024, SWZ_128B);
+            const uint64_t kdesc0 = smem_desc(sb + OFF_K, 16, 1024, SWZ_128B);
+            // V's descriptor: keys 16 kk .. 16 kk + 15 start 16 kk x 128 bytes into each span,
+            // the second 64 of d is the other span (leading offset), the next 8 keys 1024 bytes
+            // on (stride offset).
+            const uint64_t vdesc0 = smem_desc(sb + OFF_V, HALF_BYTES, 1024, SWZ_128B);
+            auto mma_s = [&](int t, int j) {   // S_t = Q_t K_j^T
+                const uint64_t qdesc = qdesc0 + static_cast<uint64_t>(t) * (TILE_BYTES >> 4);
+                const uint64_t kdesc =
+                    kdesc0 + static_cast<uint64_t>(j % K_STAGES) * (TILE_BYTES >> 4);
 #pragma unroll
                 for (uint32_t kk = 0; kk < HD / 16; ++kk) {
                     // 16 of d per MMA: span kk / 4 (64 halves each), 32 bytes kk % 4 into it
                     const uint64_t off = (kk >> 2) * (HALF_BYTES >> 4) + 2 * (kk & 3);
-                    mma_f16(tmem_base + S_COL0 + 128 * b, qdesc + off, kdesc + off, IDESC_S,
+                    mma_f16(tmem_base + s_col(t), qdesc + off, kdesc + off, IDESC_S,
                             kk > 0 ? 1u : 0u);
                 }
-                tc_commit(s_full(b));
-                tc_commit(k_empty(st));
-                return true;
             };
-            auto issue_pv = [&](int j) -> bool {
-                const int b = j % NSB, st = j % KV_STAGES;
-                if (!mbar_wait(p_full(b), (j / NSB) & 1, timeout_ns)) return false;
-                if (!mbar_wait(v_full(st), (j / KV_STAGES) & 1, timeout_ns)) return false;
-                tc_fence_after();
-                const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
+            auto mma_pv = [&](int t, int j) {   // O_t += P_t V_j, P_t in S_t's first 64 columns
+                const uint64_t vdesc =
+                    vdesc0 + static_cast<uint64_t>(j % V_STAGES) * (TILE_BYTES >> 4);
 #pragma unroll
-                for (uint32_t kk = 0; kk < BKV / 16; ++kk) {
-                    // keys 16 kk .. 16 kk + 15: P columns 8 kk.. (two fp16 per column); V rows
-                    // start 16 kk x 128 bytes into each span; the second 64 of d is the other
-                    // span (leading offset), the next 8 keys 1024 bytes on (stride offset)
-                    const uint64_t vdesc = smem_desc(sv + kk * 2048, HALF_BYTES, 1024, SWZ_128B);
-                    mma_f16_ta(tmem_base + O_COL, tmem_base + S_COL0 + 128 * b + 8 * kk, vdesc,
-                               IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(v_empty(st));
-                tc_commit(pv_done(b));
-                return true;
+                for (uint32_t kk = 0; kk < BKV / 16; ++kk)   // keys 16 kk ..: P columns 8 kk ..
+                    mma_f16_ta(tmem_base + o_col(t), tmem_base + s_col(t) + 8 * kk,
+                               vdesc + kk * (2048 >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
             };
-            // scores run NSB tiles ahead: S(0 .. NSB-1), then P V(j) followed by S(j + NSB),
-            // which reuses the buffer P V(j) has just read (the tensor pipe keeps issue order)
-            for (int j = 0; j < NSB && j < nkv && ok; ++j) ok = issue_s(j);
-            for (int j = 0; j < nkv && ok; ++j) {
-                if (!issue_pv(j)) {
-                    ok = false;
-                    break;
+            // S_0(0), S_1(0); then per key tile j two blocks, each behind its waits: P V of query
+            // tile 0 with its scores for key tile j + 1, then the same for query tile 1.  The
+            // tensor pipe's queue is short: a thread issuing into a full queue stalls until it
+            // drains, and every wait, fence and commit that follows leaves the pipe idle, so the
+            // blocks are as few and as long as the dependencies allow.  The scores S_t(j + 1)
+            // overwrite the P that P V has just read: the tensor pipe executes one thread's MMAs
+            // in issue order.
+            if (nkv > 0) {
+                ok = ok && mbar_wait_warp(k_full(0), 0, timeout_ns);
+                if (ok && elect_one()) {
+                    mma_s(0, 0);
+                    tc_commit(s_full(0));
+                    mma_s(1, 0);
+                    tc_commit(s_full(1));
+                    tc_commit(k_empty(0));
                 }
-                if (j + NSB < nkv && !issue_s(j + NSB)) ok = false;
+                __syncwarp();
             }
-            if (!ok) atomicOr(err, ERR_MMA);
-            tc_commit(drain_bar);
+            for (int j = 0; j < nkv && ok; ++j) {
+                const bool next = j + 1 < nkv;
+                const int kn = (j + 1) % K_STAGES;
+                // the three barriers are tested at once (their latencies overlap); only when one
+                // is not ready does the warp wait on each in turn
+                const uint32_t vb = v_full(j % V_STAGES), vp = (j / V_STAGES) & 1;
+                const uint32_t kb = k_full(kn), kp = ((j + 1) / K_STAGES) & 1;
+                const bool r_v = mbar_try_wait(vb, vp);
+                const bool r_p = mbar_try_wait(p_full(0), j & 1);
+                const bool r_k = !next || mbar_try_wait(kb, kp);
+                if (!__all_sync(0xFFFFFFFFu, r_v && r_p && r_k))
+                    ok = mbar_wait_warp(vb, vp, timeout_ns) &&
+                         mbar_wait_warp(p_full(0), j & 1, timeout_ns) &&
+                         (!next || mbar_wait_warp(kb, kp, timeout_ns));
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    mma_pv(0, j);
+                    if (next) {
+                        mma_s(0, j + 1);
+                        tc_commit(s_full(0));
+                    } else {
+                        tc_commit(o_done(0));
+                    }
+                }
+                __syncwarp();
+                ok = mbar_wait_warp(p_full(1), j & 1, timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    mma_pv(1, j);
+                    tc_commit(v_empty(j % V_STAGES));
+                    if (next) {
+                        mma_s(1, j + 1);
+                        tc_commit(s_full(1));
+                        tc_commit(k_empty(kn));
+                    } else {
+                        tc_commit(o_done(1));
+                    }
+                }
+                __syncwarp();
+            }
+            if (elect_one()) {
+                if (!ok) atomicOr(err, ERR_MMA);
+                tc_commit(drain_bar);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        regs_claim<208>();
         // ------------------------------------------------------- softmax and epilogue
-        const uint32_t q = warp & 3;                          // TMEM lane quarter
-        const uint32_t lq = (q * 32) << 16;                   // lane field of this warp's rows
-        const int row = q0 + static_cast<int>(q * 32 + lane);
+        const int t = static_cast<int>(warp - SOFTMAX_WARP0) >> 2;   // query tile
+        const uint32_t q = warp & 3;                                  // TMEM lane quarter
+        const uint32_t lq = (q * 32) << 16;                           // lane field of these rows
+        const int row = q0 + t * BQ + static_cast<int>(q * 32 + lane);
+        const uint32_t scol = tmem_base + lq + s_col(t);
+        const uint32_t ocol = tmem_base + lq + o_col(t);
         float m_used = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            const int b = j % NSB;
-            if (!mbar_wait(s_full(b), (j / NSB) & 1, timeout_ns)) {
+            if (!mbar_wait(s_full(t), j & 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t v[BKV];
-            const uint32_t scol = tmem_base + lq + S_COL0 + 128 * b;
-#pragma unroll
-            for (int ch = 0; ch < BKV / 32; ++ch)
-                tmem_ld_32x32b_x32(scol + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
-            tmem_wait_ld();
             const int valid = Lk - j * BKV;                   // keys of this tile inside Lk
             const bool full = valid >= BKV;
-            const float mx2 = (full ? tile_max<false>(v, valid) : tile_max<true>(v, valid)) * c_log2;
-            // raise the running maximum only when this tile exceeds it by more than 2^8
+            // the whole row of scores in registers: one TMEM round trip per tile
+            uint32_t v[128];
+            tmem_ld_32x32b_x32(scol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_32x32b_x32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+            tmem_ld_32x32b_x32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+            tmem_wait_ld();
+            const uint32_t(&v0)[64] = *reinterpret_cast<const uint32_t(*)[64]>(&v[0]);
+            const uint32_t(&v1)[64] = *reinterpret_cast<const uint32_t(*)[64]>(&v[64]);
+            // P of keys 0 .. 63 under the running maximum as it stands, computed while the tile's
+            // maximum is taken (the exponentials are bound by the MUFU pipe, the maximum fills
+            // issue slots beside them): the maximum is off the path to the first P V
+            uint32_t pk[32];
+            float l0 = full ? exp_half<false>(v0, 0, valid, c_log2, m_used, pk)
+                            : exp_half<true>(v0, 0, valid, c_log2, m_used, pk);
+            const float mx = full ? fmaxf(half_max<false>(v0, 0, valid), half_max<false>(v1, 64, valid))
+                                  : fmaxf(half_max<true>(v0, 0, valid), half_max<true>(v1, 64, valid));
+            const float mx2 = mx * c_log2;
+            // the running maximum is raised only when this tile exceeds it by more than 8 (log2
+            // units; always on the first tile): then O_t and l are rescaled and P recomputed
             const bool need = mx2 > m_used + 8.0f;
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = fmaxf(m_used, mx2);
                 if (j > 0) {
-                    // the previous P V must have completed before O is rescaled
-                    if (!mbar_wait(pv_done((j - 1) % NSB), ((j - 1) / NSB) & 1, timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    // P V of key tile j - 1 has completed: the commit behind s_full covers it
                     const float alpha = ex2_approx(m_used - m_new);
-                    const uint32_t ocol = tmem_base + lq + O_COL;
 #pragma unroll 1
                     for (int ch = 0; ch < HD / 32; ++ch) {
                         uint32_t o[32];
@@ -340,24 +408,29 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     l *= alpha;
                 }
                 m_used = m_new;
+                l0 = full ? exp_half<false>(v0, 0, valid, c_log2, m_used, pk)
+                          : exp_half<true>(v0, 0, valid, c_log2, m_used, pk);
             }
-            l += full ? softmax_tile<false>(v, valid, c_log2, m_used, scol)
-                      : softmax_tile<true>(v, valid, c_log2, m_used, scol);
+            // P over the scores: keys 0 .. 63 into columns 0 .. 31, keys 64 .. 127 into columns
+            // 32 .. 63
+            l += l0;
+            tmem_st_32x32b_x32(scol, pk);
+            l += full ? exp_half<false>(v1, 64, valid, c_log2, m_used, pk)
+                      : exp_half<true>(v1, 64, valid, c_log2, m_used, pk);
+            tmem_st_32x32b_x32(scol + 32, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(b));
+            if (lane == 0) mbar_arrive(p_full(t));
         }
         if (!ok) {
             if (lane == 0) atomicOr(err, ERR_EPILOGUE);
         } else if (nkv > 0) {
-            const int last = nkv - 1;
-            if (!mbar_wait(pv_done(last % NSB), (last / NSB) & 1, timeout_ns)) {
+            if (!mbar_wait(o_done(t), 0, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
             } else {
                 tc_fence_after();
                 const float inv = 1.0f / l;
-                const uint32_t ocol = tmem_base + lq + O_COL;
                 __half *orow = O + static_cast<int64_t>(head) * o_hs + static_cast<int64_t>(row) * o_rs;
 #pragma unroll 1
                 for (int ch = 0; ch < HD / 32; ++ch) {
@@ -409,7 +482,8 @@ cudaError_t launch_attention(const AttnArgs &a, const LaunchCtx &ctx, bool *enco
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const float c_log2 = a.scale * 1.4426950408889634f;
-    const dim3 grid(static_cast<unsigned>((a.Lq + BQ - 1) / BQ), static_cast<unsigned>(a.BH));
+    const dim3 grid(static_cast<unsigned>((a.Lq + QT * BQ - 1) / (QT * BQ)),
+                    static_cast<unsigned>(a.BH));
     attention_kernel<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(tmQ, tmK, tmV, a.O, a.o_hs, a.o_rs,
                                                                 a.Lq, a.Lk, c_log2, ctx.err,
                                                                 ctx.timeout_ns);

@@ -186,7 +186,7 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
-            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
+            if (!mbar_wait_sleep(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns, 128)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
@@ -406,7 +406,7 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             work.item(it, tile, half);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
-            if (!mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns)) {
+            if (!mbar_wait_sleep(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns, 128)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }

@@ -391,7 +391,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int mb, nb;
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it % G::ACC_BUFS;
-            if (!mbar_wait(tmem_full(ab), (acc_it / G::ACC_BUFS) & 1, timeout_ns)) {
+            if (!mbar_wait_sleep(tmem_full(ab), (acc_it / G::ACC_BUFS) & 1, timeout_ns, 128)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }

@@ -306,9 +306,11 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (rank == 0 && lane == 0) {
+        if (rank == 0) {
             // --------------------------------------------------------- MMA issuer
-            // descriptors of stage 0; stage s adds s * bytes / 16 to the start-address field
+            // The whole warp runs the loop and waits; one elected lane issues.  (A loop run by
+            // one lane alone issues measurably slower: the tensor pipe idles between stages.)
+            // Descriptors of stage 0; stage s adds s * bytes / 16 to the start-address field.
             const uint64_t adesc0 = smem_desc(sb + OFF_A, 16, 1024, SWZ_128B);
             const uint64_t bdesc0 = smem_desc(sb + OFF_B, 16, 1024, SWZ_128B);
             uint32_t acc_phase = 0, stage = 0, phase = 0;
@@ -320,13 +322,14 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t idesc = half < 0 ? F::IDESC
                                                 : (F::IDESC & ~(0x3Fu << 17)) |
                                                       (static_cast<uint32_t>((BN / 2) >> 3) << 17);
-                if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -334,27 +337,34 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
                     const uint64_t adesc = adesc0 + stage * (A_BYTES >> 4);
                     const uint64_t bdesc = bdesc0 + stage * (B_BYTES >> 4);
-                    // MMA j: 32 bytes of K at byte 32 j; its first k-block is j W, i.e. byte
-                    // (j W) % 4 of scale word (j W) / 4 (SFA word w at +4 w, SFB at +4 W + 8 w)
+                    if (elect_one()) {
+                        // MMA j: 32 bytes of K at byte 32 j; its first k-block is j W, i.e.
+                        // byte (j W) % 4 of scale word (j W) / 4 (SFA word w at +4 w, SFB at
+                        // +4 W + 8 w)
 #pragma unroll
-                    for (uint32_t j = 0; j < BK / 32; ++j) {
-                        const uint32_t blk = j * W, w = blk >> 2, id = blk & 3;
-                        F::mma(tmem_base, adesc + 2 * j, bdesc + 2 * j,
-                               idesc | (id << 4) | (id << 29), sf_col + 4 * w,
-                               sf_col + 4 * W + 8 * w, (kt > 0 || j > 0) ? 1u : 0u);
+                        for (uint32_t j = 0; j < BK / 32; ++j) {
+                            const uint32_t blk = j * W, w = blk >> 2, id = blk & 3;
+                            F::mma(tmem_base, adesc + 2 * j, bdesc + 2 * j,
+                                   idesc | (id << 4) | (id << 29), sf_col + 4 * w,
+                                   sf_col + 4 * W + 8 * w, (kt > 0 || j > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair(empty_bar(stage), 3);
                     }
-                    tc_commit_pair(empty_bar(stage), 3);
+                    __syncwarp();
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit_pair(tmem_full, 3);
+                if (elect_one()) tc_commit_pair(tmem_full, 3);
+                __syncwarp();
                 acc_phase ^= 1;
             }
-            if (!ok) atomicOr(err, ERR_MMA);
-            tc_commit_pair(drain_bar, 3);
+            if (elect_one()) {
+                if (!ok) atomicOr(err, ERR_MMA);
+                tc_commit_pair(drain_bar, 3);
+            }
         }
         __syncwarp();
         // both CTAs: every pair MMA writing this CTA's TMEM has completed before it is freed
@@ -404,7 +414,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int tile, thalf, mb, nb;
             work.item(it, tile, thalf);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+            if (!mbar_wait_sleep(tmem_full, acc_phase, timeout_ns, 128)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }

@@ -28,6 +28,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// True in exactly one active lane of the warp (the lowest); executed by the whole warp.  Code
+// that a warp runs in step and issues from one elected lane keeps its warp-uniform values (MMA
+// descriptors, addresses) in the uniform datapath.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
@@ -44,6 +57,21 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // visible (returns at once when the grid was launched without that dependency).
 __device__ __forceinline__ void griddep_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- register reallocation
+// Every warp of a warpgroup executes the same one.  A warpgroup that raises its count takes
+// registers the others have released; the counts of all warpgroups must add up to no more than
+// the block was launched with (threads x the kernel's registers per thread), or the raise waits.
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_claim() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------------------- mbarrier
@@ -130,6 +158,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
+}
+
+// As mbar_wait, for a warp that waits long and is not on the critical path (an epilogue
+// waiting for a whole tile's accumulation): between tests it sleeps about sleep_ns.  Threads
+// polling a barrier without pause slow every other mbarrier operation of the SM, the MMA
+// issuer's and the TMA producer's included.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// mbar_wait by every lane of a warp, with one outcome for all of them.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, timeout_ns));
 }
 
 // As mbar_wait, with cluster-scope acquire: for barriers that receive arrivals from the peer CTA
@@ -491,7 +540,6 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Each thread of the warp reads its TMEM lane, 32 consecutive 32-bit columns.
 // Each thread of the warp reads its TMEM lane, 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(

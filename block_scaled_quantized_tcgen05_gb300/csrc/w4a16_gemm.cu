@@ -272,7 +272,7 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             if (acc_mode)
                 mark_outlier_cols(flags, static_cast<int>(threadIdx.x) - 64, nb * BN, N, K, W, ldw,
                                   SW, ldsw);
-            bool got = mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns);
+            bool got = mbar_wait_sleep(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns, 128);
             if (acc_mode) got = epi_bar_and(got);
             if (!got) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
@@ -575,7 +575,7 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (acc_mode)
                 mark_outlier_cols(flags, static_cast<int>(threadIdx.x) - 64, nb * BN, N, K, W, ldw,
                                   SW, ldsw);
-            bool got = mbar_wait(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns);
+            bool got = mbar_wait_sleep(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns, 128);
             if (acc_mode) got = epi_bar_and(got);
             if (!got) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);

@@ -193,41 +193,50 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (rank == 0 && lane == 0) {
+        if (rank == 0) {
             // --------------------------------------------------------- MMA issuer
+            // The whole warp runs the loop and waits; one elected lane issues (a loop run by one
+            // lane alone issues measurably slower, more so beside the converter warps' ALU work).
             const uint64_t bdesc0 = smem_desc(sb + OFF_X, 16, 1024, SWZ_128B);
             uint32_t acc_phase = 0, stage = 0, phase = 0;
             bool ok = true;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns)) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                    if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_col = tmem_base + A_COL0 + stage * A_COLS;
                     const uint64_t bdesc = bdesc0 + stage * (X_BYTES >> 4);
-                    mma_f16_pair_ta(tmem_base, a_col, bdesc, IDESC, kt > 0 ? 1u : 0u);
+                    if (elect_one()) {
+                        mma_f16_pair_ta(tmem_base, a_col, bdesc, IDESC, kt > 0 ? 1u : 0u);
 #pragma unroll
-                    for (uint32_t j = 1; j < BK / 16; ++j)
-                        mma_f16_pair_ta(tmem_base, a_col + 8 * j, bdesc + 2 * j, IDESC, 1u);
-                    tc_commit_pair(empty_bar(stage), 3);
+                        for (uint32_t j = 1; j < BK / 16; ++j)
+                            mma_f16_pair_ta(tmem_base, a_col + 8 * j, bdesc + 2 * j, IDESC, 1u);
+                        tc_commit_pair(empty_bar(stage), 3);
+                    }
+                    __syncwarp();
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit_pair(tmem_full, 3);
+                if (elect_one()) tc_commit_pair(tmem_full, 3);
+                __syncwarp();
                 acc_phase ^= 1;
             }
-            if (!ok) atomicOr(err, ERR_MMA);
-            tc_commit_pair(drain_bar, 3);
+            if (elect_one()) {
+                if (!ok) atomicOr(err, ERR_MMA);
+                tc_commit_pair(drain_bar, 3);
+            }
         }
         __syncwarp();
         // both CTAs: every pair MMA writing this CTA's TMEM has completed before it is freed
@@ -371,7 +380,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     skip = w4_row_is_outlier(scales + static_cast<int64_t>(n) * lds,
                                              wdata + static_cast<int64_t>(n) * ldw, K / 32);
             }
-            if (!mbar_wait(tmem_full, acc_phase, timeout_ns)) {
+            if (!mbar_wait_sleep(tmem_full, acc_phase, timeout_ns, 128)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
