@@ -254,7 +254,8 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0) {
+        // The whole warp runs the loop and waits; one elected lane issues the copies.
+        {
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
@@ -273,22 +274,25 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t b_bytes = half < 0 ? B_BYTES : B_BYTES / 2;
                 const uint32_t sfb_bytes = half < 0 ? SFB_BYTES : SFB_BYTES / 2;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_BYTES + b_bytes));
-                    tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
-                    tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, half < 0 ? &tmB : &tmB64,
-                                          lead_full, kt * BK, nh, keep);
-                    mbar_arrive_expect_tx(sf_full(stage), SFA_BYTES + sfb_bytes);
-                    bulk_load(sb + OFF_SFA + stage * SFA_BYTES,
-                              packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W,
-                              SFA_BYTES, sf_full(stage));
-                    bulk_load(sb + OFF_SFB + stage * SFB_BYTES,
-                              packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W,
-                              sfb_bytes, sf_full(stage));
+                    if (elect_one()) {
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_BYTES + b_bytes));
+                        tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
+                        tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, half < 0 ? &tmB : &tmB64,
+                                              lead_full, kt * BK, nh, keep);
+                        mbar_arrive_expect_tx(sf_full(stage), SFA_BYTES + sfb_bytes);
+                        bulk_load(sb + OFF_SFA + stage * SFA_BYTES,
+                                  packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W,
+                                  SFA_BYTES, sf_full(stage));
+                        bulk_load(sb + OFF_SFB + stage * SFB_BYTES,
+                                  packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W,
+                                  sfb_bytes, sf_full(stage));
+                    }
+                    __syncwarp();
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -296,11 +300,12 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             }
-            if (!ok) atomicOr(err, ERR_PRODUCER);
+            if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
             if (rank == 0)   // the leader's full barriers count both CTAs' loads
                 for (int i = max(0, issued - STAGES); i < issued; ++i)
-                    if (!mbar_wait_cluster(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
-                        atomicOr(err, ERR_DRAIN);
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(full_bar(i % STAGES),
+                                                                   (i / STAGES) & 1, timeout_ns))) {
+                        if (lane == 0) atomicOr(err, ERR_DRAIN);
                         break;
                     }
         }

@@ -151,7 +151,8 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0) {
+        // The whole warp runs the loop and waits; one elected lane issues the copies.
+        {
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
@@ -161,16 +162,20 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const int w0 = wb * 2 * BW + static_cast<int>(rank) * BW;     // this CTA's weights
                 const int t0 = tb * BT + static_cast<int>(rank) * (BT / 2);   // this CTA's tokens
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
-                    tma_load_2d_pair(sb + OFF_X + stage * X_BYTES, &tmX, lead_full, kt * BK, t0);
-                    mbar_arrive_expect_tx(raw_full(stage), RAW_BYTES);
-                    tma_load_2d(sb + OFF_RAW + stage * RAW_BYTES, &tmW, raw_full(stage),
-                                kt * (BK / 2), w0);
+                    if (elect_one()) {
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+                        tma_load_2d_pair(sb + OFF_X + stage * X_BYTES, &tmX, lead_full, kt * BK,
+                                         t0);
+                        mbar_arrive_expect_tx(raw_full(stage), RAW_BYTES);
+                        tma_load_2d(sb + OFF_RAW + stage * RAW_BYTES, &tmW, raw_full(stage),
+                                    kt * (BK / 2), w0);
+                    }
+                    __syncwarp();
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -178,15 +183,14 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     }
                 }
             }
-            if (!ok) atomicOr(err, ERR_PRODUCER);
+            if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
             for (int i = max(0, issued - STAGES); i < issued; ++i) {
-                if (!mbar_wait(raw_full(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
-                    atomicOr(err, ERR_DRAIN);
-                    break;
-                }
-                if (rank == 0 &&
-                    !mbar_wait_cluster(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns)) {
-                    atomicOr(err, ERR_DRAIN);
+                const bool drained =
+                    mbar_wait(raw_full(i % STAGES), (i / STAGES) & 1, timeout_ns) &&
+                    (rank != 0 ||
+                     mbar_wait_cluster(full_bar(i % STAGES), (i / STAGES) & 1, timeout_ns));
+                if (!__all_sync(0xFFFFFFFFu, drained)) {
+                    if (lane == 0) atomicOr(err, ERR_DRAIN);
                     break;
                 }
             }
