@@ -312,7 +312,8 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const uint32_t tmem_base = *slot;
 
     if (warp == 0) {
-        if (lane == 0) {
+        // producer: the whole warp runs the loop and waits; one elected lane issues the copies
+        {
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
@@ -326,17 +327,21 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                                         : nb * P_BN + half * (P_BN / 2) + static_cast<int>(rank) * 64;
                 const uint32_t tx = 2 * (P_A_BYTES + (half < 0 ? P_B_BYTES : P_B_ATOM));
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
-                    const uint32_t sA = sb + P_OFF_A + stage * P_A_BYTES;
-                    const uint32_t sB = sb + P_OFF_B + stage * P_B_BYTES;
-                    tma_load_2d_pair(sA, &tmA, lead_full, kt * P_BK, m0);
-                    tma_load_2d_pair(sB, &tmB, lead_full, nh, kt * P_BK);
-                    if (half < 0) tma_load_2d_pair(sB + P_B_ATOM, &tmB, lead_full, nh + 64, kt * P_BK);
+                    if (elect_one()) {
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
+                        const uint32_t sA = sb + P_OFF_A + stage * P_A_BYTES;
+                        const uint32_t sB = sb + P_OFF_B + stage * P_B_BYTES;
+                        tma_load_2d_pair(sA, &tmA, lead_full, kt * P_BK, m0);
+                        tma_load_2d_pair(sB, &tmB, lead_full, nh, kt * P_BK);
+                        if (half < 0)
+                            tma_load_2d_pair(sB + P_B_ATOM, &tmB, lead_full, nh + 64, kt * P_BK);
+                    }
+                    __syncwarp();
                     ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -344,14 +349,17 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 }
             }
-            if (!ok) atomicOr(err, ERR_PRODUCER);
+            if (!ok && lane == 0) atomicOr(err, ERR_PRODUCER);
             if (rank == 0)   // the leader's full barriers count both CTAs' bytes
                 for (int i = max(0, issued - P_STAGES); i < issued; ++i)
-                    if (!mbar_wait_cluster(full_bar(i % P_STAGES), (i / P_STAGES) & 1, timeout_ns)) {
-                        atomicOr(err, ERR_DRAIN);
+                    if (!__all_sync(0xFFFFFFFFu,
+                                    mbar_wait_cluster(full_bar(i % P_STAGES), (i / P_STAGES) & 1,
+                                                      timeout_ns))) {
+                        if (lane == 0) atomicOr(err, ERR_DRAIN);
                         break;
                     }
         }
+        __syncwarp();
     } else if (warp == 1) {
         if (rank == 0) {
             uint32_t stage = 0, phase = 0, acc_it = 0;
