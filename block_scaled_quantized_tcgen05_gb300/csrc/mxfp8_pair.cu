@@ -21,10 +21,10 @@
 //     stream would sit in the tensor pipe's in-order queue in front of the MMAs; written from
 //     registers, the scales never enter that queue.
 //
-// Hand-off: only the leader (rank 0) issues MMAs, from one thread.  The tensor pipe's queue of
-// issued MMAs is shallow (a back-to-back stream of pair MMAs is accepted at exactly the rate they
-// execute, 128 cycles each), so that thread's loop does one CTA-scope barrier wait per stage and
-// nothing else but the four MMAs and a commit.  Each stage's full barrier lives in the leader and
+// Hand-off: only the leader (rank 0) issues MMAs; its MMA warp runs the loop and the barrier
+// waits together and one elected lane issues (a loop run by one thread alone issues each MMA in
+// tens of cycles and leaves the tensor pipe idle between stages).  The loop does one CTA-scope
+// barrier wait per stage and nothing else but the four MMAs and a commit.  Each stage's full barrier lives in the leader and
 // collects everything the stage needs: the leader's arrival with both CTAs' data bytes, both
 // CTAs' data loads, and one arrival from each scale warp of both CTAs once its tcgen05.st have
 // completed (tcgen05.wait::st; the arrival itself is relaxed -- a release at cluster scope costs
@@ -106,8 +106,6 @@ struct Smem {
     static constexpr int STAGES = F::STAGES;
     static constexpr uint32_t SFA_BYTES = 512 * F::W;         // 128 rows x 4 W bytes
     static constexpr uint32_t SFB_BYTES = 1024 * F::W;        // 256 rows x 4 W bytes
-    static constexpr uint32_t STAGE_TX = 2 * (A_BYTES + B_BYTES);   // both CTAs' data, on the leader
-    static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;        // this CTA's scales, locally
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -419,7 +417,7 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int tile, thalf, mb, nb;
             work.item(it, tile, thalf);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            if (!mbar_wait_sleep(tmem_full, acc_phase, timeout_ns, 128)) {
+            if (!mbar_wait_sleep(tmem_full, acc_phase, timeout_ns, 32)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
                 break;
             }
