@@ -137,18 +137,32 @@ __device__ __forceinline__ float half_max(const uint32_t (&v)[64], int k0, int v
                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
+// Partial rows a half of a split unit leaves for attention_merge_kernel: the unnormalised O of
+// its 256 rows (fp32, row-major), then their running maxima m (log2 units), then their sums l.
+constexpr int UNIT_ROWS = QT * BQ;
+constexpr size_t WS_FLOATS_PER_HALF = static_cast<size_t>(UNIT_ROWS) * (HD + 2);
+
 __global__ void __launch_bounds__(THREADS, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, __half *__restrict__ O, int64_t o_hs,
-                 int64_t o_rs, int Lq, int Lk, float c_log2, unsigned *err, uint64_t timeout_ns) {
+                 int64_t o_rs, int Lq, int Lk, float c_log2, int nqb, int n_direct, int kv_split,
+                 float *__restrict__ ws, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
-    const int head = blockIdx.y;
-    const int q0 = blockIdx.x * (QT * BQ);
-    const int nkv = (Lk + BKV - 1) / BKV;
+    // A unit is (head, 256 query rows).  CTAs below n_direct take one unit over all its key
+    // tiles; the rest come in pairs that split one unit's key tiles at kv_split (the last wave of
+    // a grid that would leave SMs idle) and leave their partial rows in ws.
+    const int nkv_all = (Lk + BKV - 1) / BKV;
+    const int s_idx = static_cast<int>(blockIdx.x) - n_direct;   // >= 0: a half of a split unit
+    const int unit = s_idx < 0 ? static_cast<int>(blockIdx.x) : n_direct + (s_idx >> 1);
+    const int kv_half = s_idx < 0 ? -1 : (s_idx & 1);
+    const int head = unit / nqb;
+    const int q0 = (unit - head * nqb) * UNIT_ROWS;
+    const int kv0 = kv_half == 1 ? kv_split : 0;                 // first key tile of this CTA
+    const int nkv = kv_half < 0 ? nkv_all : (kv_half == 0 ? kv_split : nkv_all - kv_split);
 
     const uint32_t q_full = sb + OFF_BAR;
     auto k_full = [&](int s) { return sb + OFF_BAR + 8u * (1 + s); };
@@ -216,8 +230,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     }
                     const uint32_t sk = sb + OFF_K + st * TILE_BYTES;
                     mbar_arrive_expect_tx(k_full(st), TILE_BYTES);
-                    tma_load_3d(sk, &tmK, k_full(st), 0, j * BKV, head);
-                    tma_load_3d(sk + HALF_BYTES, &tmK, k_full(st), 64, j * BKV, head);
+                    tma_load_3d(sk, &tmK, k_full(st), 0, (kv0 + j) * BKV, head);
+                    tma_load_3d(sk + HALF_BYTES, &tmK, k_full(st), 64, (kv0 + j) * BKV, head);
                     ++issued;
                 }
                 if (!ok) atomicOr(err, ERR_PRODUCER);
@@ -241,8 +255,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     }
                     const uint32_t sv = sb + OFF_V + st * TILE_BYTES;
                     mbar_arrive_expect_tx(v_full(st), TILE_BYTES);
-                    tma_load_3d(sv, &tmV, v_full(st), 0, j * BKV, head);
-                    tma_load_3d(sv + HALF_BYTES, &tmV, v_full(st), 64, j * BKV, head);
+                    tma_load_3d(sv, &tmV, v_full(st), 0, (kv0 + j) * BKV, head);
+                    tma_load_3d(sv + HALF_BYTES, &tmV, v_full(st), 64, (kv0 + j) * BKV, head);
                     ++issued;
                 }
                 if (!ok) atomicOr(err, ERR_PRODUCER);
@@ -366,7 +380,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 break;
             }
             tc_fence_after();
-            const int valid = Lk - j * BKV;                   // keys of this tile inside Lk
+            const int valid = Lk - (kv0 + j) * BKV;           // keys of this tile inside Lk
             const bool full = valid >= BKV;
             // the whole row of scores in registers: one TMEM round trip per tile
             uint32_t v[128];
@@ -428,6 +442,24 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         } else if (nkv > 0) {
             if (!mbar_wait(o_done(t), 0, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_EPILOGUE);
+            } else if (kv_half >= 0) {
+                // a half of a split unit: the row's unnormalised O, m and l for the merge
+                tc_fence_after();
+                float *wsb = ws + static_cast<size_t>(s_idx) * WS_FLOATS_PER_HALF;
+                const int r = t * BQ + static_cast<int>(q * 32 + lane);
+                float4 *dst = reinterpret_cast<float4 *>(wsb + static_cast<size_t>(r) * HD);
+#pragma unroll 1
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(ocol + 32 * ch, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[8 * ch + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+                }
+                wsb[static_cast<size_t>(UNIT_ROWS) * HD + r] = m_used;
+                wsb[static_cast<size_t>(UNIT_ROWS) * (HD + 1) + r] = l;
             } else {
                 tc_fence_after();
                 const float inv = 1.0f / l;
@@ -464,6 +496,35 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
 }
 
+// Rows of the split units: O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1) with a_h = 2^(m_h - max(m0, m1)),
+// the two halves' partial rows combined as the running-maximum recurrence combines key tiles.
+// One warp per row, four columns per lane.
+__global__ void __launch_bounds__(256)
+attention_merge_kernel(const float *__restrict__ ws, int n_direct, int n_split, int nqb,
+                       __half *__restrict__ O, int64_t o_hs, int64_t o_rs, int Lq) {
+    const int slot = static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int su = slot / UNIT_ROWS, r = slot - su * UNIT_ROWS;
+    if (su >= n_split) return;
+    const int unit = n_direct + su;
+    const int head = unit / nqb;
+    const int row = (unit - head * nqb) * UNIT_ROWS + r;
+    if (row >= Lq) return;
+    const float *w0 = ws + static_cast<size_t>(2 * su) * WS_FLOATS_PER_HALF;
+    const float *w1 = w0 + WS_FLOATS_PER_HALF;
+    const size_t im = static_cast<size_t>(UNIT_ROWS) * HD + r;
+    const size_t il = static_cast<size_t>(UNIT_ROWS) * (HD + 1) + r;
+    const float m = fmaxf(w0[im], w1[im]);
+    const float a0 = exp2f(w0[im] - m), a1 = exp2f(w1[im] - m);
+    const float inv = 1.0f / (a0 * w0[il] + a1 * w1[il]);
+    const float4 o0 = reinterpret_cast<const float4 *>(w0 + static_cast<size_t>(r) * HD)[lane];
+    const float4 o1 = reinterpret_cast<const float4 *>(w1 + static_cast<size_t>(r) * HD)[lane];
+    const uint32_t p0 = pack_f16x2((a0 * o0.x + a1 * o1.x) * inv, (a0 * o0.y + a1 * o1.y) * inv);
+    const uint32_t p1 = pack_f16x2((a0 * o0.z + a1 * o1.z) * inv, (a0 * o0.w + a1 * o1.w) * inv);
+    __half *dst = O + static_cast<int64_t>(head) * o_hs + static_cast<int64_t>(row) * o_rs + 4 * lane;
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(p0, p1);
+}
+
 }  // namespace
 
 namespace qgi {
@@ -482,12 +543,40 @@ cudaError_t launch_attention(const AttnArgs &a, const LaunchCtx &ctx, bool *enco
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const float c_log2 = a.scale * 1.4426950408889634f;
-    const dim3 grid(static_cast<unsigned>((a.Lq + QT * BQ - 1) / (QT * BQ)),
-                    static_cast<unsigned>(a.BH));
-    attention_kernel<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(tmQ, tmK, tmV, a.O, a.o_hs, a.o_rs,
-                                                                a.Lq, a.Lk, c_log2, ctx.err,
-                                                                ctx.timeout_ns);
-    return cudaGetLastError();
+    // Units (head, 256 query rows) fill whole waves of one CTA per SM; when the last wave would
+    // leave at least half the SMs idle, its units are split in two along the keys, a CTA each,
+    // and merged afterwards: that wave then takes half the time.
+    const int nqb = (a.Lq + UNIT_ROWS - 1) / UNIT_ROWS;
+    const int64_t units = static_cast<int64_t>(nqb) * a.BH;
+    const int nkv_all = (a.Lk + BKV - 1) / BKV;
+    const int64_t rem = ctx.num_sms > 0 ? units % ctx.num_sms : 0;
+    const int n_split =
+        (units > ctx.num_sms && rem > 0 && 2 * rem <= ctx.num_sms && nkv_all >= 4)
+            ? static_cast<int>(rem) : 0;
+    const int64_t n_direct = units - n_split;
+    if (n_direct + 2 * n_split > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    float *ws = nullptr;
+    if (n_split > 0) {
+        e = scratch_alloc(2 * n_split * WS_FLOATS_PER_HALF * sizeof(float), ctx,
+                          reinterpret_cast<void **>(&ws));
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned grid = static_cast<unsigned>(n_direct + 2 * n_split);
+    attention_kernel<<<grid, THREADS, SMEM_BYTES, ctx.stream>>>(
+        tmQ, tmK, tmV, a.O, a.o_hs, a.o_rs, a.Lq, a.Lk, c_log2, nqb, static_cast<int>(n_direct),
+        nkv_all / 2, ws, ctx.err, ctx.timeout_ns);
+    e = cudaGetLastError();
+    if (n_split > 0) {
+        if (e == cudaSuccess) {
+            const unsigned mgrid = static_cast<unsigned>((n_split * UNIT_ROWS + 7) / 8);
+            attention_merge_kernel<<<mgrid, 256, 0, ctx.stream>>>(
+                ws, static_cast<int>(n_direct), n_split, nqb, a.O, a.o_hs, a.o_rs, a.Lq);
+            e = cudaGetLastError();
+        }
+        const cudaError_t f = scratch_free(ws, ctx);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 }  // namespace qgi

@@ -88,6 +88,23 @@ def test_attention_interleaved_heads_layout(dev, orc):
     _check(Oi.transpose(0, 1), res, orc, "attention interleaved heads")
 
 
+def test_attention_split_last_wave(dev, orc):
+    """A grid whose last wave would leave more than half the SMs idle: its units (head, 256
+    query rows) are computed as two halves of their key tiles and merged.  The head count is
+    chosen from the SM count so that 4 BH units exceed one wave by a few; Lk = 600 puts the
+    ragged key tile in the second half."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    BH, Lq, Lk = (sms + 1 + 3) // 4 + 1, 1024, 600
+    units = BH * ((Lq + 255) // 256)
+    assert units > sms and 0 < 2 * (units - sms) <= sms      # the split path is taken
+    d = synth.attention_inputs(BH, Lq, Lk, 128, seed=74, q_std=2.0)
+    O = _run(d, dev)
+    res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"])
+    _check(O, res, orc, f"attention split last wave {BH}x{Lq}x{Lk}")
+    O2 = _run(d, dev)
+    assert torch.equal(O2.view(torch.int16), O.view(torch.int16))     # repeatable bit for bit
+
+
 def test_attention_errors(dev):
     x = torch.zeros(1, 16, 64, dtype=torch.float16, device=dev)
     with pytest.raises(q.QGemmError) as ei:
