@@ -277,25 +277,24 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             // the second 64 of d is the other span (leading offset), the next 8 keys 1024 bytes
             // on (stride offset).
             const uint64_t vdesc0 = smem_desc(sb + OFF_V, HALF_BYTES, 1024, SWZ_128B);
-            auto mma_s = [&](int t, int j) {   // S_t = Q_t K_j^T
-                const uint64_t qdesc = qdesc0 + static_cast<uint64_t>(t) * (TILE_BYTES >> 4);
-                const uint64_t kdesc =
-                    kdesc0 + static_cast<uint64_t>(j % K_STAGES) * (TILE_BYTES >> 4);
+            // The descriptors and TMEM addresses are formed by the whole warp, outside the
+            // issuing branch: formed inside it, measured, each MMA issues much more slowly.
+            const uint64_t qdesc[QT] = {qdesc0, qdesc0 + (TILE_BYTES >> 4)};
+            const uint32_t scol_t[QT] = {tmem_base + s_col(0), tmem_base + s_col(1)};
+            const uint32_t ocol_t[QT] = {tmem_base + o_col(0), tmem_base + o_col(1)};
+            auto mma_s = [&](int t, uint64_t kdesc) {   // S_t = Q_t K^T
 #pragma unroll
                 for (uint32_t kk = 0; kk < HD / 16; ++kk) {
                     // 16 of d per MMA: span kk / 4 (64 halves each), 32 bytes kk % 4 into it
                     const uint64_t off = (kk >> 2) * (HALF_BYTES >> 4) + 2 * (kk & 3);
-                    mma_f16(tmem_base + s_col(t), qdesc + off, kdesc + off, IDESC_S,
-                            kk > 0 ? 1u : 0u);
+                    mma_f16(scol_t[t], qdesc[t] + off, kdesc + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            auto mma_pv = [&](int t, int j) {   // O_t += P_t V_j, P_t in S_t's first 64 columns
-                const uint64_t vdesc =
-                    vdesc0 + static_cast<uint64_t>(j % V_STAGES) * (TILE_BYTES >> 4);
+            auto mma_pv = [&](int t, uint64_t vdesc, bool acc) {   // O_t (+)= P_t V, P_t in S_t
 #pragma unroll
                 for (uint32_t kk = 0; kk < BKV / 16; ++kk)   // keys 16 kk ..: P columns 8 kk ..
-                    mma_f16_ta(tmem_base + o_col(t), tmem_base + s_col(t) + 8 * kk,
-                               vdesc + kk * (2048 >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ta(ocol_t[t], scol_t[t] + 8 * kk, vdesc + kk * (2048 >> 4), IDESC_PV,
+                               (acc || kk > 0) ? 1u : 0u);
             };
             // S_0(0), S_1(0); then per key tile j two blocks, each behind its waits: P V of query
             // tile 0 with its scores for key tile j + 1, then the same for query tile 1.  The
@@ -307,9 +306,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (nkv > 0) {
                 ok = ok && mbar_wait_warp(k_full(0), 0, timeout_ns);
                 if (ok && elect_one()) {
-                    mma_s(0, 0);
+                    mma_s(0, kdesc0);
                     tc_commit(s_full(0));
-                    mma_s(1, 0);
+                    mma_s(1, kdesc0);
                     tc_commit(s_full(1));
                     tc_commit(k_empty(0));
                 }
@@ -331,10 +330,13 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                          (!next || mbar_wait_warp(kb, kp, timeout_ns));
                 if (!ok) break;
                 tc_fence_after();
+                const int vs = j % V_STAGES;
+                const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(vs) * (TILE_BYTES >> 4);
+                const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(kn) * (TILE_BYTES >> 4);
                 if (elect_one()) {
-                    mma_pv(0, j);
+                    mma_pv(0, vdesc, j > 0);
                     if (next) {
-                        mma_s(0, j + 1);
+                        mma_s(0, kdesc);
                         tc_commit(s_full(0));
                     } else {
                         tc_commit(o_done(0));
@@ -345,10 +347,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 if (!ok) break;
                 tc_fence_after();
                 if (elect_one()) {
-                    mma_pv(1, j);
-                    tc_commit(v_empty(j % V_STAGES));
+                    mma_pv(1, vdesc, j > 0);
+                    tc_commit(v_empty(vs));
                     if (next) {
-                        mma_s(1, j + 1);
+                        mma_s(1, kdesc);
                         tc_commit(s_full(1));
                         tc_commit(k_empty(kn));
                     } else {

@@ -134,28 +134,30 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
         }
     } else if (warp == 1) {
+        // MMA issuer: the whole warp runs the loop and its waits, one elected lane issues, the
+        // descriptors computed outside the issuing branch (stage s adds s * bytes / 16 to the
+        // start-address field).  MN-major B: LBO = stride between 64-wide N atoms, SBO = 8 k-rows.
+        const uint64_t adesc0 = smem_desc(sb + G::OFF_A, 16, 1024, SWZ_128B);
+        const uint64_t bdesc0 = smem_desc(sb + G::OFF_B, G::B_ATOM_BYTES, 1024, SWZ_128B);
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         const uint32_t idesc = f16_idesc(BN);
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
-            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
+            if (!mbar_wait_warp(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t adesc =
-                        smem_desc(sb + G::OFF_A + stage * G::A_BYTES, 16, 1024, SWZ_128B);
-                    // MN-major B: LBO = stride between 64-wide N atoms, SBO = 8 k-rows.
-                    const uint64_t bdesc = smem_desc(sb + G::OFF_B + stage * G::B_BYTES,
-                                                     G::B_ATOM_BYTES, 1024, SWZ_128B);
+                const uint64_t adesc = adesc0 + stage * (G::A_BYTES >> 4);
+                const uint64_t bdesc = bdesc0 + stage * (G::B_BYTES >> 4);
+                if (elect_one()) {
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j) {
                         // A: 16 halves = 32 bytes along the swizzle row; B: 16 k-rows = 2 KB
@@ -171,12 +173,14 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full(ab));
+            if (elect_one()) tc_commit(tmem_full(ab));
             __syncwarp();
             ++acc_it;
         }
-        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
-        if (lane == 0) tc_commit(drain_bar);
+        if (elect_one()) {
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit(drain_bar);
+        }
         __syncwarp();
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
     } else {
@@ -362,6 +366,10 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         __syncwarp();
     } else if (warp == 1) {
         if (rank == 0) {
+            // MMA issuer: the whole warp runs the loop and its waits, one elected lane issues.
+            // Descriptors of stage 0; stage s adds s * bytes / 16 to the start-address field.
+            const uint64_t adesc0 = smem_desc(sb + P_OFF_A, 16, 1024, SWZ_128B);
+            const uint64_t bdesc0 = smem_desc(sb + P_OFF_B, P_B_ATOM, 1024, SWZ_128B);
             uint32_t stage = 0, phase = 0, acc_it = 0;
             bool ok = true;
             for (int it = pair; it < work.n_items && ok; it += npairs) {
@@ -369,20 +377,22 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 work.item(it, tile, half);
                 const uint32_t idesc = half < 0 ? P_IDESC : P_IDESC_HALF;
                 const uint32_t ab = acc_it & 1;
-                if (!mbar_wait_cluster(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(ab),
+                                                               ((acc_it >> 1) & 1) ^ 1, timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait_cluster(full_bar(stage), phase, timeout_ns)) {
+                    // CTA scope: the stage's bytes arrive on this barrier by TMA from both CTAs
+                    if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t adesc = smem_desc(sb + P_OFF_A + stage * P_A_BYTES, 16, 1024, SWZ_128B);
-                        const uint64_t bdesc = smem_desc(sb + P_OFF_B + stage * P_B_BYTES, P_B_ATOM, 1024, SWZ_128B);
+                    const uint64_t adesc = adesc0 + stage * (P_A_BYTES >> 4);
+                    const uint64_t bdesc = bdesc0 + stage * (P_B_BYTES >> 4);
+                    if (elect_one()) {
 #pragma unroll
                         for (uint32_t j = 0; j < P_BK / 16; ++j)
                             mma_f16_pair(tmem_base + ab * P_BN, adesc + 2 * j, bdesc + 128 * j, idesc,
@@ -396,12 +406,14 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) tc_commit_pair(tmem_full(ab), 3);
+                if (elect_one()) tc_commit_pair(tmem_full(ab), 3);
                 __syncwarp();
                 ++acc_it;
             }
-            if (!ok && lane == 0) atomicOr(err, ERR_MMA);
-            if (lane == 0) tc_commit_pair(drain_bar, 3);
+            if (elect_one()) {
+                if (!ok) atomicOr(err, ERR_MMA);
+                tc_commit_pair(drain_bar, 3);
+            }
             __syncwarp();
         }
         // both CTAs: every pair MMA writing this CTA's TMEM has completed

@@ -327,37 +327,40 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop and its waits, one elected lane issues; descriptors of
+        // stage 0 computed once, stage s adding s * bytes / 16 to the start-address field.
+        const uint64_t adesc0 = smem_desc(sb + G::OFF_A, 16, 1024, SWZ_128B);
+        const uint64_t bdesc0 = smem_desc(sb + G::OFF_B, 16, 1024, SWZ_128B);
+        const uint64_t sfa0 = smem_desc(sb + G::OFF_SFA, 0, 128, SWZ_NONE);
+        const uint64_t sfb0 = smem_desc(sb + G::OFF_SFB, 0, 128, SWZ_NONE);
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         const uint32_t idesc = mx_idesc(BN);
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const uint32_t ab = acc_it % G::ACC_BUFS;   // accumulator buffer of this tile
-            if (!mbar_wait(tmem_empty(ab), ((acc_it / G::ACC_BUFS) & 1) ^ 1, timeout_ns)) {
+            if (!mbar_wait_warp(tmem_empty(ab), ((acc_it / G::ACC_BUFS) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
+                const uint32_t sf_col = tmem_base + G::SF_COL0 + stage * SF_COLS_PER_STAGE;
+                const uint64_t sfa = sfa0 + stage * (G::SFA_BYTES >> 4);
+                const uint64_t sfb = sfb0 + stage * (G::SFB_BYTES >> 4);
+                const uint64_t adesc = adesc0 + stage * (G::A_BYTES >> 4);
+                const uint64_t bdesc = bdesc0 + stage * (G::B_BYTES >> 4);
+                if (elect_one()) {
                     if constexpr (SFM == SFM_CPASYNC)
                         fence_proxy_async_smem();  // cp.async (generic proxy) -> tcgen05.cp reads
-                    const uint32_t sf_col = tmem_base + G::SF_COL0 + stage * SF_COLS_PER_STAGE;
-                    const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
-                    const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
-                    tc_cp_32x128b_warpx4(sf_col, smem_desc(sSFA, 0, 128, SWZ_NONE));
+                    tc_cp_32x128b_warpx4(sf_col, sfa);
 #pragma unroll
                     for (int h = 0; h < G::SFB_GROUPS; ++h)
-                        tc_cp_32x128b_warpx4(sf_col + 4 + 4 * h,
-                                             smem_desc(sSFB + h * 512, 0, 128, SWZ_NONE));
-                    const uint64_t adesc =
-                        smem_desc(sb + G::OFF_A + stage * G::A_BYTES, 16, 1024, SWZ_128B);
-                    const uint64_t bdesc =
-                        smem_desc(sb + G::OFF_B + stage * G::B_BYTES, 16, 1024, SWZ_128B);
+                        tc_cp_32x128b_warpx4(sf_col + 4 + 4 * h, sfb + h * (512 >> 4));
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 32; ++j) {
                         // advance 32 bytes of K inside the 128-byte swizzle row
@@ -374,13 +377,16 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full(ab));
+            if (elect_one()) tc_commit(tmem_full(ab));
             __syncwarp();
             ++acc_it;
         }
-        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
-        // Drain: all MMAs and TMEM copies of this CTA have completed before TMEM is freed.
-        if (lane == 0) tc_commit(drain_bar);
+        // Drain: all MMAs and TMEM copies of this CTA have completed before TMEM is freed (the
+        // commit comes from the lane that issued them: elect.sync picks the lowest active lane).
+        if (elect_one()) {
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit(drain_bar);
+        }
         __syncwarp();
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
     } else {

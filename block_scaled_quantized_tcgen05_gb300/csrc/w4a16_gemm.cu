@@ -220,24 +220,28 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop and its waits, one elected lane issues; descriptors of
+        // stage 0 computed once, stage s adding s * bytes / 16 to the start-address field.
+        const uint64_t adesc0 = smem_desc(sb + OFF_A, 16, 1024, SWZ_128B);
+        const uint64_t bdesc0 = smem_desc(sb + OFF_B, 16, 1024, SWZ_128B);
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
-            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
+            if (!mbar_wait_warp(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(full_bar(stage), phase, timeout_ns)) {
+                if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t adesc = smem_desc(sb + OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
-                    const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
+                const uint64_t adesc = adesc0 + stage * (A_BYTES >> 4);
+                const uint64_t bdesc = bdesc0 + stage * (B_BYTES >> 4);
+                if (elect_one()) {
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j)
                         mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 2 * j, IDESC,
@@ -251,12 +255,14 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full(ab));
+            if (elect_one()) tc_commit(tmem_full(ab));
             __syncwarp();
             ++acc_it;
         }
-        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
-        if (lane == 0) tc_commit(drain_bar);
+        if (elect_one()) {
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit(drain_bar);
+        }
         __syncwarp();
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
     } else if (warp < 6) {
@@ -522,25 +528,29 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop and its waits, one elected lane issues; descriptors of
+        // stage 0 computed once, stage s adding s * bytes / 16 to the start-address field.
+        const uint64_t adesc0 = smem_desc(sb + OFF_A, 16, 1024, SWZ_128B);
+        const uint64_t bdesc0 = smem_desc(sb + OFF_B, 16, 1024, SWZ_128B);
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
-            if (!mbar_wait(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
+            if (!mbar_wait_warp(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(raw_full(stage), phase, timeout_ns) ||
-                    !mbar_wait(conv_full(stage), phase, timeout_ns)) {
+                if (!mbar_wait_warp(raw_full(stage), phase, timeout_ns) ||
+                    !mbar_wait_warp(conv_full(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t adesc = smem_desc(sb + OFF_A + stage * A_BYTES, 16, 1024, SWZ_128B);
-                    const uint64_t bdesc = smem_desc(sb + OFF_B + stage * B_BYTES, 16, 1024, SWZ_128B);
+                const uint64_t adesc = adesc0 + stage * (A_BYTES >> 4);
+                const uint64_t bdesc = bdesc0 + stage * (B_BYTES >> 4);
+                if (elect_one()) {
 #pragma unroll
                     for (uint32_t j = 0; j < BK / 16; ++j)
                         mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 2 * j, IDESC,
@@ -554,12 +564,14 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(tmem_full(ab));
+            if (elect_one()) tc_commit(tmem_full(ab));
             __syncwarp();
             ++acc_it;
         }
-        if (!ok && lane == 0) atomicOr(err, ERR_MMA);
-        if (lane == 0) tc_commit(drain_bar);
+        if (elect_one()) {
+            if (!ok) atomicOr(err, ERR_MMA);
+            tc_commit(drain_bar);
+        }
         __syncwarp();
         if (!mbar_wait(drain_bar, 0, timeout_ns) && lane == 0) atomicOr(err, ERR_DRAIN);
     } else if (warp < 6) {
