@@ -140,6 +140,7 @@ template <int W>
 __global__ void __launch_bounds__(256)
 sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     __shared__ __align__(16) uint8_t tile[128 * PACK_ROW];
+    griddep_launch_dependents();   // the GEMM, a programmatic dependent, may start its set-up
     const SfPackOperand &op = blockIdx.z == 0 ? opA : opB;
     const int rb = blockIdx.x;
     if (rb >= op.rbp) return;
@@ -252,7 +253,11 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        // The whole warp runs the loop and waits; one elected lane issues the copies.
+        // The whole warp runs the loop and waits; one elected lane issues the copies.  The
+        // kernel is launched as a programmatic dependent of the scale repack: its set-up above
+        // overlaps the repack, and the producer, the only role that reads the repacked scales
+        // from global memory (every other role waits on what it loads), waits for it here.
+        griddep_wait();
         {
             uint32_t stage = 0, phase = 0;
             int issued = 0;
@@ -512,10 +517,20 @@ cudaError_t launch_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __h
     int pairs = ctx.num_sms / 2;
     if (pairs > tiles) pairs = tiles;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
-    mx_pair_kernel<F><<<2 * pairs, THREADS, Smem<F>::BYTES, ctx.stream>>>(
-        tmA, tmB, tmB64, packA, packB, rbpA, rbpB, C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err,
-        ctx.timeout_ns);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel ahead on the stream (the scale repack): it starts
+    // once the repack's CTAs have all begun and waits for its results before reading them
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Smem<F>::BYTES;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];   // the cluster shape is the kernel's own (__cluster_dims__)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mx_pair_kernel<F>, tmA, tmB, tmB64, packA, packB, rbpA, rbpB,
+                              C, ldc, c_vec, M, N, Kb, ctx.epi, ctx.err, ctx.timeout_ns);
 }
 
 template <class F>
