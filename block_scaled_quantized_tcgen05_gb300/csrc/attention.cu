@@ -19,9 +19,10 @@
 //     operand straight from TMEM (the GB300 counterpart of passing the cooperative tensor as
 //     the left input); V is read from shared memory as an MN-major operand;
 //   * two softmax warpgroups, one per query tile, alternate with the tensor pipe: the MMA warp
-//     issues, per key tile, one block with P V for tile 0 and the next scores of tile 0, then one
-//     with P V for tile 1 and the next scores of tile 1, so while one warpgroup exponentiates its
-//     scores the tensor pipe works for the other.  The whole MMA warp runs the loop and one
+//     issues, per key tile, P V for tile 0 and the next scores of tile 0, then the same for tile
+//     1, so while one warpgroup exponentiates its scores the tensor pipe works for the other.
+//     The softmax releases P in two halves of 64 keys; P V of the first half runs while it
+//     exponentiates the second.  The whole MMA warp runs the loop and one
 //     elected lane issues (measured on GB300: a lone thread issues a tcgen05.mma in about 57
 //     cycles, an elected lane of a converged warp in about 14, and the pipe queues about 8 MMAs
 //     of 128 x 128 x 16 ahead); the waits before a block test their barriers together, so
@@ -66,9 +67,10 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + QT * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + K_STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + V_STAGES * TILE_BYTES;
-// q_full, k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[QT], p_full[QT], o_done[QT],
+// q_full, k_full[K], k_empty[K], v_full[V], v_empty[V], s_full[QT], p_full[QT][2] (keys 0..63,
+// 64..127), o_done[QT],
 // drain, then the TMEM slot
-constexpr int NBARS = 1 + 2 * K_STAGES + 2 * V_STAGES + 3 * QT + 1;
+constexpr int NBARS = 1 + 2 * K_STAGES + 2 * V_STAGES + 4 * QT + 1;
 constexpr uint32_t OFF_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_SLOT + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -171,9 +173,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     auto v_empty = [&](int s) { return sb + OFF_BAR + 8u * (1 + 2 * K_STAGES + V_STAGES + s); };
     constexpr int B0 = 1 + 2 * K_STAGES + 2 * V_STAGES;
     auto s_full = [&](int t) { return sb + OFF_BAR + 8u * (B0 + t); };
-    auto p_full = [&](int t) { return sb + OFF_BAR + 8u * (B0 + QT + t); };
-    auto o_done = [&](int t) { return sb + OFF_BAR + 8u * (B0 + 2 * QT + t); };
-    const uint32_t drain_bar = sb + OFF_BAR + 8u * (B0 + 3 * QT);
+    auto p_full = [&](int t, int h) { return sb + OFF_BAR + 8u * (B0 + QT + 2 * t + h); };
+    auto o_done = [&](int t) { return sb + OFF_BAR + 8u * (B0 + 3 * QT + t); };
+    const uint32_t drain_bar = sb + OFF_BAR + 8u * (B0 + 4 * QT);
     volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_SLOT);
 
     if (threadIdx.x == 0) {
@@ -188,7 +190,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         for (int t = 0; t < QT; ++t) {
             mbar_init(s_full(t), 1);
-            mbar_init(p_full(t), 4);     // one arrival per softmax warp of the tile
+            mbar_init(p_full(t, 0), 4);   // one arrival per softmax warp of the tile
+            mbar_init(p_full(t, 1), 4);
             mbar_init(o_done(t), 1);
         }
         mbar_init(drain_bar, 1);
@@ -290,11 +293,14 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     mma_f16(scol_t[t], qdesc[t] + off, kdesc + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            auto mma_pv = [&](int t, uint64_t vdesc, bool acc) {   // O_t (+)= P_t V, P_t in S_t
+            // O_t (+)= P_t V over keys 64 h .. 64 h + 63, P_t in S_t's columns 32 h ..
+            auto mma_pv = [&](int t, int h, uint64_t vdesc, bool acc) {
 #pragma unroll
-                for (uint32_t kk = 0; kk < BKV / 16; ++kk)   // keys 16 kk ..: P columns 8 kk ..
+                for (uint32_t k4 = 0; k4 < BKV / 32; ++k4) {   // keys 16 kk ..: P columns 8 kk ..
+                    const uint32_t kk = 4 * h + k4;
                     mma_f16_ta(ocol_t[t], scol_t[t] + 8 * kk, vdesc + kk * (2048 >> 4), IDESC_PV,
                                (acc || kk > 0) ? 1u : 0u);
+                }
             };
             // S_0(0), S_1(0); then per key tile j two blocks, each behind its waits: P V of query
             // tile 0 with its scores for key tile j + 1, then the same for query tile 1.  The
@@ -322,19 +328,25 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 const uint32_t vb = v_full(j % V_STAGES), vp = (j / V_STAGES) & 1;
                 const uint32_t kb = k_full(kn), kp = ((j + 1) / K_STAGES) & 1;
                 const bool r_v = mbar_try_wait(vb, vp);
-                const bool r_p = mbar_try_wait(p_full(0), j & 1);
+                const bool r_p = mbar_try_wait(p_full(0, 0), j & 1);
                 const bool r_k = !next || mbar_try_wait(kb, kp);
                 if (!__all_sync(0xFFFFFFFFu, r_v && r_p && r_k))
                     ok = mbar_wait_warp(vb, vp, timeout_ns) &&
-                         mbar_wait_warp(p_full(0), j & 1, timeout_ns) &&
+                         mbar_wait_warp(p_full(0, 0), j & 1, timeout_ns) &&
                          (!next || mbar_wait_warp(kb, kp, timeout_ns));
                 if (!ok) break;
                 tc_fence_after();
                 const int vs = j % V_STAGES;
                 const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(vs) * (TILE_BYTES >> 4);
                 const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(kn) * (TILE_BYTES >> 4);
+                // the first half of P V while the softmax exponentiates the second half
+                if (elect_one()) mma_pv(0, 0, vdesc, j > 0);
+                __syncwarp();
+                ok = mbar_wait_warp(p_full(0, 1), j & 1, timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
                 if (elect_one()) {
-                    mma_pv(0, vdesc, j > 0);
+                    mma_pv(0, 1, vdesc, true);
                     if (next) {
                         mma_s(0, kdesc);
                         tc_commit(s_full(0));
@@ -343,11 +355,16 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     }
                 }
                 __syncwarp();
-                ok = mbar_wait_warp(p_full(1), j & 1, timeout_ns);
+                ok = mbar_wait_warp(p_full(1, 0), j & 1, timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) mma_pv(1, 0, vdesc, j > 0);
+                __syncwarp();
+                ok = mbar_wait_warp(p_full(1, 1), j & 1, timeout_ns);
                 if (!ok) break;
                 tc_fence_after();
                 if (elect_one()) {
-                    mma_pv(1, vdesc, j > 0);
+                    mma_pv(1, 1, vdesc, true);
                     tc_commit(v_empty(vs));
                     if (next) {
                         mma_s(1, kdesc);
@@ -427,17 +444,21 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 l0 = full ? exp_half<false>(v0, 0, valid, c_log2, m_used, pk)
                           : exp_half<true>(v0, 0, valid, c_log2, m_used, pk);
             }
-            // P over the scores: keys 0 .. 63 into columns 0 .. 31, keys 64 .. 127 into columns
-            // 32 .. 63
+            // P over the scores: keys 0 .. 63 into columns 0 .. 31, released to P V at once, then
+            // keys 64 .. 127 into columns 32 .. 63
             l += l0;
             tmem_st_32x32b_x32(scol, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(t, 0));
             l += full ? exp_half<false>(v1, 64, valid, c_log2, m_used, pk)
                       : exp_half<true>(v1, 64, valid, c_log2, m_used, pk);
             tmem_st_32x32b_x32(scol + 32, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(t));
+            if (lane == 0) mbar_arrive(p_full(t, 1));
         }
         if (!ok) {
             if (lane == 0) atomicOr(err, ERR_EPILOGUE);
