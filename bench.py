@@ -409,12 +409,10 @@ def run_ours(args, ws, rank, local):
     value = (whole_job_rate(ws, flops["mxfp8"], mean["mxfp8"]) / 1e12
              if mx_tflops is not None else None)
     # one qgemm_mxfp8 call at 8192^3 is two launches (scale repack + CTA-pair GEMM), one
-    # qgemm_w4a16 call two (the GEMM + the outlier-row pass), one attention call at 32 x 4096 x
-    # 4096 two when its last wave is split along the keys (the kernel + the merge of the halves)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    attn_units = 32 * (4096 // 256)
-    attn_split = attn_units > sms and 0 < 2 * (attn_units % sms) <= sms
-    launches = sum(2 if k.startswith("mxfp") or k == "w4a16" or (k == "attention" and attn_split)
+    # qgemm_w4a16 call two (the GEMM + the outlier-row pass), one attention call one (the
+    # persistent kernel merges the units its key-tile ranges split; the flags it zeroes first
+    # are a driver memset, not a kernel of this library)
+    launches = sum(2 if k.startswith("mxfp") or k == "w4a16"
                    else GEMV_RUN if k.startswith("gemv") else 1 for k in kernels) * args.steps
     launches += args.steps * (("mxfp8" in kernels) + ("gemv_m1" in kernels))   # clock probes
     line = {

@@ -88,21 +88,78 @@ def test_attention_interleaved_heads_layout(dev, orc):
     _check(Oi.transpose(0, 1), res, orc, "attention interleaved heads")
 
 
-def test_attention_split_last_wave(dev, orc):
-    """A grid whose last wave would leave more than half the SMs idle: its units (head, 256
-    query rows) are computed as two halves of their key tiles and merged.  The head count is
-    chosen from the SM count so that 4 BH units exceed one wave by a few; Lk = 600 puts the
-    ragged key tile in the second half."""
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    BH, Lq, Lk = (sms + 1 + 3) // 4 + 1, 1024, 600
-    units = BH * ((Lq + 255) // 256)
-    assert units > sms and 0 < 2 * (units - sms) <= sms      # the split path is taken
-    d = synth.attention_inputs(BH, Lq, Lk, 128, seed=74, q_std=2.0)
+def _parts(units, nkv, sms, min_range=4):
+    """The kernel's work split, restated on the host for the tests' assertions: whole waves of
+    units data-parallel while at least two waves remain, then the key tiles of the units left
+    in equal contiguous ranges, one per CTA.  Returns (CTAs, per CTA the list of (unit, first
+    key tile, key tiles, kind)) with kind 'whole', 'tail' (range starts inside the unit) or
+    'head' (range ends inside it)."""
+    G = max(1, min(sms, units * nkv // min_range))
+    D = units // G - 1 if units // G >= 2 else 0
+    u0, T = D * G, (units - D * G) * nkv
+    start = lambda c: c * (T // G) + min(c, T % G)
+    out = []
+    for c in range(G):
+        parts = [(w * G + c, 0, nkv, "whole") for w in range(D)]
+        cur, end = start(c), start(c + 1)
+        while cur < end:
+            u, kv0 = divmod(cur, nkv)
+            n = min(end, (u + 1) * nkv) - cur
+            kind = "tail" if kv0 > 0 else ("head" if cur + n < (u + 1) * nkv else "whole")
+            parts.append((u0 + u, kv0, n, kind))
+            cur += n
+        out.append(parts)
+    return G, out
+
+
+def _check_split_case(dev, orc, BH, Lq, Lk, seed, what):
+    d = synth.attention_inputs(BH, Lq, Lk, 128, seed=seed, q_std=2.0)
     O = _run(d, dev)
     res = orc.attention(d["q"].numpy(), d["k"].numpy(), d["v"].numpy(), d["scale"])
-    _check(O, res, orc, f"attention split last wave {BH}x{Lq}x{Lk}")
+    _check(O, res, orc, f"{what} {BH}x{Lq}x{Lk}")
     O2 = _run(d, dev)
     assert torch.equal(O2.view(torch.int16), O.view(torch.int16))     # repeatable bit for bit
+
+
+def test_attention_waves_then_ranges(dev, orc):
+    """More than two waves of units (head, 256 query rows): whole waves run data-parallel, and
+    the units left are shared out in key-tile ranges whose boundaries cut units into a tail
+    (its CTA's first part) and a head (another CTA's last part), merged in the head's output.
+    Lk = 600 puts the ragged key tile in the tails."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    BH, Lq, Lk = (2 * sms + 7) // 4 + 1, 1024, 600
+    units, nkv = BH * 4, (Lk + 127) // 128
+    G, parts = _parts(units, nkv, sms)
+    assert units // G >= 2                                          # a data-parallel wave
+    kinds = [k for p in parts for (_, _, _, k) in p]
+    assert "tail" in kinds and "head" in kinds
+    _check_split_case(dev, orc, BH, Lq, Lk, 74, "attention waves + ranges")
+
+
+def test_attention_ranges_only(dev, orc):
+    """Between one and two waves of units: no data-parallel wave, every CTA's work is a range,
+    some CTAs both finish a unit's tail first and start another unit's head last."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    BH, Lq, Lk = (sms + 4) // 4 + 1, 1024, 1000
+    units, nkv = BH * 4, (Lk + 127) // 128
+    G, parts = _parts(units, nkv, sms)
+    assert G == sms and units // G == 1
+    assert any(p[0][3] == "tail" and p[-1][3] == "head" for p in parts)
+    _check_split_case(dev, orc, BH, Lq, Lk, 75, "attention ranges")
+
+
+@pytest.mark.parametrize("BH,Lq,Lk", [(1, 256, 8192), (1, 100, 4096), (2, 300, 2000)])
+def test_attention_unit_over_many_ctas(dev, orc, BH, Lq, Lk):
+    """Fewer units than SMs: a unit's key tiles spread over several CTAs, whose head part merges
+    several tails; Lq = 100 and 300 leave rows of a merged unit past Lq (computed, not
+    stored)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    units, nkv = BH * ((Lq + 255) // 256), (Lk + 127) // 128
+    G, parts = _parts(units, nkv, sms)
+    tails = max(sum(1 for p in parts for (u, _, _, k) in p if k == "tail" and u == uu)
+                for uu in range(units))
+    assert tails >= 2
+    _check_split_case(dev, orc, BH, Lq, Lk, 76 + Lq, "attention unit over many CTAs")
 
 
 def test_attention_errors(dev):
