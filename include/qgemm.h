@@ -281,7 +281,13 @@ qgemm_status qgemm_w8_gemv(const void *X_f16, int64_t ldx, int64_t M, const qgem
  * rows (row stride >= d, head stride >= Lq * row stride) or rows outside heads (head stride >= d,
  * row stride >= BH * head stride, as in a [batch, L, heads, d] buffer).  BH == 0 or Lq == 0 does
  * nothing.
- * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+ * Launch: one cooperative kernel of up to one CTA per SM (every CTA resident at once: CTAs merge
+ * the rows of units they share), preceded, when work ranges cut units, by a memset of the flags
+ * in a stream-ordered workspace of about 133 KB per CTA taken from the library's pool and freed
+ * after the launch.  The result does not depend on the stream's other work and repeats bit for
+ * bit for the same inputs and SM count.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA (including a
+ * cooperative launch the device cannot make resident). */
 qgemm_status qgemm_attention_f16(const void *Q, const void *K, const void *V, void *O, int64_t BH,
                                  int64_t Lq, int64_t Lk, int64_t d, int64_t q_head_stride,
                                  int64_t q_row_stride, int64_t k_head_stride, int64_t k_row_stride,
