@@ -55,6 +55,10 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr int S = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    // a kernel launched after this one as a programmatic dependent (a decode GEMV) may be
+    // scheduled now: it waits for this grid's completion before it touches memory, and its
+    // launch no longer waits for the last CTA to exit
+    griddep_launch_dependents();
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -270,6 +274,10 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                      int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
+    // a kernel launched after this one as a programmatic dependent (a decode GEMV) may be
+    // scheduled now: it waits for this grid's completion before it touches memory, and its
+    // launch no longer waits for the last CTA to exit
+    griddep_launch_dependents();
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
