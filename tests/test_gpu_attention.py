@@ -148,11 +148,12 @@ def test_attention_ranges_only(dev, orc):
     _check_split_case(dev, orc, BH, Lq, Lk, 75, "attention ranges")
 
 
-@pytest.mark.parametrize("BH,Lq,Lk", [(1, 256, 8192), (1, 100, 4096), (2, 300, 2000)])
+@pytest.mark.parametrize("BH,Lq,Lk", [(1, 256, 8192), (1, 100, 4096), (2, 300, 2000),
+                                      (1, 256, 65536), (1, 1, 4096), (3, 1, 2048)])
 def test_attention_unit_over_many_ctas(dev, orc, BH, Lq, Lk):
     """Fewer units than SMs: a unit's key tiles spread over several CTAs, whose head part merges
-    several tails; Lq = 100 and 300 leave rows of a merged unit past Lq (computed, not
-    stored)."""
+    several tails (127 of them for one unit over 65536 keys); Lq = 100, 300 and 1 leave rows of a
+    merged unit past Lq (computed, not stored)."""
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     units, nkv = BH * ((Lq + 255) // 256), (Lk + 127) // 128
     G, parts = _parts(units, nkv, sms)
