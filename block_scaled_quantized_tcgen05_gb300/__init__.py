@@ -42,8 +42,13 @@ class QGemmError(RuntimeError):
         super().__init__(f"{where}: {self.name}: {message}")
 
 
+def debug_build_selected() -> bool:
+    """QGEMM_DEBUG=1 selects the bounds-checking build libqgemm_debug.so (see build.py)."""
+    return os.environ.get("QGEMM_DEBUG", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_build_selected() else _build.LIB_PATH
 
 
 def load_library():
@@ -53,8 +58,9 @@ def load_library():
         return _lib
     path = library_path()
     if not os.path.exists(path):
-        raise ImportError(f"libqgemm.so not built at {path}; run "
-                          "`python -m block_scaled_quantized_tcgen05_gb300.build`")
+        raise ImportError(f"{os.path.basename(path)} not built at {path}; run "
+                          "`python -m block_scaled_quantized_tcgen05_gb300.build"
+                          + (" --debug`" if debug_build_selected() else "`"))
     lib = ctypes.CDLL(path)
     P, I64, I32, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
     S = ctypes.c_int

@@ -59,6 +59,7 @@
 // Every wait is bounded; on a timeout the kernel records the error bit, stops issuing work,
 // waits for its copies and MMAs, frees TMEM and returns.
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -401,7 +402,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     for (int j = 0; j < p.nkv; ++j) {
                         const uint32_t full = isk ? k_full(st) : v_full(st);
                         const uint32_t empty = isk ? k_empty(st) : v_empty(st);
-                        if (!mbar_wait(empty, ph ^ 1, timeout_ns)) {
+                        // debug build: the key tile starts inside Lk
+                        if (!QG_IN_BOUNDS(err, (p.kv0 + j) * BKV < Lk) ||
+                            !mbar_wait(empty, ph ^ 1, timeout_ns)) {
                             ok = false;
                             break;
                         }
@@ -662,6 +665,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 break;
             }
             tc_fence_after();
+            // debug build: a part that shares its unit with another CTA has the workspace and
+            // flags the host allocates when some range starts inside a unit
+            if (p.kind != PART_WHOLE && !QG_IN_BOUNDS(err, ws != nullptr && flags != nullptr)) {
+                ok = false;
+                break;
+            }
             if (p.kind == PART_TAIL) {
                 // the unit's tail: unnormalised rows, m and l for the CTA holding its head
                 float *wsb = ws + static_cast<size_t>(sc.cta) * WS_FLOATS;
@@ -694,7 +703,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     const int64_t uend = (p.unit - sc.u0 + 1) * nkv_all;
                     while (w_end < sc.G && range_start(w_end, sc.T, sc.G) < uend) ++w_end;
                     for (int64_t w = w0; w < w_end && ok; ++w) {
-                        ok = wait_flag(flags + w * FLAGS_PER_SLOT + slab, timeout_ns);
+                        // debug build: the writer's range starts inside this unit
+                        ok = QG_IN_BOUNDS(err, range_start(w, sc.T, sc.G) >
+                                                   (p.unit - sc.u0) * nkv_all) &&
+                             wait_flag(flags + w * FLAGS_PER_SLOT + slab, timeout_ns);
                         if (ok) m_tot = fmaxf(m_tot, __ldcg(ws + w * WS_FLOATS + WS_M + r));
                     }
                     if (!__all_sync(0xFFFFFFFFu, ok)) {

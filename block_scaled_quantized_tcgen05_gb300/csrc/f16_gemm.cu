@@ -11,6 +11,7 @@
 //   warps 2-5  epilogue: TMEM -> fp16 -> global, masked at the M / N edges.
 // Shapes with more than one 128-row and one 128-column block use the CTA-pair kernel below.
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -109,6 +110,11 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                if (!QG_IN_BOUNDS(err, (kt * BK) % 8 == 0 && (nb * BN) % 8 == 0)) {
                     ok = false;
                     break;
                 }
@@ -340,6 +346,11 @@ gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 const uint32_t tx = 2 * (P_A_BYTES + (half < 0 ? P_B_BYTES : P_B_ATOM));
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                    if (!QG_IN_BOUNDS(err, (kt * P_BK) % 8 == 0 && nh % 8 == 0)) {
                         ok = false;
                         break;
                     }

@@ -24,6 +24,7 @@
 // byte loads).  The epilogue stages each 32 x 32 chunk in shared memory for sector-wide stores.
 // Every wait is bounded.
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -225,6 +226,11 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                if (!QG_IN_BOUNDS(err, (kt * BK) % 16 == 0)) {
                     ok = false;
                     break;
                 }

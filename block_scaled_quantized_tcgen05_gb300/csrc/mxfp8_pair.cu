@@ -47,6 +47,7 @@
 // the scale blocks as 2-D tensor boxes 16 bytes wide (+0.6%); raster groups of 8 or 32 pair rows
 // instead of 16 (+1%, +5%); L2 prefetch of A and B eight k-tiles ahead (+10%).
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -138,7 +139,7 @@ struct SfPackOperand {
 // word kw is word kw % W of stage kw / W.
 template <int W>
 __global__ void __launch_bounds__(256)
-sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
+sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT, unsigned *err) {
     __shared__ __align__(16) uint8_t tile[128 * PACK_ROW];
     griddep_launch_dependents();   // the GEMM, a programmatic dependent, may start its set-up
     const SfPackOperand &op = blockIdx.z == 0 ? opA : opB;
@@ -181,9 +182,10 @@ sf_pack_kernel(SfPackOperand opA, SfPackOperand opB, int KT) {
     v.y = w[(i + 32) * WPR + ktl];
     v.z = w[(i + 64) * WPR + ktl];
     v.w = w[(i + 96) * WPR + ktl];
-    uint8_t *dst =
-        op.out + (((static_cast<int64_t>(kw / W) * op.rbp + rb) * W + kw % W) * 32 + i) * 16;
-    *reinterpret_cast<uint4 *>(dst) = v;
+    const int64_t off = (((static_cast<int64_t>(kw / W) * op.rbp + rb) * W + kw % W) * 32 + i) * 16;
+    // the repacked plane holds KT x rbp x W x 32 lines of 16 bytes
+    if (QG_IN_BOUNDS(err, off >= 0 && off + 16 <= static_cast<int64_t>(KT) * op.rbp * W * 512))
+        *reinterpret_cast<uint4 *>(op.out + off) = v;
 }
 
 // -------------------------------------------------------------------------------- the GEMM
@@ -282,18 +284,28 @@ mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         break;
                     }
                     const uint32_t lead_full = map_to_cta(full_bar(stage), 0);
+                    // debug build: the stage's scale lines lie inside the repacked planes, and
+                    // the copies' innermost coordinate is a multiple of 16 bytes
+                    const int64_t sa_off = (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W;
+                    const int64_t sb_off = (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W;
+                    if (!(QG_IN_BOUNDS(err, (kt * BK) % 16 == 0) &&
+                          QG_IN_BOUNDS(err, sa_off >= 0 && sa_off + SFA_BYTES <=
+                                                static_cast<int64_t>(KT) * rbpA * 512 * W) &&
+                          QG_IN_BOUNDS(err, sb_off >= 0 && sb_off + sfb_bytes <=
+                                                static_cast<int64_t>(KT) * rbpB * 512 * W))) {
+                        ok = false;
+                        break;
+                    }
                     if (elect_one()) {
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_BYTES + b_bytes));
                         tma_load_2d_pair(sb + OFF_A + stage * A_BYTES, &tmA, lead_full, kt * BK, m0);
                         tma_load_2d_pair_hint(sb + OFF_B + stage * B_BYTES, half < 0 ? &tmB : &tmB64,
                                               lead_full, kt * BK, nh, keep);
                         mbar_arrive_expect_tx(sf_full(stage), SFA_BYTES + sfb_bytes);
-                        bulk_load(sb + OFF_SFA + stage * SFA_BYTES,
-                                  packA + (static_cast<int64_t>(kt) * rbpA * 32 + la) * 16 * W,
-                                  SFA_BYTES, sf_full(stage));
-                        bulk_load(sb + OFF_SFB + stage * SFB_BYTES,
-                                  packB + (static_cast<int64_t>(kt) * rbpB * 32 + lb) * 16 * W,
-                                  sfb_bytes, sf_full(stage));
+                        bulk_load(sb + OFF_SFA + stage * SFA_BYTES, packA + sa_off, SFA_BYTES,
+                                  sf_full(stage));
+                        bulk_load(sb + OFF_SFB + stage * SFB_BYTES, packB + sb_off, sfb_bytes,
+                                  sf_full(stage));
                     }
                     __syncwarp();
                     ++issued;
@@ -483,12 +495,12 @@ SfPackOperand pack_operand(const qgemm_tensor *t, uint8_t *out) {
 // Repack one or two operands' scale planes (nops = 1: opA only).
 template <class F>
 cudaError_t launch_sf_pack(const SfPackOperand &pa, const SfPackOperand &pb, int nops, int KT,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, unsigned *err) {
     const int rbp = nops == 2 && pb.rbp > pa.rbp ? pb.rbp : pa.rbp;
     const dim3 pgrid(static_cast<unsigned>(rbp),
                      static_cast<unsigned>((KT * F::W + PACK_KT - 1) / PACK_KT),
                      static_cast<unsigned>(nops));
-    sf_pack_kernel<F::W><<<pgrid, 256, 0, stream>>>(pa, nops == 2 ? pb : pa, KT);
+    sf_pack_kernel<F::W><<<pgrid, 256, 0, stream>>>(pa, nops == 2 ? pb : pa, KT, err);
     return cudaGetLastError();
 }
 
@@ -541,7 +553,7 @@ cudaError_t launch_pair(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,
     uint8_t *packB = packA + static_cast<size_t>(KT) * padded_blocks(A->rows) * 512 * F::W;
     *encode_ok = true;
     cudaError_t e = launch_sf_pack<F>(pack_operand<F>(A, packA), pack_operand<F>(B, packB), 2,
-                                      KT, ctx.stream);
+                                      KT, ctx.stream, ctx.err);
     if (e != cudaSuccess) return e;
     return launch_pair_packed<F>(A, B, C, ldc, packA, packB, ctx, encode_ok);
 }
@@ -571,7 +583,7 @@ size_t mxfp8_pack_bytes(const qgemm_tensor *T) {
 cudaError_t launch_mxfp8_sf_pack(const qgemm_tensor *T, void *out, const LaunchCtx &ctx) {
     const int KT = static_cast<int>((k_bytes<FmtE4M3>(T) + BK - 1) / BK);
     const SfPackOperand op = pack_operand<FmtE4M3>(T, static_cast<uint8_t *>(out));
-    return launch_sf_pack<FmtE4M3>(op, op, 1, KT, ctx.stream);
+    return launch_sf_pack<FmtE4M3>(op, op, 1, KT, ctx.stream, ctx.err);
 }
 
 cudaError_t launch_mxfp8_pair_packed(const qgemm_tensor *A, const qgemm_tensor *B, __half *C,

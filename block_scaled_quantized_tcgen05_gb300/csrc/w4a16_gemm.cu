@@ -19,6 +19,7 @@
 // The fp16 weight q * 2^(e-127) is exact for 103 <= e <= 139; other bytes give 0 (NaN for 255)
 // and the rows where that matters are rewritten by w4a16_outlier.cu (w4a16_convert.cuh).
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 #include "w4a16_convert.cuh"
@@ -195,6 +196,11 @@ w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__rest
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                if (!QG_IN_BOUNDS(err, (kt * BK) % 8 == 0)) {
                     ok = false;
                     break;
                 }
@@ -495,6 +501,11 @@ w4a16_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                if (!QG_IN_BOUNDS(err, (kt * BK) % 8 == 0 && (kt * (BK / 2)) % 16 == 0 && (16 * (kt / T_SF_GROUP)) % 8 == 0)) {
                     ok = false;
                     break;
                 }

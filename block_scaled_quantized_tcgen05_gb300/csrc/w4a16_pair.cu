@@ -41,6 +41,7 @@
 // which is that recipe's half multiply; scales are read 16 bytes = 4 k-tiles at a time, so that
 // instance needs K % 256 == 0 and 16-byte aligned scale rows, and takes every M and N.
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 #include "w4a16_convert.cuh"
@@ -163,6 +164,11 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const int t0 = tb * BT + static_cast<int>(rank) * (BT / 2);   // this CTA's tokens
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // debug build: the copies' innermost coordinates are multiples of 16 bytes
+                    if (!QG_IN_BOUNDS(err, (kt * BK) % 8 == 0 && (kt * (BK / 2)) % 16 == 0)) {
                         ok = false;
                         break;
                     }

@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include "qgemm_common.cuh"
+#include "qgemm_debug.cuh"
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
@@ -250,6 +251,12 @@ w8_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             for (int rb = blockIdx.x; rb < nrb && ok; rb += gridDim.x) {
                 for (int kc = 0; kc < nkc; ++kc) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // debug build: innermost coordinates multiples of 16 bytes, the row block
+                    // inside N
+                    if (!QG_IN_BOUNDS(err, (kc * KC) % 16 == 0 && rb * ROWS < N)) {
                         ok = false;
                         break;
                     }

@@ -349,7 +349,9 @@ const char *qgemm_last_error_message(void);
 
 /* Synchronise `stream`, then read and clear the device error word of the current device.
  * *code_out (may be NULL) receives the raw word: 0 = no kernel gave up; otherwise bits name the
- * wait that ran out (1 producer, 2 MMA issuer, 4 epilogue, 8 drain, 16 test wait).
+ * wait that ran out (1 producer, 2 MMA issuer, 4 epilogue, 8 drain, 16 test wait) or, in the
+ * debug build (libqgemm_debug.so, compiled with QGEMM_DEBUG), 32 = a kernel's own bounds check
+ * failed and the access was skipped.
  * Returns QGEMM_ERR_TIMEOUT if the word was non-zero, QGEMM_ERR_CUDA if synchronisation failed. */
 qgemm_status qgemm_poll_device_error(void *stream, uint32_t *code_out);
 
