@@ -15,7 +15,7 @@ from . import build as _build
 
 __all__ = [
     "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
-    "qgemm_version", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
+    "qgemm_version", "qgemm_debug_build", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
     "qgemm_mxfp8", "qgemm_mxfp8_host", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout", "qgemm_sm_clock_probe",
@@ -66,6 +66,7 @@ def load_library():
     S = ctypes.c_int
     sig = {
         "qgemm_version": (I32, []),
+        "qgemm_debug_build": (I32, []),
         "qgemm_create_tensor": (S, [ctypes.POINTER(P), S, I64, I64, P, I64, P, I64, I32]),
         "qgemm_tensor_slice": (S, [P, I64, I64, I64, I64, ctypes.POINTER(P)]),
         "qgemm_destroy_tensor": (None, [P]),
@@ -160,6 +161,11 @@ class QTensor:
 
 def qgemm_version() -> int:
     return load_library().qgemm_version()
+
+
+def qgemm_debug_build() -> bool:
+    """True when the loaded library is the bounds-checking debug build."""
+    return load_library().qgemm_debug_build() == 1
 
 
 def qgemm_status_string(status: int) -> str:

@@ -197,6 +197,14 @@ extern "C" {
 
 int32_t qgemm_version(void) { return (1 << 16) | 0; }
 
+int32_t qgemm_debug_build(void) {
+#ifdef QGEMM_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 const char *qgemm_status_string(qgemm_status s) {
     switch (s) {
     case QGEMM_OK: return "QGEMM_OK";

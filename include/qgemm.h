@@ -68,6 +68,12 @@ typedef struct qgemm_tensor qgemm_tensor;
 /* Library version, (major << 16) | minor. */
 int32_t qgemm_version(void);
 
+/* 1 in the debug build (libqgemm_debug.so, compiled with QGEMM_DEBUG: every kernel checks its own
+ * index arithmetic and reports a failed check as bit 32 of the device error word, see
+ * qgemm_poll_device_error), 0 in the release build.  The pages have no counterpart: it lets a
+ * test confirm which build it runs. */
+int32_t qgemm_debug_build(void);
+
 /* Create a view of a quantized matrix: data plane plus UE8M0 scale plane.
  * Passage: "TensorOps: quantized matmul ...", section "Scale planes: one MTLTensor = data +
  * scales" (one object carries the data plane and an auxiliary plane of block scales; the block

@@ -29,6 +29,7 @@ import oracle
 from block_scaled_quantized_tcgen05_gb300 import synth
 
 assert os.path.basename(q.library_path()) == "libqgemm_debug.so", q.library_path()
+assert q.qgemm_debug_build(), "the loaded library was not compiled with QGEMM_DEBUG"
 g.smoke()   # every hot-path route against the oracle; raises on a non-zero error word
 dev = torch.device("cuda:0")
 
