@@ -286,7 +286,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t lane = threadIdx.x & 31;
     // Every role walks the CTA's parts in the same order.  The K and V rings and the score / P
     // barriers run on across part boundaries (their phases follow a key-tile count over the
-    // whole range), so the next part's loads and first scores overlap the last part's end.
+    // whole range), so the next part's K and V loads overlap the last part's end; its Q waits
+    // for the last part's output to leave the Q buffer.
     const int nkv_all = (Lk + BKV - 1) / BKV;
     const Sched sc = make_sched(units, nkv_all, nqb);
 
