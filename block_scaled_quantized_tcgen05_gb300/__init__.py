@@ -16,7 +16,7 @@ from . import build as _build
 __all__ = [
     "QGemmError", "QTensor", "F16", "E4M3", "INT8", "INT4", "E2M1", "load_library", "library_path",
     "qgemm_version", "qgemm_debug_build", "qgemm_create_tensor", "qgemm_tensor_slice", "qgemm_destroy_tensor",
-    "qgemm_mxfp8", "qgemm_mxfp8_host", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
+    "qgemm_mxfp8", "qgemm_mxfp8_scratch_bytes", "qgemm_mxfp8_host", "qgemm_mxfp4", "gemm_f16", "qgemm_w4a16", "qgemm_w4a16_f16s", "qgemm_attention", "qgemm_w8_gemv", "qgemm_dequant_debug",
     "qgemm_status_string", "qgemm_poll_device_error", "qgemm_set_wait_timeout_ns",
     "qgemm_selftest_wait_timeout", "qgemm_sm_clock_probe",
 ]
@@ -75,6 +75,7 @@ def load_library():
                                   ctypes.POINTER(P), ctypes.POINTER(I64)]),
         "qgemm_mxfp8": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_noalloc": (S, [P, P, P, I64, P]),
+        "qgemm_mxfp8_scratch_bytes": (S, [P, P, ctypes.POINTER(I64)]),
         "qgemm_mxfp8_ex": (S, [P, P, P, I64, ctypes.POINTER(Epilogue), P]),
         "qgemm_mxfp4": (S, [P, P, P, I64, P]),
         "qgemm_mxfp8_host": (S, [P, P, P, I64, P]),
@@ -224,6 +225,14 @@ def qgemm_mxfp8_host(A: QTensor, B: QTensor, C, stream=None):
     _check(load_library().qgemm_mxfp8_host(A.handle, B.handle, _ptr(C), _ld(C), _stream(stream)),
            "qgemm_mxfp8_host")
     return C
+
+
+def qgemm_mxfp8_scratch_bytes(A: QTensor, B: QTensor) -> int:
+    """Bytes of pooled device scratch one qgemm_mxfp8 call on these views takes (0: none)."""
+    n = ctypes.c_int64(0)
+    _check(load_library().qgemm_mxfp8_scratch_bytes(A.handle, B.handle, ctypes.byref(n)),
+           "qgemm_mxfp8_scratch_bytes")
+    return n.value
 
 
 def qgemm_mxfp8_noalloc(A: QTensor, B: QTensor, C, stream=None):

@@ -15,6 +15,8 @@
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
+#include <algorithm>
+
 namespace {
 
 using namespace qg;
@@ -22,6 +24,7 @@ using namespace qg;
 constexpr int BM = 128;
 constexpr int BK = 64;         // fp16 elements of K per k-tile (one 128-byte swizzle row)
 constexpr int THREADS = 192;
+constexpr int SPLIT_UNIT = 8;  // split-K ranges are whole 512-wide slices of K (8 k-tiles)
 
 
 template <int BN>
@@ -50,15 +53,15 @@ __host__ __device__ constexpr uint32_t f16_idesc(int n) {
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, int epi,
-                unsigned *err, uint64_t timeout_ns) {
+                __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K, int splits,
+                float *__restrict__ P, int64_t ldp, int epi, unsigned *err, uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
-    // a kernel launched after this one as a programmatic dependent (a decode GEMV) may be
-    // scheduled now: it waits for this grid's completion before it touches memory, and its
-    // launch no longer waits for the last CTA to exit
+    // a kernel launched after this one as a programmatic dependent (a decode GEMV, the split-K
+    // reduction) may be scheduled now: it waits for this grid's completion before it touches
+    // memory, and its launch no longer waits for the last CTA to exit
     griddep_launch_dependents();
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
@@ -76,7 +79,9 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
+    const int num_items = num_tiles * splits;        // (tile, k range) work items
     const int KT = (K + BK - 1) / BK;
+    const int64_t plane = static_cast<int64_t>(M) * ldp;   // floats per split-K partial plane
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -105,10 +110,11 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint32_t stage = 0, phase = 0;
         int issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            int mb, nb;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            int tile, split, kt0, kt1, mb, nb;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            for (int kt = 0; kt < KT; ++kt) {
+            for (int kt = kt0; kt < kt1; ++kt) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
                     ok = false;
                     break;
@@ -152,14 +158,16 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         const uint32_t idesc = f16_idesc(BN);
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const uint32_t ab = acc_it & 1;       // accumulator buffer of this tile
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            int tile, split, kt0, kt1;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
+            const uint32_t ab = acc_it & 1;       // accumulator buffer of this item
             if (!mbar_wait_warp(tmem_empty(ab), ((acc_it >> 1) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int kt = 0; kt < KT; ++kt) {
+            for (int kt = kt0; kt < kt1; ++kt) {
                 if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
@@ -172,7 +180,7 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (uint32_t j = 0; j < BK / 16; ++j) {
                         // A: 16 halves = 32 bytes along the swizzle row; B: 16 k-rows = 2 KB
                         mma_f16(tmem_base + ab * BN, adesc + 2 * j, bdesc + 128 * j, idesc,
-                                (kt > 0 || j > 0) ? 1u : 0u);
+                                (kt > kt0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
                 }
@@ -196,8 +204,9 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else {
         const uint32_t q = warp & 3;
         uint32_t acc_it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            int mb, nb;
+        for (int it = blockIdx.x; it < num_items; it += gridDim.x) {
+            int tile, split, kt0, kt1, mb, nb;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it & 1;
             if (!mbar_wait_sleep(tmem_full(ab), (acc_it >> 1) & 1, timeout_ns, 128)) {
@@ -205,8 +214,13 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048, epi);
+            if (splits > 1)    // this k range's unrounded sum into its partial plane
+                partial_tile<BN>(tmem_base + ab * BN, q, lane, P + split * plane, ldp, mb * BM,
+                                 nb * BN, M, tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048);
+            else
+                epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                  c_vec != 0, tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048,
+                                  epi);
             ++acc_it;
         }
     }
@@ -219,8 +233,8 @@ gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
 template <int BN>
 cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb, __half *C,
-                      int64_t ldc, int M, int N, int K, const qgi::LaunchCtx &ctx,
-                      bool *encode_ok) {
+                      int64_t ldc, int M, int N, int K, int splits, float *P, int64_t ldp,
+                      const qgi::LaunchCtx &ctx, bool *encode_ok) {
     using G = Cfg<BN>;
     CUtensorMap tmA, tmB;
     *encode_ok = qgi::encode_tma_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK,
@@ -232,12 +246,44 @@ cudaError_t launch_bn(const __half *A, int64_t lda, const __half *B, int64_t ldb
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    const int64_t items = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * splits;
+    const int grid = items < ctx.num_sms ? static_cast<int>(items) : ctx.num_sms;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
-    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, c_vec, M, N, K, ctx.epi,
-                                                        ctx.err, ctx.timeout_ns);
+    kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, C, ldc, c_vec, M, N, K, splits, P,
+                                                        ldp, ctx.epi, ctx.err, ctx.timeout_ns);
     return cudaGetLastError();
+}
+
+// Split-K on the one-CTA route, as for the one-CTA MXFP8 GEMM: when the output has at most half
+// as many tiles as the GPU has SMs, each tile's k-tiles are shared out over up to SMs / tiles CTAs
+// (whole 512-wide slices of K), which write fp32 partial planes (M rows of tiles_n * BN floats)
+// that splitk_reduce.cu adds in split order.
+int f16_splits(int M, int N, int K, int bn, int num_sms) {
+    const int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+    const int64_t units = ((K + BK - 1) / BK + SPLIT_UNIT - 1) / SPLIT_UNIT;
+    if (2 * tiles > num_sms) return 1;
+    const int64_t s = std::min<int64_t>(num_sms / tiles, units);
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+template <int BN>
+cudaError_t launch_one_cta(const __half *A, int64_t lda, const __half *B, int64_t ldb, __half *C,
+                           int64_t ldc, int M, int N, int K, const qgi::LaunchCtx &ctx,
+                           bool *encode_ok) {
+    const int splits = f16_splits(M, N, K, BN, ctx.num_sms);
+    const int64_t ldp = static_cast<int64_t>((N + BN - 1) / BN) * BN;
+    void *ws = nullptr;
+    if (splits > 1) {
+        const cudaError_t e = qgi::scratch_alloc(
+            static_cast<size_t>(splits) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * sizeof(float),
+            ctx, &ws);
+        if (e != cudaSuccess) return e;
+    }
+    float *P = static_cast<float *>(ws);
+    cudaError_t e = launch_bn<BN>(A, lda, B, ldb, C, ldc, M, N, K, splits, P, ldp, ctx, encode_ok);
+    if (e == cudaSuccess && splits > 1) e = qgi::launch_splitk_reduce(P, splits, ldp, M, N, C, ldc, ctx);
+    const cudaError_t f = qgi::scratch_free(ws, ctx);
+    return e != cudaSuccess ? e : f;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -502,8 +548,8 @@ cudaError_t launch_gemm_f16(const __half *A, int64_t lda, const __half *B, int64
     // CTA pairs once there are at least two 128-row blocks and more than one 128-column block.
     if (M > 128 && N > 128)
         return launch_gemm_f16_pair(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
-    if (N > 128) return launch_bn<256>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
-    return launch_bn<128>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
+    if (N > 128) return launch_one_cta<256>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
+    return launch_one_cta<128>(A, lda, B, ldb, C, ldc, M, N, K, ctx, encode_ok);
 }
 
 }  // namespace qgi

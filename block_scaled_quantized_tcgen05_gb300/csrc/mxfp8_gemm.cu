@@ -28,6 +28,8 @@
 #include "qgemm_internal.h"
 #include "qgemm_ptx.cuh"
 
+#include <algorithm>
+
 namespace {
 
 using namespace qg;
@@ -39,6 +41,8 @@ constexpr uint32_t TMEM_COLS = 512;          // 2 accumulators of BN columns + s
 constexpr uint32_t SF_COLS_PER_STAGE = 16;  // SFA: 4 columns, SFB: 4 per 128 rows of B
 constexpr int SF_GROUP = 8;                 // k-tiles per scale group (SFM_TMA)
 constexpr uint32_t SF_ROW = SF_GROUP * 4;   // bytes of one row's scales per group (32)
+// Split-K ranges start on multiples of 4 k-tiles: 16 scale bytes, the TMA box's start rule.
+constexpr int SPLIT_UNIT = 4;
 
 enum { SFM_BYTES = 0, SFM_CPASYNC = 1, SFM_TMA = 2 };
 
@@ -113,7 +117,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                   const uint8_t *__restrict__ sfa, int64_t lds_a, const uint8_t *__restrict__ sfb,
                   int64_t lds_b, __half *__restrict__ C, int64_t ldc, int c_vec, int M, int N, int K,
-                  int epi, unsigned *err, uint64_t timeout_ns) {
+                  int splits, float *__restrict__ P, int64_t ldp, int epi, unsigned *err,
+                  uint64_t timeout_ns) {
     using G = Cfg<BN>;
     constexpr int S = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -121,6 +126,9 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
+    // a split-K reduction launched as a programmatic dependent may be scheduled now (it waits
+    // for this grid to complete before it reads anything)
+    griddep_launch_dependents();
 
     auto full_bar = [&](int s) { return sb + G::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + G::OFF_BAR + 8u * (S + s); };
@@ -135,9 +143,10 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
+    const int num_items = num_tiles * splits;        // (tile, k range) work items
     const int KT = (K + BK - 1) / BK;
     const int nkb = K / 32;                          // scale blocks per row
-    const int ngk = (KT + SF_GROUP - 1) / SF_GROUP;  // scale groups per tile
+    const int64_t plane = static_cast<int64_t>(M) * ldp;   // floats per split-K partial plane
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -169,38 +178,50 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        uint32_t stage = 0, phase = 0;
         int issued = 0;
-        int sf_issued = 0;       // scale groups requested (SFM_TMA), in CTA-local sequence
+        int sf_issued = 0;       // scale groups requested (SFM_TMA), in CTA-local sequence (lane 0)
         int sf_waited = 0;       // scale groups whose arrival this warp has observed
+        int sf_seq = 0;          // scale groups consumed
         bool ok = true;
-        // Request scale group q (sequence over this CTA's tiles) into the staging slot; the
-        // slot's barrier completes phase q when it lands.
-        auto issue_sf = [&](int q) {
-            const int tile = blockIdx.x + (q / ngk) * gridDim.x;
-            if (tile >= num_tiles) return;
-            int mb, nb;
+        // The next scale group to request (lane 0): group sf_g of work item sf_it, eight k-tiles
+        // from the item's first; the staging slot's barrier completes phase q when the q-th
+        // request lands.
+        int sf_it = static_cast<int>(blockIdx.x), sf_g = 0;
+        auto issue_sf = [&]() {
+            if (sf_it >= num_items) return;
+            int tile, split, kt0, kt1, mb, nb;
+            split_item(sf_it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
-            const int g = q % ngk;
+            const int x = 4 * kt0 + static_cast<int>(SF_ROW) * sf_g;   // 4 scale bytes per k-tile
             const uint32_t stg = sb + G::OFF_STG;
-            mbar_arrive_expect_tx(sf_full, (BM + BN) * SF_ROW);   // the two boxes' bytes
-            tma_load_2d(stg, &tmSA, sf_full, SF_ROW * g, mb * BM);
-            tma_load_2d(stg + G::STG_A, &tmSB, sf_full, SF_ROW * g, nb * BN);
-            sf_issued = q + 1;
+            // debug build: the boxes' innermost coordinate is a multiple of 16 bytes
+            if (QG_IN_BOUNDS(err, x % 16 == 0)) {
+                mbar_arrive_expect_tx(sf_full, (BM + BN) * SF_ROW);   // the two boxes' bytes
+                tma_load_2d(stg, &tmSA, sf_full, x, mb * BM);
+                tma_load_2d(stg + G::STG_A, &tmSB, sf_full, x, nb * BN);
+            } else {
+                mbar_arrive(sf_full);
+            }
+            ++sf_issued;
+            if (++sf_g == (kt1 - kt0 + SF_GROUP - 1) / SF_GROUP) {
+                sf_g = 0;
+                sf_it += static_cast<int>(gridDim.x);
+            }
         };
         const uint64_t keep_policy = l2_policy_evict_last();
         // current scale group in registers: [half of the group][line lane + 32 c (+ 128 h)]
         uint4 ra[2][4], rb[2][G::SFB_GROUPS][4];
-        int tile_iter = 0;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tile_iter) {
-            int mb, nb;
+        uint32_t stage = 0, phase = 0;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            int tile, split, kt0, kt1, mb, nb;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const int m0 = mb * BM, n0 = nb * BN;
-            for (int kt = 0; kt < KT; ++kt) {
+            for (int kt = kt0; kt < kt1; ++kt) {
                 if constexpr (SFM == SFM_TMA) {
-                    if (kt % SF_GROUP == 0) {
-                        const int q = tile_iter * ngk + kt / SF_GROUP;
-                        if (q == 0 && lane == 0) issue_sf(0);
+                    if ((kt - kt0) % SF_GROUP == 0) {
+                        const int q = sf_seq++;
+                        if (q == 0 && lane == 0) issue_sf();
                         if (!mbar_wait(sf_full, q & 1, timeout_ns)) {
                             ok = false;
                             break;
@@ -222,7 +243,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         // the whole group is in registers: refill the slot with the next one
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) issue_sf(q + 1);
+                        if (lane == 0) issue_sf();
                     }
                 }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1, timeout_ns)) {
@@ -249,8 +270,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t sSFA = sb + G::OFF_SFA + stage * G::SFA_BYTES;
                 const uint32_t sSFB = sb + G::OFF_SFB + stage * G::SFB_BYTES;
                 if constexpr (SFM == SFM_TMA) {
-                    const int j = kt % 4;
-                    const bool hi = (kt % SF_GROUP) >= 4;
+                    const int j = kt % 4;                          // kt0 % 4 == 0
+                    const bool hi = ((kt - kt0) % SF_GROUP) >= 4;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         if ((hf == 1) != hi) continue;
@@ -279,8 +300,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int c = 0; c < 4; ++c) {
                             const int r = n0 + 128 * h + 32 * c + static_cast<int>(lane);
                             const bool v = r < N;
-                            const uint8_t *src =
-                                v ? sfb + static_cast<int64_t>(r) * lds_b + kb0 : sfb;
+                            const uint8_t *src = v ? sfb + static_cast<int64_t>(r) * lds_b + kb0 : sfb;
                             cp_async_4(sSFB + h * 512 + lane * 16 + c * 4, src, v ? nbytes : 0u);
                         }
                     }
@@ -342,14 +362,16 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t stage = 0, phase = 0, acc_it = 0;
         bool ok = true;
         const uint32_t idesc = mx_idesc(BN);
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const uint32_t ab = acc_it % G::ACC_BUFS;   // accumulator buffer of this tile
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            int tile, split, kt0, kt1;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
+            const uint32_t ab = acc_it % G::ACC_BUFS;   // accumulator buffer of this item
             if (!mbar_wait_warp(tmem_empty(ab), ((acc_it / G::ACC_BUFS) & 1) ^ 1, timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int kt = 0; kt < KT; ++kt) {
+            for (int kt = kt0; kt < kt1; ++kt) {
                 if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                     ok = false;
                     break;
@@ -372,7 +394,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         // advance 32 bytes of K inside the 128-byte swizzle row
                         mma_mxf8(tmem_base + ab * BN, adesc + 2 * j, bdesc + 2 * j,
                                  idesc | (j << 4) | (j << 29), sf_col, sf_col + 4,
-                                 (kt > 0 || j > 0) ? 1u : 0u);
+                                 (kt > kt0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
                 }
@@ -399,8 +421,9 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ---------------------------------------------------------------- epilogue
         const uint32_t q = warp & 3;  // TMEM lane quarter this warp may read
         uint32_t acc_it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            int mb, nb;
+        for (int it = blockIdx.x; it < num_items; it += gridDim.x) {
+            int tile, split, kt0, kt1, mb, nb;
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
             tile_coords(tile, tiles_m, tiles_n, mb, nb);
             const uint32_t ab = acc_it % G::ACC_BUFS;
             if (!mbar_wait_sleep(tmem_full(ab), (acc_it / G::ACC_BUFS) & 1, timeout_ns, 128)) {
@@ -408,9 +431,13 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after();
-            epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N, c_vec != 0,
-                              tmem_empty(ab),
-                              sb + G::OFF_EPI + (warp - 2) * 2048, epi);
+            if (splits > 1)    // this k range's unrounded sum into its partial plane
+                partial_tile<BN>(tmem_base + ab * BN, q, lane, P + split * plane, ldp, mb * BM,
+                                 nb * BN, M, tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048);
+            else
+                epilogue_tile<BN>(tmem_base + ab * BN, q, lane, C, ldc, mb * BM, nb * BN, M, N,
+                                  c_vec != 0, tmem_empty(ab), sb + G::OFF_EPI + (warp - 2) * 2048,
+                                  epi);
             ++acc_it;
         }
     }
@@ -423,7 +450,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
 template <int BN, int SFM>
 cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
-                      const qgi::LaunchCtx &ctx, bool *encode_ok) {
+                      int splits, float *P, int64_t ldp, const qgi::LaunchCtx &ctx,
+                      bool *encode_ok) {
     using G = Cfg<BN>;
     const int M = static_cast<int>(A->rows), N = static_cast<int>(B->rows),
               K = static_cast<int>(A->k);
@@ -444,32 +472,67 @@ cudaError_t launch_bn(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, i
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+    const int64_t items = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * splits;
+    const int grid = items < ctx.num_sms ? static_cast<int>(items) : ctx.num_sms;
     const int c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0) ? 1 : 0;
     kern<<<grid, THREADS, G::SMEM_BYTES, ctx.stream>>>(tmA, tmB, tmSA, tmSB, A->scales, A->lds,
                                                         B->scales, B->lds, C, ldc, c_vec, M, N, K,
-                                                        ctx.epi, ctx.err, ctx.timeout_ns);
+                                                        splits, P, ldp, ctx.epi, ctx.err,
+                                                        ctx.timeout_ns);
     return cudaGetLastError();
 }
 
 template <int BN>
 cudaError_t launch_sfm(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
-                       const qgi::LaunchCtx &ctx, bool *encode_ok) {
+                       int splits, float *P, int64_t ldp, const qgi::LaunchCtx &ctx,
+                       bool *encode_ok) {
     auto al = [](const qgemm_tensor *t, int a) {
         return reinterpret_cast<uintptr_t>(t->scales) % a == 0 && t->lds % a == 0;
     };
-    if (al(A, 16) && al(B, 16)) return launch_bn<BN, SFM_TMA>(A, B, C, ldc, ctx, encode_ok);
-    if (al(A, 4) && al(B, 4)) return launch_bn<BN, SFM_CPASYNC>(A, B, C, ldc, ctx, encode_ok);
-    return launch_bn<BN, SFM_BYTES>(A, B, C, ldc, ctx, encode_ok);
+    if (al(A, 16) && al(B, 16))
+        return launch_bn<BN, SFM_TMA>(A, B, C, ldc, splits, P, ldp, ctx, encode_ok);
+    if (al(A, 4) && al(B, 4))
+        return launch_bn<BN, SFM_CPASYNC>(A, B, C, ldc, splits, P, ldp, ctx, encode_ok);
+    return launch_bn<BN, SFM_BYTES>(A, B, C, ldc, splits, P, ldp, ctx, encode_ok);
+}
+
+// Split-K on the one-CTA route: when the output has at most half as many tiles as the GPU has
+// SMs, each tile's k-tiles are shared out over up to SMs / tiles CTAs (whole units of four
+// k-tiles each), which write fp32 partial planes that splitk_reduce.cu adds in split order.
+// Partial planes are M rows of ldp = tiles_n * BN floats.
+struct SplitPlan {
+    int bn, splits;
+    int64_t ldp;
+    size_t bytes;
+};
+
+SplitPlan split_plan(const qgemm_tensor *A, const qgemm_tensor *B, int num_sms, bool allow) {
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    SplitPlan p;
+    p.bn = N > 128 ? 256 : 128;
+    const int64_t tiles_n = (N + p.bn - 1) / p.bn;
+    const int64_t tiles = ((M + BM - 1) / BM) * tiles_n;
+    const int64_t units = ((K + BK - 1) / BK + SPLIT_UNIT - 1) / SPLIT_UNIT;
+    int64_t s = 1;
+    if (allow && 2 * tiles <= num_sms) s = std::min<int64_t>(num_sms / tiles, units);
+    p.splits = static_cast<int>(s < 1 ? 1 : s);
+    p.ldp = tiles_n * p.bn;
+    p.bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * M * p.ldp * sizeof(float) : 0;
+    return p;
 }
 
 }  // namespace
 
 namespace qgi {
 
+size_t mxfp8_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B, int num_sms) {
+    if (A->rows == 0 || B->rows == 0 || A->k == 0) return 0;
+    if (mxfp8_pair_eligible(A, B)) return mxfp8_pair_scratch_bytes(A, B);
+    return split_plan(A, B, num_sms, true).bytes;
+}
+
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
-                         const LaunchCtx &ctx, bool *encode_ok) {
+                         const LaunchCtx &ctx, bool *encode_ok, bool allow_split) {
     // CTA pairs (mxfp8_pair.cu, scales repacked into pooled scratch) when both operands span
     // more than one 128-row block; otherwise one CTA per tile.  BN = 256 with one accumulator
     // measured faster than BN = 224 with two at 8192^3.
@@ -481,8 +544,20 @@ cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C
         const cudaError_t f = scratch_free(scratch, ctx);
         return e != cudaSuccess ? e : f;
     }
-    if (B->rows > 128) return launch_sfm<256>(A, B, C, ldc, ctx, encode_ok);
-    return launch_sfm<128>(A, B, C, ldc, ctx, encode_ok);
+    const SplitPlan p = split_plan(A, B, ctx.num_sms, allow_split);
+    void *ws = nullptr;
+    if (p.splits > 1) {
+        cudaError_t e = scratch_alloc(p.bytes, ctx, &ws);
+        if (e != cudaSuccess) return e;
+    }
+    float *P = static_cast<float *>(ws);
+    cudaError_t e = p.bn == 256 ? launch_sfm<256>(A, B, C, ldc, p.splits, P, p.ldp, ctx, encode_ok)
+                                : launch_sfm<128>(A, B, C, ldc, p.splits, P, p.ldp, ctx, encode_ok);
+    if (e == cudaSuccess && p.splits > 1)
+        e = launch_splitk_reduce(P, p.splits, p.ldp, static_cast<int>(A->rows),
+                                 static_cast<int>(B->rows), C, ldc, ctx);
+    const cudaError_t f = scratch_free(ws, ctx);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace qgi

@@ -176,7 +176,9 @@ extern "C" qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tens
                     e = qgi::launch_mxfp8_pair_packed(&ac, &bc, dC + r0 * ldcd, ldcd, pack_a, pack,
                                                       ctx, &enc);
             } else {
-                e = qgi::launch_mxfp8(&ac, &bc, dC + r0 * ldcd, ldcd, ctx, &enc);
+                // a K split only where the device call on the whole of A would split (A is one
+                // chunk), so both calls sum in the same order and give the same bits
+                e = qgi::launch_mxfp8(&ac, &bc, dC + r0 * ldcd, ldcd, ctx, &enc, rows == M);
             }
             if (!enc) return QGEMM_ERR_CUDA;
         }

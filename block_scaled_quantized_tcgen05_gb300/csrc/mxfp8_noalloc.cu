@@ -111,8 +111,8 @@ extern "C" qgemm_status qgemm_mxfp8_noalloc(const qgemm_tensor *A, const qgemm_t
         if (st != QGEMM_OK) return st;
         e = qgi::launch_mxfp8_pair(A, B, static_cast<__half *>(C), ldc, scratch, ctx, &enc);
     } else {
-        // one CTA per tile: this path uses no scratch
-        e = qgi::launch_mxfp8(A, B, static_cast<__half *>(C), ldc, ctx, &enc);
+        // one CTA per tile, K not split: this path uses no scratch
+        e = qgi::launch_mxfp8(A, B, static_cast<__half *>(C), ldc, ctx, &enc, false);
     }
     if (!enc) return QGEMM_ERR_CUDA;
     if (e != cudaSuccess)

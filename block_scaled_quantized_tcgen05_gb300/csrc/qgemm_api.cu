@@ -544,6 +544,22 @@ qgemm_status qgemm_mxfp8_ex(const qgemm_tensor *A, const qgemm_tensor *B, void *
     return st != QGEMM_OK ? st : mxfp8_impl(A, B, C, ldc, f, stream);
 }
 
+qgemm_status qgemm_mxfp8_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B,
+                                       int64_t *bytes) {
+    if (!bytes) return fail(QGEMM_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    if (!A || !B) return fail(QGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if (A->dtype != QGEMM_E4M3 || B->dtype != QGEMM_E4M3)
+        return fail(QGEMM_ERR_UNSUPPORTED_DTYPE, "qgemm_mxfp8 takes E4M3 views");
+    if (A->k != B->k) return fail(QGEMM_ERR_INVALID_ARG, "K mismatch (%lld vs %lld)",
+                                  (long long)A->k, (long long)B->k);
+    qgi::LaunchCtx ctx;
+    const qgemm_status st = get_ctx(nullptr, &ctx);
+    if (st != QGEMM_OK) return st;
+    *bytes = static_cast<int64_t>(qgi::mxfp8_scratch_bytes(A, B, ctx.num_sms));
+    return QGEMM_OK;
+}
+
 qgemm_status qgemm_mxfp4(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                          void *stream) {
     return mxfp4_impl(A, B, C, ldc, 0, stream);

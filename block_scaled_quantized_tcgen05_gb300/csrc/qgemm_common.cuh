@@ -199,6 +199,72 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tmem_base, uint32_t q, ui
     }
 }
 
+// Split-K: drain one 128 x BN fp32 accumulator tile, unrounded, into a partial plane P (row
+// stride ldp floats, rows 16-byte aligned, every column of the tile inside a row).  The warp's 32
+// rows go through its 2 KB of shared memory 16 columns at a time (the row-pair swizzle of the fp16
+// staging above), so each store instruction writes 8 rows x 64 contiguous bytes.  Rows >= M are
+// not written.  The accumulator is released (every lane arrives on `tmem_empty`) after its last
+// column has been read.
+template <int BN>
+__device__ __forceinline__ void partial_tile(uint32_t tmem_base, uint32_t q, uint32_t lane,
+                                             float *P, int64_t ldp, int m0, int n0, int M,
+                                             uint32_t tmem_empty, uint32_t stage) {
+    const uint32_t sw = (lane >> 1) & 3;
+    const uint32_t c16 = lane & 3;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + ch * 32, v);
+        tmem_wait_ld();
+        if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(tmem_empty);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t a = stage + lane * 64 + ((j ^ sw) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                             "r"(v[16 * h + 4 * j]), "r"(v[16 * h + 4 * j + 1]),
+                             "r"(v[16 * h + 4 * j + 2]), "r"(v[16 * h + 4 * j + 3])
+                             : "memory");
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t r = (lane >> 2) + 8 * i;
+                uint4 w;
+                const uint32_t a = stage + r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                             : "r"(a)
+                             : "memory");
+                const int grow = m0 + static_cast<int>(q * 32 + r);
+                const int gcol = n0 + ch * 32 + 16 * h + static_cast<int>(4 * c16);
+                if (grow < M)
+                    *reinterpret_cast<uint4 *>(P + static_cast<int64_t>(grow) * ldp + gcol) = w;
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// K range of split-K work item `it` of a one-CTA GEMM: tile it % num_tiles, split it / num_tiles.
+// The KT k-tiles are cut into `splits` ranges of whole units of `unit` k-tiles, as even as they
+// go (the first KU % splits ranges one unit longer), so a range starts on a unit boundary; the
+// last unit may be short.  splits <= ceil(KT / unit) keeps every range non-empty.
+__device__ __forceinline__ void split_item(int it, int num_tiles, int splits, int KT, int unit,
+                                           int &tile, int &split, int &kt0, int &kt1) {
+    tile = it % num_tiles;
+    split = it / num_tiles;
+    const int KU = (KT + unit - 1) / unit;
+    const int u0 = split * (KU / splits) + min(split, KU % splits);
+    const int u1 = u0 + KU / splits + (split < KU % splits ? 1 : 0);
+    kt0 = unit * u0;
+    kt1 = min(KT, unit * u1);
+}
+
 // Stage one 32 x 32 fp16 chunk (16 packed pairs per lane, lane = row) through this warp's 2 KB of
 // shared memory and store it with whole-sector 16-byte stores (rows >= M and columns >= N masked).
 __device__ __forceinline__ void store_chunk_staged(const uint32_t (&p)[16], uint32_t lane,

@@ -49,8 +49,17 @@ bool encode_tma_3d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, u
                    uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle);
 
 // Kernel launchers (one per translation unit).  Arguments are already validated.
+// allow_split = false keeps the one-CTA route to one pass (no K split, hence no scratch).
 cudaError_t launch_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, __half *C, int64_t ldc,
-                         const LaunchCtx &ctx, bool *encode_ok);
+                         const LaunchCtx &ctx, bool *encode_ok, bool allow_split = true);
+// Device scratch a launch_mxfp8 call (allow_split = true) takes from the pool, in bytes.
+size_t mxfp8_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B, int num_sms);
+// Split-K reduction: C[m, n] = fp16_rn( relu?( sum_{s = 0 .. splits-1, in order} P[s][m][n]
+// [+ C_old[m, n]] ) ) under ctx.epi, P holding `splits` planes of M rows x ldp floats (ldp a
+// multiple of 4, P 16-byte aligned).  Launched as a programmatic dependent of the GEMM that
+// writes P.
+cudaError_t launch_splitk_reduce(const float *P, int splits, int64_t ldp, int M, int N, __half *C,
+                                 int64_t ldc, const LaunchCtx &ctx);
 // CTA-pair MXFP8 path: scales are repacked into `scratch` (mxfp8_pair_scratch_bytes bytes,
 // 256-byte aligned device memory that stays untouched by anything else until the GEMM is done).
 bool mxfp8_pair_eligible(const qgemm_tensor *A, const qgemm_tensor *B);

@@ -15,8 +15,9 @@
  *   - All data, scale and output pointers are DEVICE pointers owned by the caller (host pointers
  *     for qgemm_mxfp8_host).  The library never frees or retains them; a qgemm_tensor only
  *     borrows pointers.  The device memory the library takes for itself is stated at each call
- *     that uses it: the scale scratch of the CTA-pair block-scaled GEMMs (from a per-device
- *     pool), the staging buffers of qgemm_mxfp8_host, the fixed array of qgemm_mxfp8_noalloc.
+ *     that uses it: the scale scratch of the CTA-pair block-scaled GEMMs and the fp32 partial
+ *     planes of a split K (both from a per-device pool), the attention workspace, the staging
+ *     buffers of qgemm_mxfp8_host, the fixed array of qgemm_mxfp8_noalloc.
  *   - Results are repeatable: the same inputs on the same GPU give the same output bits (every
  *     sum is taken in a fixed order, independent of timing).
  *   - Matrices are row-major with the reduction dimension K contiguous ("K-major"), except the
@@ -133,11 +134,28 @@ qgemm_status qgemm_tensor_info(const qgemm_tensor *t, int32_t *dtype, int64_t *r
  * ceil(K/128) * 512 bytes of device scratch taken from a library-owned per-device memory pool
  * with cudaMallocFromPoolAsync on `stream` and handed back with cudaFreeAsync on the same stream
  * after the GEMM (two kernel launches).  The pool keeps its memory between calls, so steady-state
- * calls do not reach the driver's allocator; it is released at process exit.
+ * calls do not reach the driver's allocator; it is released at process exit.  Otherwise (M or
+ * N <= 128) one CTA computes each 128 x 256 (128 x 128 for N <= 128) output tile; when there are
+ * at most half as many tiles as SMs, K is split: S = min(SMs / tiles, ceil(K / 512)) CTAs per
+ * tile each sum a range of whole 512-wide slices of K into an fp32 partial plane of pooled
+ * scratch (S * M * ceil(N / BN) * BN * 4 bytes, BN the tile width), and a second kernel adds the
+ * S planes in a fixed order and writes C (so the bits depend on S, which depends on the GPU's SM
+ * count, and remain repeatable).  qgemm_mxfp8_scratch_bytes tells how much a call takes.
  * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA
  * (including a failed scratch allocation). */
 qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, int64_t ldc,
                          void *stream);
+
+/* The device scratch one qgemm_mxfp8 call with these views takes from the library's pool on the
+ * current device, in bytes (0: none): the repacked scale planes on the CTA-pair route, or the
+ * fp32 partial planes of a K split on the one-CTA route (both described at qgemm_mxfp8).  No
+ * counterpart on the pages: it lets a caller that manages device memory itself leave room for the
+ * call (or take qgemm_mxfp8_noalloc).  Nothing is launched.
+ *   bytes  host pointer receiving the size.
+ * Errors: INVALID_ARG (NULL view or bytes, K mismatch), UNSUPPORTED_DTYPE (not E4M3 views), CUDA
+ * (the device cannot be queried). */
+qgemm_status qgemm_mxfp8_scratch_bytes(const qgemm_tensor *A, const qgemm_tensor *B,
+                                       int64_t *bytes);
 
 /* qgemm_mxfp8 without any device allocation.  The paper has no counterpart: this entry point
  * exists for callers that cannot let a library allocate device memory while they run -- a serving
@@ -147,7 +165,9 @@ qgemm_status qgemm_mxfp8(const qgemm_tensor *A, const qgemm_tensor *B, void *C, 
  * scratch for the repacked scale planes (M > 128 and N > 128), this call uses a fixed 8 MiB
  * device array compiled into the library instead (held, once placed, on each device until exit)
  * and makes no cudaMalloc, pool allocation or other allocating call.  M or N <= 128 runs the
- * one-CTA kernel of qgemm_mxfp8, which needs no scratch.
+ * one-CTA kernel of qgemm_mxfp8 in one pass over K, which needs no scratch; where qgemm_mxfp8
+ * splits K for such a shape the two calls sum in different orders, and their outputs can differ
+ * in the last bit (both within the same bound of the exact product).
  * Limits and rules:
  *   - a shape whose repacked scales need more than 8 MiB ((2 ceil(M/256) + 2 ceil(N/256)) *
  *     ceil(K/128) * 512 bytes, e.g. more than M = N = 16384 at K = 8192) is rejected with
@@ -207,7 +227,13 @@ qgemm_status qgemm_mxfp8_host(const qgemm_tensor *A, const qgemm_tensor *B, void
  * output cast on store).
  * Requirements: A, B, C 16-byte aligned; lda, ldb, ldc multiples of 8 elements; lda >= K,
  * ldb >= N, ldc >= N.  Any M, N, K >= 0 (ragged tiles masked; K == 0 writes zeros).
- * Errors: INVALID_ARG, MISALIGNED (nothing enqueued); CUDA. */
+ * Scratch: M > 128 and N > 128 run on CTA pairs and take none.  Otherwise one CTA computes each
+ * 128 x 256 (128 x 128 for N <= 128) tile, and when there are at most half as many tiles as SMs
+ * K is split as for qgemm_mxfp8: S = min(SMs / tiles, ceil(K / 512)) CTAs per tile write fp32
+ * partial planes into S * M * ceil(N / BN) * BN * 4 bytes taken from the library's pool on
+ * `stream` (and handed back after the reduction kernel that adds them in a fixed order).
+ * Errors: INVALID_ARG, MISALIGNED (nothing enqueued); CUDA (including a failed scratch
+ * allocation). */
 qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
                       int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream);
 

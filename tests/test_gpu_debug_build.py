@@ -62,6 +62,27 @@ for (M, N, K) in ((300, 520, 224), (100, 136, 224)):
     clean(f"mxfp8 {M}x{N}x{K}")
     close(f"mxfp8 {M}x{N}x{K}", C, oracle.mxfp8(d["a"].numpy(), d["sa"].numpy(),
                                                  d["b"].numpy(), d["sb"].numpy()))
+# fp16 one-CTA route with K split over CTAs (ragged last k-tile)
+df = synth.f16_inputs(64, 1000, 2080, seed=32)
+Cf = torch.empty(64, 1000, dtype=torch.float16, device=dev)
+q.gemm_f16(df["a"].to(dev), df["b"].to(dev), Cf)
+clean("fp16 split-K")
+close("fp16 split-K", Cf, oracle.gemm_f16(df["a"].numpy(), df["b"].numpy()))
+# MXFP8 one-CTA route with K split over CTAs (partial planes, then the ordered reduction), with a
+# K window that starts one scale byte in
+for (M, N, K, k0) in ((64, 1000, 2080, 0), (40, 520, 1024, 32)):
+    d = synth.mxfp8_inputs(M, N, K + k0, seed=M + K)
+    A = q.qgemm_create_tensor(q.E4M3, d["a"].to(dev), d["sa"].to(dev))
+    B = q.qgemm_create_tensor(q.E4M3, d["b"].to(dev), d["sb"].to(dev))
+    A, B = q.qgemm_tensor_slice(A, 0, M, k0, K), q.qgemm_tensor_slice(B, 0, N, k0, K)
+    assert q.qgemm_mxfp8_scratch_bytes(A, B) > 0, "meant to split K"
+    C = torch.empty(M, N, dtype=torch.float16, device=dev)
+    q.qgemm_mxfp8(A, B, C)
+    clean(f"mxfp8 split-K {M}x{N}x{K}")
+    kb = slice(k0 // 32, (k0 + K) // 32)
+    close(f"mxfp8 split-K {M}x{N}x{K}", C,
+          oracle.mxfp8(d["a"][:, k0:k0 + K].numpy(), d["sa"][:, kb].numpy(),
+                       d["b"][:, k0:k0 + K].numpy(), d["sb"][:, kb].numpy()))
 # attention: a CTA with a tail first and a head last; one unit over eight CTAs
 for (BH, Lq, Lk) in ((3, 200, 300), (1, 100, 4096)):
     d = synth.attention_inputs(BH, Lq, Lk, 128, seed=BH + Lk, q_std=2.0)

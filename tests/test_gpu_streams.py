@@ -23,7 +23,10 @@ def dev():
 
 
 def test_overlapping_calls_on_streams_match_serial_calls(dev):
+    # two CTA-pair calls (pooled scale scratch) and one small-M call whose K is split over CTAs
+    # (pooled partial planes)
     mx = [synth.mxfp8_inputs(1024, 768, 1024, seed=s, row_variance=True) for s in (1, 2)]
+    mx.append(synth.mxfp8_inputs(64, 768, 4096, seed=9, row_variance=True))
     f16 = synth.f16_inputs(768, 1024, 512, seed=3)
     w8 = synth.w8_inputs(9, 4096, 2048, seed=4)
     w4 = synth.w4a16_inputs(384, 512, 1024, seed=5)
@@ -49,12 +52,13 @@ def test_overlapping_calls_on_streams_match_serial_calls(dev):
     atd = [tuple(d[k].to(dev) for k in ("q", "k", "v")) + (d["scale"],) for d in at]
 
     def run(streams):
-        outs = [torch.empty(1024, 768, dtype=torch.float16, device=dev) for _ in mxv]
+        outs = [torch.empty(d["a"].shape[0], 768, dtype=torch.float16, device=dev) for d in mx]
         cf = torch.empty(768, 1024, dtype=torch.float16, device=dev)
         y8 = torch.empty(9, 4096, dtype=torch.float16, device=dev)
         c4 = torch.empty(384, 512, dtype=torch.float16, device=dev)
         ao = [torch.empty_like(t[0]) for t in atd]
-        calls = [lambda s, i=i: q.qgemm_mxfp8(mxv[i][0], mxv[i][1], outs[i], stream=s) for i in range(2)]
+        calls = [lambda s, i=i: q.qgemm_mxfp8(mxv[i][0], mxv[i][1], outs[i], stream=s)
+                 for i in range(len(mxv))]
         calls += [lambda s: q.gemm_f16(fa, fb, cf, stream=s),
                   lambda s: q.qgemm_w8_gemv(x8, W8, y8, stream=s),
                   lambda s: q.qgemm_w4a16(a4, W4, c4, stream=s)]
