@@ -21,13 +21,15 @@ pytestmark = pytest.mark.gpu
 REL = 2e-3
 
 # (name, M, N, K, scale-row padding in bytes): which kernel runs is decided by the shape and
-# the scale rows' alignment -- CTA pairs (M > 128, N > 128, K % 512 == 0, 16-byte scale rows),
-# the one-CTA TMA route (the same without M > 128), and the one-CTA cp.async route (K % 512 != 0)
+# the scale rows' alignment -- CTA pairs (N > 128, K % 512 == 0, 16-byte scale rows; any M, a
+# few tokens included), the one-CTA TMA route (the same with N <= 128), and the one-CTA cp.async
+# route (K % 512 != 0)
 # with 4-byte scale words or, for scale rows 21 bytes apart, byte loads.
 ROUTES = [
     ("pair", 300, 600, 1024, 0),
     ("pair_many_ctas", 1100, 600, 512, 0),
-    ("tma_one_cta", 128, 600, 1024, 0),
+    ("pair_few_tokens", 40, 600, 1024, 0),
+    ("tma_one_cta", 300, 120, 1024, 0),
     ("cp_async_word_scales", 200, 300, 640, 0),
     ("cp_async_byte_scales", 200, 300, 640, 1),
 ]
@@ -91,7 +93,7 @@ def test_w4a16_every_scale_byte(dev, orc, name, M, N, K, pad, accumulate, relu):
                 assert np.median(np.abs(ref[:, kind == k_])) > 1000 * 2.0 ** -24
 
 
-@pytest.mark.parametrize("name,M,N,K,pad", ROUTES[:3])
+@pytest.mark.parametrize("name,M,N,K,pad", ROUTES[:4])
 def test_w4a16_every_scale_byte_repeatable(dev, name, M, N, K, pad):
     """Outlier rows are summed in a fixed order: two calls give the same bits."""
     d, W, _sv = _inputs(M, N, K, pad, seed=5 * M + N, dev=dev)
