@@ -8,7 +8,9 @@
 //              boxes of B (64 k-rows x 64 n = 128 B), all with the 128-byte swizzle.
 //   warp 1     TMEM owner + MMA issuer: four 128 x BN x 16 MMAs per k-tile; B is described
 //              as MN-major (64-element swizzle atoms BN/64 apart, 8-row k groups 1 KB apart).
-//   warps 2-5  epilogue: TMEM -> fp16 -> global, masked at the M / N edges.
+//   warps 2-5  epilogue: TMEM -> fp16 -> global, masked at the M / N edges (or, when K is split
+//              over several CTAs because there are few tiles, TMEM -> an fp32 partial plane that
+//              splitk_reduce.cu adds in order).
 // Shapes with more than one 128-row and one 128-column block use the CTA-pair kernel below.
 #include "qgemm_common.cuh"
 #include "qgemm_debug.cuh"

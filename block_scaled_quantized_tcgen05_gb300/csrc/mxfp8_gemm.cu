@@ -7,7 +7,9 @@
 // sm_103a: the tensor core consumes the E4M3 planes and the UE8M0 planes directly
 // (tcgen05.mma kind::mxf8f6f4 with block_scale), so no dequantised copy ever exists.
 //
-// One persistent CTA per SM walks output tiles of 128 x BN (BN = 256, or 128 for narrow N).  Two
+// One persistent CTA per SM walks output tiles of 128 x BN (BN = 256, or 128 for narrow N); with
+// few tiles (M or N small: a decode-sized batch) its work items are (tile, k range) pairs, each
+// range's unrounded sum going to an fp32 partial plane that splitk_reduce.cu adds in order.  Two
 // TMEM accumulators are used when they fit beside the per-stage scale columns (BN = 128); at
 // BN = 256 the 512 TMEM columns hold one accumulator plus the scale slots.  Warp roles:
 //   warp 0     producer: TMA loads of the A / B k-tiles (128 B of K per row, 128-byte swizzle)
