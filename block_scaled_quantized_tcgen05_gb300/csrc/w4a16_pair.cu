@@ -46,6 +46,8 @@
 #include "qgemm_ptx.cuh"
 #include "w4a16_convert.cuh"
 
+#include <algorithm>
+
 namespace {
 
 using namespace qg;
@@ -58,6 +60,7 @@ constexpr int EPI_WARPS = 8;            // two per lane quarter, one per half of
 constexpr int CONV_WARP0 = 2 + EPI_WARPS;
 constexpr int CONV_WARPS = 8;           // two per lane quarter, alternate k-tiles
 constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
+constexpr int SPLIT_UNIT = 8;           // split-K ranges: whole 512-wide slices of K (8 k-tiles)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL0 = 256;        // weight slots after the 256-column accumulator
 constexpr uint32_t A_COLS = BK / 2;     // 32 columns per stage
@@ -93,16 +96,18 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
 }
 
 // SB: bytes per block scale (1: UE8M0 byte, 2: fp16).  lds is in bytes.
-template <int SB>
+template <int SB, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ CUtensorMap tmC, int c_tma,
                   const uint8_t *__restrict__ scales, int64_t lds,
                   const uint8_t *__restrict__ wdata, int64_t ldw, __half *__restrict__ C,
-                  int64_t ldc, int M, int N, int K, int epi, unsigned *err, uint64_t timeout_ns) {
+                  int64_t ldc, int M, int N, int K, int splits, float *__restrict__ P,
+                  int64_t ldp, int epi, unsigned *err, uint64_t timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
-    griddep_launch_dependents();   // the outlier-row pass may take the room this CTA leaves
+    // the split-K reduction or the outlier-row pass may take the room this CTA leaves
+    griddep_launch_dependents();
     const uint32_t sb = smem_u32(smem);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -123,8 +128,21 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int tiles_t = (M + BT - 1) / BT;
     const int num_tiles = tiles_w * tiles_t;
     const int KT = K / BK;
-    const int my_tiles = pair < num_tiles ? (num_tiles - pair + npairs - 1) / npairs : 0;
-    const int total = my_tiles * KT;
+    // work items (tile, k range): with splits > 1 each tile's K is cut into `splits` ranges of
+    // whole scale groups (SPLIT_UNIT k-tiles), each summed into its own fp32 partial plane
+    const int num_items = num_tiles * splits;
+    const int64_t plane = static_cast<int64_t>(M) * ldp;
+    // (the instance without a split compiles to whole tiles over all of K)
+    auto item_of = [&](int it, int &tile, int &split, int &kt0, int &kt1) {
+        if constexpr (SPLIT) {
+            split_item(it, num_tiles, splits, KT, SPLIT_UNIT, tile, split, kt0, kt1);
+        } else {
+            tile = it;
+            split = 0;
+            kt0 = 0;
+            kt1 = KT;
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -157,12 +175,13 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                int wb, tb;
+            for (int it = pair; it < num_items && ok; it += npairs) {
+                int tile, split, kt0, kt1, wb, tb;
+                item_of(it, tile, split, kt0, kt1);
                 tile_coords(tile, tiles_w, tiles_t, wb, tb);
                 const int w0 = wb * 2 * BW + static_cast<int>(rank) * BW;     // this CTA's weights
                 const int t0 = tb * BT + static_cast<int>(rank) * (BT / 2);   // this CTA's tokens
-                for (int kt = 0; kt < KT; ++kt) {
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!mbar_wait_warp(empty_bar(stage), phase ^ 1, timeout_ns)) {
                         ok = false;
                         break;
@@ -210,14 +229,16 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             const uint64_t bdesc0 = smem_desc(sb + OFF_X, 16, 1024, SWZ_128B);
             uint32_t acc_phase = 0, stage = 0, phase = 0;
             bool ok = true;
-            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+            for (int it = pair; it < num_items && ok; it += npairs) {
+                int tile, split, kt0, kt1;
+                item_of(it, tile, split, kt0, kt1);
                 if (!__all_sync(0xFFFFFFFFu,
                                 mbar_wait_cluster(tmem_empty, acc_phase ^ 1, timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int kt = 0; kt < KT; ++kt) {
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!mbar_wait_warp(full_bar(stage), phase, timeout_ns)) {
                         ok = false;
                         break;
@@ -226,7 +247,7 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     const uint32_t a_col = tmem_base + A_COL0 + stage * A_COLS;
                     const uint64_t bdesc = bdesc0 + stage * (X_BYTES >> 4);
                     if (elect_one()) {
-                        mma_f16_pair_ta(tmem_base, a_col, bdesc, IDESC, kt > 0 ? 1u : 0u);
+                        mma_f16_pair_ta(tmem_base, a_col, bdesc, IDESC, kt > kt0 ? 1u : 0u);
 #pragma unroll
                         for (uint32_t j = 1; j < BK / 16; ++j)
                             mma_f16_pair_ta(tmem_base, a_col + 8 * j, bdesc + 2 * j, IDESC, 1u);
@@ -260,41 +281,70 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         const uint32_t lead_full = map_to_cta(full_bar(0), 0);
         const int r = static_cast<int>(q * 32 + lane);
         constexpr int SPG = 8 / SB;              // k-tiles per 16-byte scale group
-        const int KG = KT / SPG;                 // 16-byte scale groups per weight row
-        // scale group cache: the group of (tile index ti, group g), and the next one prefetched
-        auto group_ptr = [&](int ti, int g) -> const uint8_t * {
-            const int tile = pair + ti * npairs;
-            if (tile >= num_tiles) return nullptr;
+        // this pair's work items in order (ti = 0, 1, ...): item pair + ti * npairs, whose
+        // k-tiles [kt0, kt1) hold whole scale groups kt0 / SPG .. kt1 / SPG - 1
+        auto item_range = [&](int ti, int &tile, int &kt0, int &kt1) -> bool {
+            const int it = pair + ti * npairs;
+            if (it >= num_items) return false;
+            int split;
+            item_of(it, tile, split, kt0, kt1);
+            return true;
+        };
+        int total = 0;                           // this pair's k-tiles over all its items
+        for (int ti = 0;; ++ti) {
+            int tile, a0, a1;
+            if (!item_range(ti, tile, a0, a1)) break;
+            total += a1 - a0;
+        }
+        // Scale group prefetch cursor: group nxt_g of item nxt_ti, whose groups end at nxt_g1
+        // and whose scale row for this lane starts at nxt_row (null past N or past the last
+        // item).  The item's tile and range are looked up once per item, not per group.
+        int nxt_ti = 0, nxt_g = 0, nxt_g1 = 0;
+        const uint8_t *nxt_row = nullptr;
+        auto load_item = [&](int ti) {
+            int tile, a0, a1;
+            nxt_ti = ti;
+            nxt_row = nullptr;
+            nxt_g = nxt_g1 = 0;
+            if (!item_range(ti, tile, a0, a1)) return;
             int wb, tb;
             tile_coords(tile, tiles_w, tiles_t, wb, tb);
             const int n = wb * 2 * BW + static_cast<int>(rank) * BW + r;
-            return n < N ? scales + static_cast<int64_t>(n) * lds + 16 * g : nullptr;
+            if (n < N) nxt_row = scales + static_cast<int64_t>(n) * lds;
+            nxt_g = a0 / SPG;
+            nxt_g1 = a1 / SPG;
         };
         // rows past N: scale 1 (their weights are TMA zero fill, so any finite scale gives 0)
         constexpr uint32_t ONE = SB == 1 ? 0x7F7F7F7Fu : 0x3C003C00u;
         const uint4 unit = make_uint4(ONE, ONE, ONE, ONE);
-        int cur_ti = 0, cur_g = 0;
-        const uint8_t *p0 = total > 0 ? group_ptr(0, 0) : nullptr;
-        uint4 cur = p0 ? ld_nc_v4(p0) : unit;
-        int nxt_ti = KG > 1 ? 0 : 1, nxt_g = KG > 1 ? 1 : 0;
-        const uint8_t *p1 = total > 0 ? group_ptr(nxt_ti, nxt_g) : nullptr;
-        uint4 nxt = p1 ? ld_nc_v4(p1) : unit;
-        // each warp walks only its own k-tiles, every other one (KT is a multiple of SPG >= 4, so
-        // both parities visit every scale group in order)
+        auto fetch = [&]() -> uint4 {
+            return nxt_row != nullptr && nxt_g < nxt_g1 ? ld_nc_v4(nxt_row + 16 * nxt_g) : unit;
+        };
+        auto advance = [&]() {
+            if (++nxt_g >= nxt_g1) load_item(nxt_ti + 1);
+        };
+        load_item(0);
+        int cur_ti = nxt_ti, cur_g = nxt_g;
+        uint4 cur = total > 0 ? fetch() : unit;
+        advance();
+        uint4 nxt = total > 0 ? fetch() : unit;
+        // each warp walks only its own k-tiles, every other one (an item's k-tiles are whole
+        // scale groups of SPG >= 4, an even count, so both parities visit every group in order)
         uint32_t stage = static_cast<uint32_t>(parity), phase = 0;
-        int ti = 0, kt = parity;
+        int ti = 0, it_kt0, it_kt1;
+        {
+            int tile;
+            if (!item_range(0, tile, it_kt0, it_kt1)) it_kt0 = it_kt1 = 0;
+        }
+        int kt = it_kt0 + parity;
         for (int it = parity; it < total; it += 2) {
             const int g = kt / SPG;
             if (ti != cur_ti || g != cur_g) {    // move to the next scale group, prefetch one more
                 cur = nxt;
                 cur_ti = nxt_ti;
                 cur_g = nxt_g;
-                if (++nxt_g == KG) {
-                    nxt_g = 0;
-                    ++nxt_ti;
-                }
-                const uint8_t *pn = group_ptr(nxt_ti, nxt_g);
-                nxt = pn ? ld_nc_v4(pn) : unit;
+                advance();
+                nxt = fetch();
             }
             if (!mbar_wait(raw_full(stage), phase, timeout_ns)) {
                 if (lane == 0) atomicOr(err, ERR_PRODUCER);
@@ -364,9 +414,12 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 stage -= STAGES;
                 phase ^= 1;
             }
-            if ((kt += 2) >= KT) {
-                kt -= KT;
+            if ((kt += 2) >= it_kt1) {           // on to this warp's first k-tile of the next item
+                const int over = kt - it_kt1;
                 ++ti;
+                int tile;
+                if (!item_range(ti, tile, it_kt0, it_kt1)) it_kt0 = it_kt1 = 0;
+                kt = it_kt0 + over;
             }
         }
     } else {
@@ -377,8 +430,9 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         const uint32_t half = (warp - 2) >> 2;
         const uint32_t lead_empty = map_to_cta(tmem_empty, 0);
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < num_tiles; tile += npairs) {
-            int wb, tb;
+        for (int it = pair; it < num_items; it += npairs) {
+            int tile, split, kt0, kt1, wb, tb;
+            item_of(it, tile, split, kt0, kt1);
             tile_coords(tile, tiles_w, tiles_t, wb, tb);
             const int n0 = wb * 2 * BW + static_cast<int>(rank) * BW + static_cast<int>(q * 32);
             const int n = n0 + static_cast<int>(lane);
@@ -396,6 +450,31 @@ w4a16_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             }
             tc_fence_after();
             const int m0 = tb * BT + static_cast<int>(half) * (BT / 2);
+            if constexpr (SPLIT) {
+                // this k range's unrounded sums into its partial plane, [token][weight row]:
+                // lane = weight row, so each store writes 32 consecutive floats of a token row
+                float *pl = P + split * plane;
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + half * (BT / 2) + ch * 32, v);
+                    tmem_wait_ld();
+                    if (ch == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_relaxed_cluster(lead_empty);
+                    }
+                    if (n < N) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int m = m0 + ch * 32 + c;
+                            if (m < M) pl[static_cast<int64_t>(m) * ldp + n] = __uint_as_float(v[c]);
+                        }
+                    }
+                }
+                acc_phase ^= 1;
+                continue;
+            }
             const uint32_t stg = sb + OFF_EPI + (warp - 2) * EPI_BYTES;
             if (c_tma) {   // the previous tile's stores have finished reading the staging
                 if (lane == 0) bulk_wait_read<0>();
@@ -515,16 +594,42 @@ cudaError_t launch_pair_impl(const __half *A, int64_t lda, int M, const qgemm_te
     } else {
         tmC = tmX;   // unused
     }
-    cudaError_t e = cudaFuncSetAttribute(w4a16_pair_kernel<SB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int tiles = ((N + 2 * BW - 1) / (2 * BW)) * ((M + BT - 1) / BT);
-    int pairs = ctx.num_sms / 2;
-    if (pairs > tiles) pairs = tiles;
-    w4a16_pair_kernel<SB><<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
-        tmX, tmW, tmC, c_tma, W->scales, W->lds, W->data, W->ld, C, ldc, M, N, K, ctx.epi,
-        ctx.err, ctx.timeout_ns);
-    return cudaGetLastError();
+    cudaError_t e;
+    const int tiles_w = (N + 2 * BW - 1) / (2 * BW);
+    const int tiles = tiles_w * ((M + BT - 1) / BT);
+    // A few tokens against many weight rows leave most pairs idle: when the tiles fill at most
+    // half of the pairs, each tile's K is split over up to pairs / tiles pairs (whole 512-wide
+    // slices), their fp32 partial planes added in order by splitk_reduce.cu.  Not when the
+    // output is accumulated: the outlier-row pass then needs the old C of its columns, which
+    // the reduction would overwrite.
+    const int avail = ctx.num_sms / 2;
+    int splits = 1;
+    if (!(ctx.epi & qgi::EPI_ACCUMULATE) && 2 * tiles <= avail)
+        splits = std::min(avail / tiles, (K / BK) / SPLIT_UNIT);
+    if (splits < 1) splits = 1;
+    const int64_t ldp = static_cast<int64_t>(tiles_w) * 2 * BW;
+    void *ws = nullptr;
+    if (splits > 1) {
+        e = qgi::scratch_alloc(static_cast<size_t>(splits) * static_cast<size_t>(M) *
+                                   static_cast<size_t>(ldp) * sizeof(float),
+                               ctx, &ws);
+        if (e != cudaSuccess) return e;
+    }
+    float *P = static_cast<float *>(ws);
+    const int items = tiles * splits;
+    int pairs = avail;
+    if (pairs > items) pairs = items;
+    auto kern = splits > 1 ? w4a16_pair_kernel<SB, true> : w4a16_pair_kernel<SB, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess) {
+        kern<<<2 * pairs, THREADS, SMEM_BYTES, ctx.stream>>>(
+            tmX, tmW, tmC, c_tma, W->scales, W->lds, W->data, W->ld, C, ldc, M, N, K, splits, P, ldp,
+            ctx.epi, ctx.err, ctx.timeout_ns);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess && splits > 1) e = qgi::launch_splitk_reduce(P, splits, ldp, M, N, C, ldc, ctx);
+    const cudaError_t f = qgi::scratch_free(ws, ctx);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace

@@ -1,4 +1,5 @@
-"""Split-K on the one-CTA MXFP8 and fp16 routes, through the C ABI.
+"""Split-K for decode-sized batches: the one-CTA MXFP8 and fp16 routes and the W4A16 CTA pairs,
+through the C ABI.
 
 An output of at most 128 rows on one side has few 128 x 256 tiles; when there are at most half as
 many tiles as SMs, each tile's k range is shared out over S CTAs (whole 512-wide slices of K),
@@ -167,3 +168,48 @@ def test_f16_split_k_epilogue(dev, orc, accumulate, relu):
     q.gemm_f16_ex(d["a"].to(dev), d["b"].to(dev), C, accumulate=accumulate, relu=relu)
     _check(C, orc.epilogue(res, old.numpy() if accumulate else None, relu), orc,
            f"fp16 split-K epilogue acc={accumulate} relu={relu}")
+
+
+# ---------------------------------------------------------------- W4A16 on CTA pairs, few tokens
+# A few tokens against many weight rows fill few pair tiles; each tile's K is then split over up to
+# pairs / tiles pairs (whole 512-wide slices), the partial planes added in order, and the outlier-row
+# pass runs after that reduction.  Accumulating calls are not split (that pass needs the old C).
+@pytest.mark.parametrize("M,N,K", [(64, 4096, 4096), (1, 1024, 2048), (100, 1000, 1024)])
+def test_w4a16_split_k_matches_oracle(dev, orc, M, N, K):
+    d = synth.w4a16_inputs(M, N, K, seed=M + N + K)
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
+    a = d["a"].to(dev)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_w4a16(a, W, C)
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    _check(C, res, orc, f"w4a16 split-K {M}x{N}x{K}")
+    C2 = torch.empty_like(C)
+    q.qgemm_w4a16(a, W, C2)
+    torch.cuda.synchronize()
+    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
+
+
+@pytest.mark.parametrize("accumulate,relu", [(False, False), (False, True), (True, True)])
+def test_w4a16_split_k_every_scale_byte(dev, orc, accumulate, relu):
+    """Every UE8M0 byte class, outlier rows included, on a 40-token batch (split unless the
+    output is accumulated)."""
+    M, N, K = 40, 600, 2048
+    d = synth.w4a16_scale_extremes_inputs(M, N, K, seed=77)
+    W = q.qgemm_create_tensor(q.INT4, d["w"].to(dev), d["sw"].to(dev))
+    res = orc.w4a16(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy())
+    old = (torch.randn((M, N), generator=synth.generator(8)) * 4).to(torch.float16)
+    C = old.to(dev) if accumulate else torch.full((M, N), float("nan"), dtype=torch.float16,
+                                                  device=dev)
+    q.qgemm_w4a16_ex(d["a"].to(dev), W, C, accumulate=accumulate, relu=relu)
+    if accumulate or relu:
+        res = orc.epilogue(res, old.numpy() if accumulate else None, relu=relu)
+    _check(C, res, orc, f"w4a16 split-K extremes acc={accumulate} relu={relu}")
+
+
+def test_w4a16_f16s_split_k(dev, orc):
+    M, N, K = 64, 1024, 2048
+    d = synth.w4a16_f16s_inputs(M, N, K, seed=9)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    q.qgemm_w4a16_f16s(d["a"].to(dev), d["w"].to(dev), d["sw"].to(dev), C)
+    _check(C, orc.w4a16_f16s(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy()), orc,
+           "w4a16 fp16 scales split-K")
