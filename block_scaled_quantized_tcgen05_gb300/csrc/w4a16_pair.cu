@@ -30,7 +30,9 @@
 // stage on its full barrier, which collects both CTAs' activation bytes and one relaxed arrival
 // from each converter warp of both CTAs after its tcgen05.st completed; commits are multicast;
 // every wait is bounded.  Used for K % 512 == 0 with 16-byte aligned scale rows (scales are read
-// 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.  Scale bytes outside the
+// 16 bytes = 8 k-tiles at a time); other shapes take w4a16_gemm.cu.  With few tiles (a few tokens
+// against many weight rows) and no accumulation, the SPLIT instance cuts each tile's K into whole
+// 512-wide slices over several pairs, which write fp32 partial planes for splitk_reduce.cu.  Scale bytes outside the
 // fold window convert to zero weights (w4a16_convert.cuh); when the output is accumulated, the
 // columns of outlier rows are left to w4a16_outlier.cu, which runs next and needs the old C.
 //
