@@ -206,10 +206,11 @@ def test_w4a16_split_k_every_scale_byte(dev, orc, accumulate, relu):
     _check(C, res, orc, f"w4a16 split-K extremes acc={accumulate} relu={relu}")
 
 
-def test_w4a16_f16s_split_k(dev, orc):
-    M, N, K = 64, 1024, 2048
-    d = synth.w4a16_f16s_inputs(M, N, K, seed=9)
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 2048), (40, 1000, 2304)])
+def test_w4a16_f16s_split_k(dev, orc, M, N, K):
+    """fp16 scales (4 k-tiles per scale group): K = 2304 leaves a last slice of four k-tiles."""
+    d = synth.w4a16_f16s_inputs(M, N, K, seed=9 + K)
     C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
     q.qgemm_w4a16_f16s(d["a"].to(dev), d["w"].to(dev), d["sw"].to(dev), C)
     _check(C, orc.w4a16_f16s(d["a"].numpy(), d["w"].numpy(), d["sw"].numpy()), orc,
-           "w4a16 fp16 scales split-K")
+           f"w4a16 fp16 scales split-K {M}x{N}x{K}")
