@@ -253,9 +253,16 @@ qgemm_status gemm_f16(const void *A, int64_t lda, const void *B, int64_t ldb, vo
  * times its 2^(e - 127) and summed in fp64, one fp16 rounding (with the epilogue of the _ex call
  * applied to that sum).  Outlier rows cost M * K fused multiply-adds each on the CUDA cores; the
  * second kernel is launched by every call and, with no outlier row, only reads the scale plane.
+ * Scratch: with N > 128, K % 512 == 0 and 16-byte aligned scale rows the product runs on CTA
+ * pairs (256 weight rows x 256 tokens per pair tile); when the tiles fill at most half of the
+ * pairs (a few tokens against many weight rows) and C is not accumulated (qgemm_w4a16_ex), each
+ * tile's K is split in whole 512-wide slices over S = min(pairs / tiles, K / 512) pairs, whose
+ * fp32 partial planes (S * M * ceil(N / 256) * 256 * 4 bytes, from the library's pool on
+ * `stream`) a reduction kernel adds in a fixed order before the outlier-row kernel runs.
  * Requirements: K % 64 == 0; A, C 16-byte aligned; lda, ldc multiples of 8; W data 16-byte
  * aligned with a 16-byte multiple row stride; any M, N.
- * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA. */
+ * Errors: INVALID_ARG, UNSUPPORTED_DTYPE, UNSUPPORTED_SHAPE, MISALIGNED; CUDA (including a
+ * failed scratch allocation). */
 qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_tensor *W,
                          void *C_f16, int64_t ldc, void *stream);
 
@@ -277,8 +284,11 @@ qgemm_status qgemm_w4a16(const void *A_f16, int64_t lda, int64_t M, const qgemm_
  * Requirements: K % 256 == 0; A 16-byte aligned with lda % 8 == 0; W 16-byte aligned with
  * ldw_bytes % 16 == 0; scales 16-byte aligned with lds % 8 == 0; C 2-byte aligned (16-byte
  * aligned C with ldc % 8 == 0 takes TMA stores); any M, N >= 0 (ragged tiles masked; K == 0
- * writes zeros).  Runs on CTA pairs for every shape.
- * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA. */
+ * writes zeros).  Runs on CTA pairs for every shape, with K split over several pairs as for
+ * qgemm_w4a16 when the tiles fill at most half of them and C is not accumulated (pooled fp32
+ * partial planes, reduced in a fixed order).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (nothing enqueued); CUDA (including a
+ * failed scratch allocation). */
 qgemm_status qgemm_w4a16_f16s(const void *A_f16, int64_t lda, int64_t M, const void *W_int4,
                               int64_t ldw_bytes, const void *scales_f16, int64_t lds, int64_t N,
                               int64_t K, void *C_f16, int64_t ldc, void *stream);
