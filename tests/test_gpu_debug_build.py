@@ -83,6 +83,13 @@ for (M, N, K, k0) in ((64, 1000, 2080, 0), (40, 520, 1024, 32)):
     close(f"mxfp8 split-K {M}x{N}x{K}", C,
           oracle.mxfp8(d["a"][:, k0:k0 + K].numpy(), d["sa"][:, kb].numpy(),
                        d["b"][:, k0:k0 + K].numpy(), d["sb"][:, kb].numpy()))
+# W4A16 on CTA pairs with K split over four pairs (few tokens), outlier rows included
+dw = synth.w4a16_scale_extremes_inputs(40, 1000, 2048, seed=34)
+Ww = q.qgemm_create_tensor(q.INT4, dw["w"].to(dev), dw["sw"].to(dev))
+Cw = torch.empty(40, 1000, dtype=torch.float16, device=dev)
+q.qgemm_w4a16(dw["a"].to(dev), Ww, Cw)
+clean("w4a16 split-K")
+close("w4a16 split-K", Cw, oracle.w4a16(dw["a"].numpy(), dw["w"].numpy(), dw["sw"].numpy()))
 # attention: a CTA with a tail first and a head last; one unit over eight CTAs
 for (BH, Lq, Lk) in ((3, 200, 300), (1, 100, 4096)):
     d = synth.attention_inputs(BH, Lq, Lk, 128, seed=BH + Lk, q_std=2.0)
